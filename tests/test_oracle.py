@@ -1,0 +1,120 @@
+"""CPU tests of the oracle against its pins, and of the pins against planted mistakes."""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle_pins as pins
+from kv_cache_decode_06_b300.inputs import (
+    CONFIGS, T5XXL_SWEEP_GS, bf16_bits_to_f32, f32_to_bf16_bits, make_decode_inputs,
+)
+
+
+@pytest.mark.parametrize("check", pins.DECODE_CHECKS + pins.MEANPOOL_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_pin(check, oracle_lib):
+    check(oracle_lib)
+
+
+def test_group_map_is_contiguous_blocks(oracle_lib):
+    for H, G in ((8, 2), (32, 8), (64, 1), (64, 64), (12, 3)):
+        assert [oracle.group_of(i, H, G, lib=oracle_lib) for i in range(H)] == [i // (H // G) for i in range(H)]
+
+
+def test_oracle_rejects_bad_arguments(oracle_lib):
+    inp = make_decode_inputs(CONFIGS["tiny"])
+    with pytest.raises(ValueError):   # H % G != 0
+        oracle.gqa_decode_f64(inp.q[:, :7], inp.k, inp.v, inp.seq_lens, inp.scale, lib=oracle_lib)
+    with pytest.raises(ValueError):   # seq_len > Lmax
+        oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens + 1, inp.scale, lib=oracle_lib)
+
+
+# ------------------------------------------------------------ planted mistakes
+# Each mutant edits one expression in a copy of the oracle source; at least one
+# pin must then fail.  The mutants are compiled into a temporary directory and
+# never replace the real oracle.
+
+MUTANTS = {
+    "group_map_modulo": ("return i / (H / G);", "return i % G;"),
+    "scale_dropped": ("s[t] = sc * dot;", "s[t] = dot;"),
+    "k_and_v_swapped": ("acc += s[t] * bf16_value(vg[(int64_t)t * d + j]);",
+                        "acc += s[t] * bf16_value(kg[(int64_t)t * d + j]);"),
+    "one_past_the_end": ("const int T = seq_lens[b];",
+                         "const int T = seq_lens[b] < Lmax ? seq_lens[b] + 1 : seq_lens[b];"),
+    "normaliser_missing": ("o[j] = acc / l;", "o[j] = acc;"),
+    "exp_of_unshifted_sum": ("l += s[t];", "l += s[t] * s[t];"),
+    "meanpool_divides_by_H": ("out[(o * G + g) * inner + x] = acc / (float)n;",
+                              "out[(o * G + g) * inner + x] = acc / (float)H;"),
+    "meanpool_drops_last_member": ("for (int j = 1; j < n; ++j)\n                    acc = acc + w",
+                                   "for (int j = 1; j < n - 1; ++j)\n                    acc = acc + w"),
+}
+
+
+@pytest.fixture(scope="module")
+def mutant_dir(tmp_path_factory):
+    return tmp_path_factory.mktemp("oracle_mutants")
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, mutant_dir):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "gqa_oracle.c")).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) >= 1, f"mutant pattern not found: {old!r}"
+    mpath = mutant_dir / f"{name}.c"
+    mpath.write_text(src.replace(old, new, 1))
+    so = mutant_dir / f"lib{name}.so"
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", str(so), str(mpath), "-lm"], check=True)
+    lib = oracle.load(str(so))
+    checks = pins.MEANPOOL_CHECKS if name.startswith("meanpool") else pins.DECODE_CHECKS
+    failed = []
+    for check in checks:
+        try:
+            check(lib)
+        except (AssertionError, ValueError):
+            failed.append(check.__name__)
+    assert failed, f"no pin caught mutant {name}"
+
+
+# ------------------------------------------------------------- input recipe
+
+def test_bf16_rounding_is_nearest_even():
+    x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -9, -2.5, 3.14159], dtype=np.float32)
+    got = bf16_bits_to_f32(f32_to_bf16_bits(x))
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: even mantissa wins (1.0)
+    assert got[1] == np.float32(1.0)
+    assert got[2] == np.float32(1.0 + 2 ** -6)
+    assert got[0] == 1.0 and got[4] == -2.5
+    assert abs(float(got[5]) - 3.14159) <= 2 ** -7 * 4
+
+
+def test_inputs_are_seeded_and_shaped():
+    a = make_decode_inputs(CONFIGS["tiny"])
+    b = make_decode_inputs(CONFIGS["tiny"])
+    assert np.array_equal(a.q, b.q) and np.array_equal(a.k, b.k)
+    assert a.q.shape == (1, 8, 64) and a.k.shape == (1, 2, 128, 64) and a.seq_lens.tolist() == [128]
+    m = CONFIGS["mistral7b"]
+    from kv_cache_decode_06_b300.inputs import draw_seq_lens
+    sl = draw_seq_lens(m)
+    assert sl.shape == (16,) and sl.min() >= 1024 and sl.max() <= 4096
+    for G in T5XXL_SWEEP_GS:
+        c = CONFIGS["t5xxl_sweep"].with_G(G)
+        assert c.H % c.G == 0
+
+
+def test_outlier_keys_are_scaled_by_four():
+    c = CONFIGS["llama3_70b"].with_(B=2, Lmax=4096, seq_lo=4096, seq_hi=4096)
+    inp = make_decode_inputs(c)
+    k = bf16_bits_to_f32(inp.k)
+    rms = np.sqrt((k.astype(np.float64) ** 2).mean(axis=(1, 3)))   # [B, T]
+    big = rms > 2.5
+    frac = big.mean()
+    assert 0.003 < frac < 0.03
+    assert np.all(rms[big] > 3.0)
+
+
+@pytest.mark.slow
+def test_oracle_tiny_config_runs(oracle_lib):
+    inp = make_decode_inputs(CONFIGS["tiny"])
+    out = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale, lib=oracle_lib)
+    assert np.isfinite(out).all() and out.shape == (1, 8, 64)
