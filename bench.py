@@ -1,0 +1,365 @@
+"""Benchmark of one GQA decode step (KV-cache HBM GB/s and decode steps/s).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one gqa_decode call on the workload's whole batch (one layer), with
+the bf16 KV cache resident in HBM.  GB/s counts algorithmic bytes only: the
+valid K and V rows, sum_b seq_lens[b] * G * d * 2 bytes * 2.  L2 is flushed
+(a 256 MiB write) before every timed step, outside the timed events.  The step
+time is measured with CUDA events on the launching stream; the step is a single
+kernel launch, so the same events time the dominant kernel.
+
+Under torchrun (N > 1) every rank runs an independent replica of the step on
+its own GPU (nothing is sharded); value = bytes of all ranks / max time.
+
+``--impl reference`` times the float64 CPU oracle on the host cores instead, on
+a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from kv_cache_decode_06_b300.inputs import CONFIGS, T5XXL_SWEEP_GS, make_decode_inputs  # noqa: E402
+
+METRIC = "GQA decode KV-cache HBM GB/s (% of B300 peak) and decode steps/s, 1 GPU"
+UNIT = "GB/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6400.0
+
+
+def workload(name: str):
+    if name.startswith("t5xxl_sweep_G"):
+        return CONFIGS["t5xxl_sweep"].with_G(int(name.split("_G")[1]))
+    return CONFIGS[name]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kv_cache_decode_06_b300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, wl: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{wl}.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)\s+source_hash:\s*([0-9a-f]+)", txt)
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, smax = [], []
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_step(inp, segments, threads=None):
+    """Time the float64 oracle on the rows of the given (b, g) segments; returns (seconds, kv bytes)."""
+    import oracle
+    cfg = inp.cfg
+    rows = np.array([b * cfg.H + g * cfg.n + h for (b, g) in segments for h in range(cfg.n)], dtype=np.int64)
+    kv = sum(int(inp.seq_lens[b]) for (b, _) in segments) * cfg.d * 2 * 2
+    t0 = time.perf_counter()
+    oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale, rows=rows)
+    return time.perf_counter() - t0, kv
+
+
+def all_segments(cfg):
+    return [(b, g) for b in range(cfg.B) for g in range(cfg.G)]
+
+
+def run_reference(args, rank: int) -> None:
+    """The float64 CPU oracle as the reference arm, rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    cfg = workload(args.workload)
+    inp = make_decode_inputs(cfg, poison_tail=False)
+    segs = all_segments(cfg)
+    cores = oracle.num_threads()
+    # calibrate: seconds per segment on this host
+    t, _ = cpu_oracle_step(inp, segs[:1])
+    per_seg = max(t, 1e-4)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    nseg = int(max(1, min(len(segs), budget / per_seg)))
+    for i in range(args.warmup):
+        cpu_oracle_step(inp, [segs[(i * nseg + k) % len(segs)] for k in range(nseg)])
+    total_t, total_b = 0.0, 0
+    for i in range(args.steps):
+        sel = [segs[(i * nseg + k) % len(segs)] for k in range(nseg)]
+        t, b = cpu_oracle_step(inp, sel)
+        total_t += t
+        total_b += b
+    value = total_b / total_t / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": config_dict(cfg, inp, extra={"sample_segments_per_step": nseg}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{nseg} of {len(segs)} (batch, K/V head) segments per step, all H/G heads "
+                                   f"of each, float64 oracle (OpenMP over rows)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(cfg, inp, extra=None):
+    d = {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "G": cfg.G, "d": cfg.d, "Lmax": cfg.Lmax,
+         "seq_lens": (list(cfg.fixed_seq) if cfg.fixed_seq else f"U[{cfg.seq_lo},{cfg.seq_hi}] seeded"),
+         "kv_bytes_per_step": inp.kv_bytes, "inputs": "N(0,1) -> bf16, seeded",
+         "l2": "flushed before every timed step (256 MiB write, outside the timed events)"}
+    if extra:
+        d.update(extra)
+    return d
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="mistral7b",
+                    help="mistral7b | llama3_70b | long_ragged | tiny | t5xxl_sweep_G<1..64>")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", type=int, default=0, help="0 auto, 1 simt, 2 tcgen05")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from kv_cache_decode_06_b300 import build_lib, gqa
+
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    build_lib.build()
+    gqa.load()
+
+    cfg = workload(args.workload)
+    inp = make_decode_inputs(cfg, poison_tail=False)
+    q = torch.from_numpy(inp.q).view(torch.bfloat16).to(dev)
+    k = torch.from_numpy(inp.k).view(torch.bfloat16).to(dev)
+    v = torch.from_numpy(inp.v).view(torch.bfloat16).to(dev)
+    sl = torch.from_numpy(inp.seq_lens).to(dev)
+    out = torch.empty((cfg.B, cfg.H, cfg.d), dtype=torch.float32, device=dev)
+    ws = gqa.alloc_workspace(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scale = float(inp.scale)
+    path = args.path or gqa.select_path(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax)
+
+    def step():
+        gqa.decode(q, k, v, sl, out=out, workspace=ws, scale=scale, stream=stream, path=path)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    durs = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = float(sum(durs))
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * inp.kv_bytes * args.steps / (total_ms / 1e3) / 1e9
+    flags = gqa.read_flags(ws)
+    if flags:
+        raise RuntimeError(f"decode reported flags 0x{flags:x} during the benchmark")
+
+    # ---- end to end through the public API with host buffers (pinned)
+    hq = torch.from_numpy(inp.q).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(inp.k).view(torch.bfloat16).pin_memory()
+    hv = torch.from_numpy(inp.v).view(torch.bfloat16).pin_memory()
+    hsl = torch.from_numpy(inp.seq_lens).pin_memory()
+    hout = torch.empty((cfg.B, cfg.H, cfg.d), dtype=torch.float32).pin_memory()
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hsl.numel() * 4
+    d2h = hout.numel() * 4
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        sl.copy_(hsl, non_blocking=True)
+        gqa.decode(q, k, v, sl, out=out, workspace=ws, scale=scale, stream=stream, path=path)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    e2e_value = world * inp.kv_bytes / (e2e_ms / 1e3) / 1e9
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_value = world * inp.kv_bytes / (float(t.item()) / 1e3) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peak()
+    kernel = "gqa_decode_tc_kernel" if path == gqa.PATH_TCGEN05 else "gqa_decode_simt_kernel"
+    achieved = inp.kv_bytes / (ms_per_step / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profiled_traffic(kernel, cfg.name), "kernel": kernel,
+                "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+                "algorithmic_bytes_per_launch": inp.kv_bytes,
+                "frac_of_8TBps_nominal": achieved / 8000.0}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        segs = all_segments(cfg)
+        t, b = cpu_oracle_step(inp, segs[:1])
+        nseg = int(max(1, min(len(segs), 15.0 / max(t, 1e-4))))
+        t, b = cpu_oracle_step(inp, segs[:nseg])
+        cpu = {"value": b / t / 1e9, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{nseg} of {len(segs)} (batch, K/V head) segments, all H/G query heads each, "
+                         f"float64 oracle, {t:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if path == gqa.PATH_TCGEN05 else "f32", "data": "synthetic",
+        "steps_per_s": world * 1e3 / ms_per_step,
+        "config": config_dict(cfg, inp, extra={"path": "tcgen05" if path == gqa.PATH_TCGEN05 else "simt",
+                                               "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": args.e2e_steps,
+                "what": "H2D of q, k_cache, v_cache (whole buffers), seq_lens from pinned host memory + "
+                        "gqa.decode + D2H of out, per step"},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+/*
+ * gqa.h — C ABI of the B300 (sm_103a) grouped-query attention decode library.
+ *
+ * Grouped-query attention (GQA): the H query heads are split into G groups and
+ * every query head of group g attends with that group's single key head and
+ * value head, so the KV cache holds G instead of H K/V heads per token.
+ * G = 1 is multi-query attention, G = H is multi-head attention.
+ * ["Grouped-query attention (GQA)" concept page, "Overview" and "Choosing the
+ *  group count G"; arxiv:2305.13245 §2.2]
+ *
+ * Conventions shared by every entry point:
+ *   - G counts K/V heads, as in the GQA paper (GQA-8 has 8 K/V heads).  It is
+ *     not Gemma 2's `num_groups` (query heads per K/V head).  [same page,
+ *     "Contradictions"]
+ *   - Query head i belongs to group g(i) = i / (H/G) (contiguous blocks; the
+ *     paper leaves the map open and the page's conversion sketch assumes
+ *     blocks).
+ *   - Device pointers are CUDA global-memory addresses on the current device.
+ *     bf16 tensors are passed as `const void*` holding IEEE bfloat16 values.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *     only enqueues work on `stream` and never synchronises; results are ready
+ *     when the stream reaches that point.
+ *   - The library never allocates device memory and keeps no per-call state on
+ *     the host.  The caller owns every buffer.
+ *   - Host-checkable errors return before anything is enqueued.  A failed
+ *     launch returns GQA_ERR_LAUNCH.
+ *   - Thread safety: calls from several host threads are safe; two calls that
+ *     share a workspace must not overlap on the device.
+ */
+#ifndef GQA_B300_GQA_H
+#define GQA_B300_GQA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQA_ABI_VERSION 1
+
+typedef enum gqa_status {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, H % G != 0, bad stride */
+    GQA_ERR_UNSUPPORTED = 2,   /* valid but not built: head dim, H/G, batch or size limits */
+    GQA_ERR_WORKSPACE = 3,     /* workspace null or smaller than gqa_decode_workspace_size() */
+    GQA_ERR_LAUNCH = 4,        /* a CUDA call or kernel launch failed */
+    GQA_ERR_DEVICE = 5         /* no usable CUDA device, or not an sm_103 device */
+} gqa_status;
+
+/* Bits the decode kernel ORs into the workspace's flag word (see gqa_decode_read_flags). */
+#define GQA_FLAG_SEQ_LEN_CLAMPED 0x1u  /* some seq_lens[b] was < 0 or > Lmax; it was clamped */
+#define GQA_FLAG_WAIT_TIMEOUT    0x2u  /* a pipeline wait ran out; that call's output is invalid */
+
+/* Kernel variants of gqa_decode_ex. */
+#define GQA_PATH_AUTO    0   /* pick per shape (the default of gqa_decode) */
+#define GQA_PATH_SIMT    1   /* CUDA-core dot products and online softmax, H/G <= 8 */
+#define GQA_PATH_TCGEN05 2   /* fifth-generation tensor cores (tcgen05, TMEM), H/G <= 64 */
+
+/* Limits of this build. */
+#define GQA_MAX_BATCH 1024
+#define GQA_MAX_CTAS 1024
+
+/* Human-readable name of a status code.  Never NULL. */
+const char *gqa_status_string(int status);
+
+/* GQA_ABI_VERSION of the loaded library. */
+int gqa_abi_version(void);
+
+/*
+ * Bytes of device workspace gqa_decode needs for this shape.  The value does not
+ * depend on seq_lens or on the device.  Writes *bytes and returns GQA_OK, or
+ * returns the status gqa_decode would return for the same shape.
+ *
+ * The workspace holds split-combine partial results (one (m, l, acc) triple per
+ * query head per piece of a sequence), one arrival counter per (batch, K/V head)
+ * and one flag word.  It MUST be zero-filled before its first use (for example
+ * cudaMemsetAsync(ws, 0, bytes, stream)).  Every completed gqa_decode call
+ * leaves the counters at zero again, so later calls with the same B and G need
+ * no reset; before a call with another (B, G), zero it again (the counters sit
+ * at a shape-dependent offset).  The flag word is only ever OR-ed into.
+ */
+gqa_status gqa_decode_workspace_size(int B, int H, int G, int d, int Lmax, size_t *bytes);
+
+/*
+ * One GQA decode step over a bf16 KV cache.
+ * ["Grouped-query attention (GQA)" concept page, "Implementation sketch", the
+ *  decode-step pseudocode; arxiv:2305.13245 §2.2]
+ *
+ * For every sequence b and query head i, with g = i / (H/G) and
+ * T = seq_lens[b]:
+ *   s_t        = scale * sum_j q[b,i,j] * k_cache[b,g,t,j]      t = 0 .. T-1
+ *   out[b,i,:] = sum_t softmax(s)_t * v_cache[b,g,t,:]
+ * The token being decoded must already be in the cache (the page appends the new
+ * key and value before attending), so T counts it.  There is no mask inside the
+ * T positions.  Positions t >= T are never used; they may hold anything,
+ * including NaN.  T = 0 gives out = 0.
+ *
+ * q         device, bf16 [B, H, d], contiguous (row b*H+i holds head i of sequence b)
+ * k_cache   device, bf16 [B, G, Lmax, d], contiguous; 16-byte aligned
+ * v_cache   device, bf16 [B, G, Lmax, d], contiguous; 16-byte aligned
+ * seq_lens  device, int32 [B]; expected 0 <= seq_lens[b] <= Lmax.  Values outside
+ *           are clamped into that range on the device and GQA_FLAG_SEQ_LEN_CLAMPED
+ *           is set in the workspace flag word.
+ * out       device, float32 [B, H, d], contiguous.  Must not overlap any input.
+ * workspace device, zero-filled before first use, >= gqa_decode_workspace_size bytes,
+ *           256-byte aligned.  Used by one call at a time.
+ * B         1 .. GQA_MAX_BATCH
+ * H, G      H >= G >= 1, H % G == 0, H/G <= 64
+ * d         head dimension: 64 or 128
+ * Lmax      >= 1, cache capacity per sequence
+ * scale     score scale, normally 1/sqrt(d), used as given (fp32)
+ *
+ * Arithmetic: exact bf16 products accumulated in fp32, softmax in fp32 with a
+ * running maximum, fp32 output.  Error bound vs the exact result: see the design
+ * notes (max abs <= 1e-2 and row-relative <= 2e-3 on the benchmark workloads).
+ */
+gqa_status gqa_decode(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *seq_lens, float *out,
+                      void *workspace, size_t workspace_bytes,
+                      int B, int H, int G, int d, int Lmax, float scale, void *stream);
+
+/* Knobs for tests and tuning.  Zero-initialise, then set what you need. */
+typedef struct gqa_decode_options {
+    int path;          /* GQA_PATH_*; 0 = automatic */
+    int num_ctas;      /* CTAs of the split kernel; 0 = automatic (1..GQA_MAX_CTAS) */
+    int reserved[6];   /* must be zero */
+} gqa_decode_options;
+
+/* gqa_decode with explicit options (opts may be NULL = defaults).  A path that
+ * does not support the shape returns GQA_ERR_UNSUPPORTED. */
+gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *seq_lens, float *out,
+                         void *workspace, size_t workspace_bytes,
+                         int B, int H, int G, int d, int Lmax, float scale, void *stream,
+                         const gqa_decode_options *opts);
+
+/* The path gqa_decode would take for this shape (GQA_PATH_SIMT or
+ * GQA_PATH_TCGEN05), or a negative gqa_status if the shape is rejected. */
+int gqa_decode_select_path(int B, int H, int G, int d, int Lmax);
+
+/*
+ * Copy the workspace flag word (GQA_FLAG_* bits, OR-ed by earlier decode calls)
+ * to *flags.  Enqueued on `stream` and then synchronises that stream.
+ * With clear != 0 the word is reset to zero afterwards (also on `stream`).
+ */
+gqa_status gqa_decode_read_flags(void *workspace, uint32_t *flags, int clear, void *stream);
+
+/*
+ * Mean-pool conversion of K (or V) projection heads into G groups.
+ * ["Grouped-query attention (GQA)" concept page, "Converted and uptrained
+ *  checkpoints" and the conversion pseudocode; arxiv:2305.13245 §2.1]
+ *
+ * w_in   device, float32 [H, h, d_model], head-major (head i's projection slice)
+ * w_out  device, float32 [G, h, d_model]
+ * w_out[g, r, c] = ((w_in[g*n, r, c] + w_in[g*n+1, r, c]) + ... + w_in[g*n+n-1, r, c]) / n
+ * with n = H/G, each addition and the division rounded in fp32 (IEEE, round to
+ * nearest), in that order: the result is bit-identical to that sequence.
+ * Call it once for W_K and once for W_V; the query and output projections are
+ * left unchanged by the conversion.
+ */
+gqa_status gqa_meanpool_kv(const float *w_in, float *w_out, int H, int G, int h, int d_model,
+                           void *stream);
+
+/*
+ * The same pooling for any layout with heads on a middle axis:
+ * w_in [outer, H, inner] -> w_out [outer, G, inner].  The head-major layout is
+ * outer = 1, inner = h*d_model; the pages' [d_model, H*h] projection (head i in
+ * columns i*h .. (i+1)*h-1) is outer = d_model, inner = h.
+ */
+gqa_status gqa_meanpool_kv_strided(const float *w_in, float *w_out, int64_t outer, int H, int G,
+                                   int64_t inner, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_B300_GQA_H */

@@ -1,0 +1,266 @@
+// The C ABI: argument checks, tensor maps, path choice and launches.
+// Declarations and the contract of every entry point are in include/gqa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gqa.h"
+#include "launch.h"
+
+namespace {
+
+using gqa::DecodeParams;
+
+constexpr int kMaxHeadsPerGroup = 64;
+constexpr int kMaxHeads = 4096;
+constexpr long long kMaxLmax = 1ll << 24;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    bool ok = false;
+};
+
+// Per-device facts, looked up once per device.
+gqa_status device_info(DeviceInfo *out) {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    static bool seen[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return GQA_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!seen[dev]) {
+        DeviceInfo d;
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            d.ok = (major == 10 && minor == 3);
+        cudaGetLastError();
+        cache[dev] = d;
+        seen[dev] = true;
+    }
+    *out = cache[dev];
+    return out->ok ? GQA_OK : GQA_ERR_DEVICE;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+constexpr size_t kHeaderBytes = 256;
+
+size_t counters_bytes(int B, int G) { return align_up((size_t)B * G * sizeof(int), 256); }
+
+size_t workspace_bytes_for(int B, int H, int G, int d) {
+    const int n = H / G;
+    const size_t slots = (size_t)GQA_MAX_CTAS + (size_t)B * G;
+    return kHeaderBytes + counters_bytes(B, G) + slots * (size_t)n * (d + 2) * sizeof(float);
+}
+
+gqa_status check_shape(int B, int H, int G, int d, int Lmax) {
+    if (B <= 0 || H <= 0 || G <= 0 || d <= 0 || Lmax <= 0) return GQA_ERR_INVALID_ARG;
+    if (G > H || H % G != 0) return GQA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
+    if (B > GQA_MAX_BATCH || H > kMaxHeads || H / G > kMaxHeadsPerGroup || Lmax > kMaxLmax)
+        return GQA_ERR_UNSUPPORTED;
+    return GQA_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Cache viewed as a 3-D tensor [B*G][Lmax][d] of bf16, loaded in boxes of
+// 64 columns (128 bytes, 128-byte swizzle) x 128 positions x 1.  Positions past
+// Lmax read as zero.
+bool make_cache_map(CUtensorMap *map, const void *base, int B, int G, int d, int Lmax) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Lmax, (cuuint64_t)B * G};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)Lmax * d * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)gqa::kBoxCols, (cuuint32_t)gqa::kTile, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q viewed as [B*H][d] bf16, boxes of 64 columns x `rows` rows (128-byte swizzle).
+bool make_q_map(CUtensorMap *map, const void *base, int B, int H, int d, int rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)B * H};
+    const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)gqa::kBoxCols, (cuuint32_t)rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int auto_path(int H, int G, int d) {
+    const int n = H / G;
+    if (gqa::tc_max_heads() >= n && n >= 8) return GQA_PATH_TCGEN05;
+    if (n <= gqa::simt_max_heads()) return GQA_PATH_SIMT;
+    return GQA_PATH_TCGEN05;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gqa_status_string(int status) {
+    switch (status) {
+        case GQA_OK: return "GQA_OK";
+        case GQA_ERR_INVALID_ARG: return "GQA_ERR_INVALID_ARG: invalid argument";
+        case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED: shape or option not supported by this build";
+        case GQA_ERR_WORKSPACE: return "GQA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case GQA_ERR_LAUNCH: return "GQA_ERR_LAUNCH: a CUDA call or kernel launch failed";
+        case GQA_ERR_DEVICE: return "GQA_ERR_DEVICE: no usable sm_103 CUDA device";
+        default: return "unknown gqa_status";
+    }
+}
+
+int gqa_abi_version(void) { return GQA_ABI_VERSION; }
+
+gqa_status gqa_decode_workspace_size(int B, int H, int G, int d, int Lmax, size_t *bytes) {
+    if (!bytes) return GQA_ERR_INVALID_ARG;
+    const gqa_status s = check_shape(B, H, G, d, Lmax);
+    if (s != GQA_OK) return s;
+    *bytes = workspace_bytes_for(B, H, G, d);
+    return GQA_OK;
+}
+
+int gqa_decode_select_path(int B, int H, int G, int d, int Lmax) {
+    const gqa_status s = check_shape(B, H, G, d, Lmax);
+    if (s != GQA_OK) return -(int)s;
+    return auto_path(H, G, d);
+}
+
+gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                         float *out, void *workspace, size_t workspace_bytes, int B, int H, int G, int d, int Lmax,
+                         float scale, void *stream, const gqa_decode_options *opts) {
+    if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
+    gqa_status s = check_shape(B, H, G, d, Lmax);
+    if (s != GQA_OK) return s;
+    if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+        !aligned(seq_lens, 4))
+        return GQA_ERR_INVALID_ARG;
+    gqa_decode_options o{};
+    if (opts) o = *opts;
+    for (int r : o.reserved)
+        if (r != 0) return GQA_ERR_INVALID_ARG;
+    if (o.num_ctas < 0 || o.num_ctas > GQA_MAX_CTAS) return GQA_ERR_INVALID_ARG;
+    if (o.path < 0 || o.path > GQA_PATH_TCGEN05) return GQA_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < workspace_bytes_for(B, H, G, d))
+        return GQA_ERR_WORKSPACE;
+
+    const int n = H / G;
+    int path = o.path ? o.path : auto_path(H, G, d);
+    if (path == GQA_PATH_SIMT && n > gqa::simt_max_heads()) return GQA_ERR_UNSUPPORTED;
+    if (path == GQA_PATH_TCGEN05 && n > gqa::tc_max_heads()) return GQA_ERR_UNSUPPORTED;
+
+    DeviceInfo dev;
+    s = device_info(&dev);
+    if (s != GQA_OK) return s;
+
+    // One CTA per SM, never more than there are tiles.
+    const long long tiles_max = (long long)B * G * ((Lmax + gqa::kTile - 1) / gqa::kTile);
+    long long ctas = o.num_ctas ? o.num_ctas : dev.sms;
+    if (ctas > GQA_MAX_CTAS) ctas = GQA_MAX_CTAS;
+    if (ctas > tiles_max) ctas = tiles_max;
+    if (ctas < 1) ctas = 1;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    DecodeParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.flags = reinterpret_cast<unsigned int *>(ws);
+    p.counters = reinterpret_cast<int *>(ws + kHeaderBytes);
+    p.partials = reinterpret_cast<float *>(ws + kHeaderBytes + counters_bytes(B, G));
+    p.B = B;
+    p.H = H;
+    p.G = G;
+    p.n = n;
+    p.Lmax = Lmax;
+    p.scale_log2 = scale * 1.4426950408889634f;
+
+    CUtensorMap tk, tv;
+    if (!make_cache_map(&tk, k_cache, B, G, d, Lmax) || !make_cache_map(&tv, v_cache, B, G, d, Lmax))
+        return GQA_ERR_LAUNCH;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (path == GQA_PATH_SIMT) {
+        e = gqa::launch_decode_simt(tk, tv, p, d, (int)ctas, st);
+    } else {
+        const int rows = n <= 16 ? 16 : (n + 15) / 16 * 16;
+        CUtensorMap tq;
+        if (!make_q_map(&tq, q, B, H, d, rows)) return GQA_ERR_LAUNCH;
+        e = gqa::launch_decode_tc(tk, tv, tq, p, d, (int)ctas, st);
+    }
+    if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_LAUNCH;
+}
+
+gqa_status gqa_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens, float *out,
+                      void *workspace, size_t workspace_bytes, int B, int H, int G, int d, int Lmax, float scale,
+                      void *stream) {
+    return gqa_decode_ex(q, k_cache, v_cache, seq_lens, out, workspace, workspace_bytes, B, H, G, d, Lmax, scale,
+                         stream, nullptr);
+}
+
+gqa_status gqa_decode_read_flags(void *workspace, uint32_t *flags, int clear, void *stream) {
+    if (!workspace || !flags || !aligned(workspace, 256)) return GQA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t host = 0;
+    if (cudaMemcpyAsync(&host, workspace, sizeof host, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        (clear && cudaMemsetAsync(workspace, 0, sizeof host, st) != cudaSuccess) ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_LAUNCH;
+    }
+    *flags = host;
+    return GQA_OK;
+}
+
+gqa_status gqa_meanpool_kv_strided(const float *w_in, float *w_out, int64_t outer, int H, int G, int64_t inner,
+                                   void *stream) {
+    if (!w_in || !w_out) return GQA_ERR_INVALID_ARG;
+    if (outer <= 0 || inner <= 0 || H <= 0 || G <= 0 || G > H || H % G != 0) return GQA_ERR_INVALID_ARG;
+    if (!aligned(w_in, 4) || !aligned(w_out, 4)) return GQA_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    const gqa_status s = device_info(&dev);
+    if (s != GQA_OK) return s;
+    const cudaError_t e = gqa::launch_meanpool(w_in, w_out, outer, H, G, inner, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_LAUNCH;
+}
+
+gqa_status gqa_meanpool_kv(const float *w_in, float *w_out, int H, int G, int h, int d_model, void *stream) {
+    if (h <= 0 || d_model <= 0) return GQA_ERR_INVALID_ARG;
+    return gqa_meanpool_kv_strided(w_in, w_out, 1, H, G, (int64_t)h * d_model, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,169 @@
+// Work decomposition and split-combine shared by the decode kernels.
+//
+// Work unit: a tile of 128 consecutive cache positions of one (sequence b,
+// K/V head g) pair, a "segment".  Segment s = b*G + g holds
+// tiles_b = ceil(seq_lens[b] / 128) tiles.  All tiles of all segments form one
+// list in (b, g, j) order, W tiles long.  CTA c of P processes the contiguous
+// range [c*W/P, (c+1)*W/P): every CTA gets the same number of tiles (+-1), however
+// ragged the sequence lengths are, and the whole grid is one wave.  When there
+// are fewer tiles than CTAs, only the first W CTAs take tiles (P = min(grid, W)),
+// so no working range is empty.
+//
+// A CTA's range cuts segments into "pieces".  A piece that covers its whole
+// segment is finished in place (out = acc / l).  Otherwise the piece's partial
+// softmax state (m, l, acc) goes to a workspace slot and the CTA bumps the
+// segment's arrival counter; the CTA that arrives last merges every piece of
+// the segment and resets the counter to zero.  Nobody waits for anybody: the
+// merge is done by whoever comes last.
+//
+// Partial slot of the piece of segment s cut by CTA c: slot = c + s.  This is
+// one-to-one: if c < c' then every segment of c is <= every segment of c', so
+// c + s = c' + s' with c < c' would need s > s'.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace gqa {
+
+constexpr int kTile = 128;          // cache positions per tile
+constexpr int kBoxCols = 64;        // bf16 elements per 128-byte swizzled row
+constexpr int kBoxBytes = kTile * 128;
+constexpr int kMaxBatch = 1024;
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;   // [B, H, D]
+    const int32_t *seq_lens;  // [B]
+    float *out;               // [B, H, D]
+    unsigned int *flags;      // workspace flag word
+    int *counters;            // [B*G] arrival counters (zero between calls)
+    float *partials;          // slots of n*(D+2) floats: m[n], l[n], acc[n][D]
+    int B, H, G, n, Lmax;
+    float scale_log2;         // scale * log2(e): scores are kept in base-2 units
+};
+
+__device__ __forceinline__ int tiles_of(int seq) { return (seq + kTile - 1) / kTile; }
+
+__device__ __forceinline__ int clamp_seq(int s, int Lmax) { return s < 0 ? 0 : (s > Lmax ? Lmax : s); }
+
+__device__ __forceinline__ long long range_start(int c, long long W, int P) {
+    return (long long)c * W / P;
+}
+
+// The CTA whose range holds tile t (0 <= t < W).
+__device__ __forceinline__ int cta_of_tile(long long t, long long W, int P) {
+    return (int)(((t + 1) * P - 1) / W);
+}
+
+struct Cursor {
+    int b, g, j, tiles;
+};
+
+// prefix[b] = tiles of sequences 0..b-1, prefix[B] = total.
+__device__ __forceinline__ Cursor cursor_at(long long u, const int *prefix, int B, int G) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)G * prefix[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    Cursor c;
+    c.b = lo;
+    c.tiles = prefix[lo + 1] - prefix[lo];
+    const long long r = u - (long long)G * prefix[lo];
+    c.g = (int)(r / c.tiles);
+    c.j = (int)(r % c.tiles);
+    return c;
+}
+
+__device__ __forceinline__ void cursor_next(Cursor &c, const int *prefix, int B, int G) {
+    if (++c.j < c.tiles) return;
+    c.j = 0;
+    if (++c.g < G) return;
+    c.g = 0;
+    do { ++c.b; } while (c.b < B && prefix[c.b + 1] == prefix[c.b]);
+    if (c.b < B) c.tiles = prefix[c.b + 1] - prefix[c.b];
+}
+
+// Block-wide: clamps seq_lens into [0, Lmax] and writes the tile prefix sums.
+// `scratch` needs 32 ints.  Ends with __syncthreads().
+__device__ inline void build_prefix(const int32_t *seq_lens, int B, int Lmax, int *prefix, int *scratch,
+                             unsigned int *flags) {
+    const int tid = threadIdx.x, nth = blockDim.x;
+    const int per = (B + nth - 1) / nth;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    int local = 0;
+    bool bad = false;
+    for (int b = b0; b < b1; ++b) {
+        const int s = __ldg(seq_lens + b);
+        bad |= (s < 0 || s > Lmax);
+        local += tiles_of(clamp_seq(s, Lmax));
+    }
+    // exclusive scan of `local` over the block
+    const int lane = tid & 31, warp = tid >> 5, nwarps = (nth + 31) >> 5;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < nwarps; ++w) {
+        const int x = scratch[w];
+        if (w < warp) before += x;
+        total += x;
+    }
+    int run = before + incl - local;
+    for (int b = b0; b < b1; ++b) {
+        prefix[b] = run;
+        run += tiles_of(clamp_seq(__ldg(seq_lens + b), Lmax));
+    }
+    if (tid == 0) prefix[B] = total;
+    if (bad && blockIdx.x == 0) atomicOr(flags, 0x1u /* GQA_FLAG_SEQ_LEN_CLAMPED */);
+    __syncthreads();
+}
+
+// Segments with no valid position get out = 0 (the empty sum).  CTA c takes
+// sequences b with b % P == c.
+template <int D>
+__device__ void zero_empty_sequences(const DecodeParams &p, const int *prefix, int P, int tid, int nthreads) {
+    for (int b = blockIdx.x; b < p.B; b += P) {
+        if (prefix[b + 1] != prefix[b]) continue;
+        float4 *o = reinterpret_cast<float4 *>(p.out + (size_t)b * p.H * D);
+        for (int x = tid; x < p.H * D / 4; x += nthreads) o[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+__device__ __forceinline__ float *slot_ptr(const DecodeParams &p, int slot, int D) {
+    return p.partials + (size_t)slot * p.n * (D + 2);
+}
+
+// Merge every piece of segment (b, g) from its slots and write the n output rows.
+// Called by `nthreads` threads with ids 0..nthreads-1 after the caller has made
+// the other pieces' writes visible (__threadfence after the last arrival).
+template <int D>
+__device__ void combine_segment(const DecodeParams &p, int first_slot, int count, int b, int g, int tid,
+                                int nthreads) {
+    const int n = p.n;
+    const size_t stride = (size_t)n * (D + 2);
+    const float *base = p.partials + (size_t)first_slot * stride;
+    float *orow = p.out + ((size_t)b * p.H + (size_t)g * n) * D;
+    for (int idx = tid; idx < n * D; idx += nthreads) {
+        const int h = idx / D, dim = idx - h * D;
+        float M = -INFINITY;
+        for (int k = 0; k < count; ++k) M = fmaxf(M, __ldcg(base + k * stride + h));
+        float L = 0.f, A = 0.f;
+        for (int k = 0; k < count; ++k) {
+            const float *sl = base + k * stride;
+            const float w = exp2f(__ldcg(sl + h) - M);
+            L = fmaf(__ldcg(sl + n + h), w, L);
+            A = fmaf(__ldcg(sl + 2 * n + h * D + dim), w, A);
+        }
+        orow[idx] = A / L;
+    }
+}
+
+}  // namespace gqa

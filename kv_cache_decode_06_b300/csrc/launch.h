@@ -1,0 +1,22 @@
+// Internal interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "decode_common.cuh"
+
+namespace gqa {
+
+int simt_max_heads();
+cudaError_t launch_decode_simt(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int D,
+                               int ctas, cudaStream_t stream);
+
+int tc_max_heads();
+cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
+                             const DecodeParams &p, int D, int ctas, cudaStream_t stream);
+
+cudaError_t launch_meanpool(const float *w_in, float *w_out, long long outer, int H, int G, long long inner,
+                            cudaStream_t stream);
+
+}  // namespace gqa

@@ -1,0 +1,192 @@
+"""Python binding of libgqa_b300.so (ctypes).  Argument marshalling only.
+
+Every step of the decode and of the mean-pool conversion runs in the CUDA
+library; this module checks tensor properties, passes raw device pointers and
+the current CUDA stream, and turns status codes into exceptions.  PyTorch is
+used for device memory and streams.  If the shared library is missing the
+first call raises: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgqa_b300.so")
+
+GQA_OK = 0
+STATUS_NAMES = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_UNSUPPORTED", 3: "GQA_ERR_WORKSPACE",
+                4: "GQA_ERR_LAUNCH", 5: "GQA_ERR_DEVICE"}
+PATH_AUTO, PATH_SIMT, PATH_TCGEN05 = 0, 1, 2
+FLAG_SEQ_LEN_CLAMPED = 0x1
+FLAG_WAIT_TIMEOUT = 0x2
+
+# Every symbol include/gqa.h declares.
+EXPORTS = ("gqa_status_string", "gqa_abi_version", "gqa_decode_workspace_size", "gqa_decode", "gqa_decode_ex",
+           "gqa_decode_select_path", "gqa_decode_read_flags", "gqa_meanpool_kv", "gqa_meanpool_kv_strided")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GQAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+class DecodeOptions(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("num_ctas", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+
+
+def load(path: Optional[str] = None):
+    """Load libgqa_b300.so and declare its C signatures.  Raises if it is absent."""
+    global _lib
+    if path is None and _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with `python -m kv_cache_decode_06_b300.build_lib` "
+                           "(the GQA decode path has no CPU fallback)")
+    with _lock:
+        lib = ctypes.CDLL(p)
+        V, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.gqa_status_string.restype = ctypes.c_char_p
+        lib.gqa_status_string.argtypes = [I]
+        lib.gqa_abi_version.restype = I
+        lib.gqa_abi_version.argtypes = []
+        lib.gqa_decode_workspace_size.restype = I
+        lib.gqa_decode_workspace_size.argtypes = [I, I, I, I, I, ctypes.POINTER(Z)]
+        lib.gqa_decode.restype = I
+        lib.gqa_decode.argtypes = [V, V, V, V, V, V, Z, I, I, I, I, I, F, V]
+        lib.gqa_decode_ex.restype = I
+        lib.gqa_decode_ex.argtypes = [V, V, V, V, V, V, Z, I, I, I, I, I, F, V, ctypes.POINTER(DecodeOptions)]
+        lib.gqa_decode_select_path.restype = I
+        lib.gqa_decode_select_path.argtypes = [I, I, I, I, I]
+        lib.gqa_decode_read_flags.restype = I
+        lib.gqa_decode_read_flags.argtypes = [V, ctypes.POINTER(ctypes.c_uint32), I, V]
+        lib.gqa_meanpool_kv.restype = I
+        lib.gqa_meanpool_kv.argtypes = [V, V, I, I, I, I, V]
+        lib.gqa_meanpool_kv_strided.restype = I
+        lib.gqa_meanpool_kv_strided.argtypes = [V, V, ctypes.c_int64, I, I, ctypes.c_int64, V]
+        if path is None:
+            _lib = lib
+    return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != GQA_OK:
+        raise GQAError(status, what)
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device: torch.device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _require(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_size(B: int, H: int, G: int, d: int, Lmax: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().gqa_decode_workspace_size(B, H, G, d, Lmax, ctypes.byref(n)), "gqa_decode_workspace_size")
+    return n.value
+
+
+def alloc_workspace(B: int, H: int, G: int, d: int, Lmax: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace of the size gqa_decode needs (256-byte aligned by the allocator)."""
+    return torch.zeros(workspace_size(B, H, G, d, Lmax), dtype=torch.uint8, device=device)
+
+
+def select_path(B: int, H: int, G: int, d: int, Lmax: int) -> int:
+    r = load().gqa_decode_select_path(B, H, G, d, Lmax)
+    if r < 0:
+        raise GQAError(-r, "gqa_decode_select_path")
+    return r
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens: torch.Tensor,
+           out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+           scale: Optional[float] = None, stream: Optional[torch.cuda.Stream] = None,
+           path: int = PATH_AUTO, num_ctas: int = 0) -> torch.Tensor:
+    """One GQA decode step: q [B,H,d] bf16, caches [B,G,Lmax,d] bf16, seq_lens [B] int32 -> out [B,H,d] fp32.
+
+    Enqueued on ``stream`` (default: the current stream); returns ``out``.
+    ``workspace`` must come from :func:`alloc_workspace` (zero-filled), or be
+    reused from an earlier call with the same B and G (the counters it holds
+    are back at zero after every call); for another (B, G), zero it again.
+    """
+    dev = q.device
+    B, H, d = q.shape
+    Bk, G, Lmax, dk = k_cache.shape
+    if Bk != B or dk != d or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(seq_lens.shape) != (B,):
+        raise ValueError("shape mismatch between q, k_cache, v_cache and seq_lens")
+    _require(q, "q", torch.bfloat16, dev)
+    _require(k_cache, "k_cache", torch.bfloat16, dev)
+    _require(v_cache, "v_cache", torch.bfloat16, dev)
+    _require(seq_lens, "seq_lens", torch.int32, dev)
+    if out is None:
+        out = torch.empty((B, H, d), dtype=torch.float32, device=dev)
+    _require(out, "out", torch.float32, dev)
+    if workspace is None:
+        workspace = alloc_workspace(B, H, G, d, Lmax, dev)
+    _require(workspace, "workspace", torch.uint8, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    opts = DecodeOptions(path, num_ctas)
+    _check(load().gqa_decode_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seq_lens.data_ptr(),
+                                out.data_ptr(), workspace.data_ptr(), workspace.numel(), B, H, G, d, Lmax,
+                                float(scale), _stream_handle(stream, dev), ctypes.byref(opts)),
+           "gqa_decode")
+    return out
+
+
+def read_flags(workspace: torch.Tensor, clear: bool = False, stream: Optional[torch.cuda.Stream] = None) -> int:
+    """GQA_FLAG_* bits recorded in ``workspace`` by earlier decode calls (synchronises the stream)."""
+    f = ctypes.c_uint32(0)
+    _check(load().gqa_decode_read_flags(workspace.data_ptr(), ctypes.byref(f), int(clear),
+                                        _stream_handle(stream, workspace.device)), "gqa_decode_read_flags")
+    return f.value
+
+
+def meanpool_kv(w_in: torch.Tensor, G: int, out: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Mean-pool a head-major projection [H, h, d_model] fp32 into [G, h, d_model]."""
+    dev = w_in.device
+    _require(w_in, "w_in", torch.float32, dev)
+    H, h, dm = w_in.shape
+    if out is None:
+        out = torch.empty((G, h, dm), dtype=torch.float32, device=dev)
+    _require(out, "out", torch.float32, dev)
+    if tuple(out.shape) != (G, h, dm):
+        raise ValueError("out must be [G, h, d_model]")
+    _check(load().gqa_meanpool_kv(w_in.data_ptr(), out.data_ptr(), H, G, h, dm, _stream_handle(stream, dev)),
+           "gqa_meanpool_kv")
+    return out
+
+
+def meanpool_kv_strided(w_in: torch.Tensor, G: int, out: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Mean-pool heads on the middle axis: [outer, H, inner] -> [outer, G, inner]."""
+    dev = w_in.device
+    _require(w_in, "w_in", torch.float32, dev)
+    outer, H, inner = w_in.shape
+    if out is None:
+        out = torch.empty((outer, G, inner), dtype=torch.float32, device=dev)
+    _require(out, "out", torch.float32, dev)
+    if tuple(out.shape) != (outer, G, inner):
+        raise ValueError("out must be [outer, G, inner]")
+    _check(load().gqa_meanpool_kv_strided(w_in.data_ptr(), out.data_ptr(), outer, H, G, inner,
+                                          _stream_handle(stream, dev)), "gqa_meanpool_kv_strided")
+    return out

@@ -17,3 +17,10 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+@pytest.fixture(scope="session")
+def gqa_lib():
+    from kv_cache_decode_06_b300 import build_lib, gqa
+    build_lib.build()
+    return gqa.load()

@@ -1,0 +1,161 @@
+"""CPU tests of the C ABI: the library loads, exports what include/gqa.h declares,
+and rejects bad arguments before touching a GPU.  No compute call runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from kv_cache_decode_06_b300 import gqa
+from kv_cache_decode_06_b300.inputs import CONFIGS, T5XXL_SWEEP_GS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa.h")
+
+# Any non-null, suitably aligned address: validation never dereferences it.
+FAKE = 0x10000
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declarations_match_binding():
+    assert declared_functions() == sorted(gqa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(gqa_lib):
+    for name in declared_functions():
+        assert hasattr(gqa_lib, name), name
+
+
+def test_library_does_not_link_the_oracle(gqa_lib):
+    with pytest.raises(AttributeError):
+        getattr(gqa_lib, "oracle_gqa_decode_f64")
+
+
+def test_abi_version_matches_header(gqa_lib):
+    m = re.search(r"#define GQA_ABI_VERSION (\d+)", open(HEADER).read())
+    assert gqa_lib.gqa_abi_version() == int(m.group(1))
+
+
+def test_status_strings(gqa_lib):
+    for code, name in gqa.STATUS_NAMES.items():
+        assert gqa_lib.gqa_status_string(code).decode().startswith(name)
+    assert gqa_lib.gqa_status_string(99) == b"unknown gqa_status"
+
+
+def _ws(*shape):
+    n = ctypes.c_size_t(0)
+    st = gqa.load().gqa_decode_workspace_size(*shape, ctypes.byref(n))
+    return st, n.value
+
+
+def test_workspace_size_for_every_workload(gqa_lib):
+    cfgs = [CONFIGS[k] for k in ("tiny", "mistral7b", "llama3_70b", "long_ragged")]
+    cfgs += [CONFIGS["t5xxl_sweep"].with_G(G) for G in T5XXL_SWEEP_GS]
+    for c in cfgs:
+        st, n = _ws(c.B, c.H, c.G, c.d, c.Lmax)
+        assert st == 0 and n > 0
+        # partial slots: (GQA_MAX_CTAS + B*G) * n * (d + 2) floats, plus header and counters
+        assert n >= (1024 + c.B * c.G) * c.n * (c.d + 2) * 4
+        assert n < 64 * 2 ** 20
+
+
+@pytest.mark.parametrize("shape,status", [
+    ((0, 8, 2, 64, 128), 1), ((1, 8, 3, 64, 128), 1), ((1, 8, 16, 64, 128), 1), ((1, 8, 2, 96, 128), 2),
+    ((1, 8, 2, 64, 0), 1), ((2048, 8, 2, 64, 128), 2), ((1, 128, 1, 64, 128), 2), ((1, 8, 2, -64, 128), 1),
+    ((1, 8, 2, 64, 1 << 25), 2),
+])
+def test_workspace_size_rejects(shape, status, gqa_lib):
+    assert _ws(*shape)[0] == status
+
+
+def _decode(lib, ptrs=None, shape=(1, 8, 2, 64, 128), scale=0.125, ws_bytes=None, opts=None):
+    q, k, v, sl, out, ws = ptrs or (FAKE,) * 6
+    B, H, G, d, L = shape
+    if ws_bytes is None:
+        ws_bytes = _ws(*shape)[1] if _ws(*shape)[0] == 0 else 1 << 30
+    o = ctypes.byref(opts) if opts is not None else None
+    return lib.gqa_decode_ex(q, k, v, sl, out, ws, ws_bytes, B, H, G, d, L, scale, None, o)
+
+
+def test_decode_rejects_null_pointers(gqa_lib):
+    for i in range(5):
+        ptrs = [FAKE] * 6
+        ptrs[i] = None
+        assert _decode(gqa_lib, ptrs) == 1
+    ptrs = [FAKE] * 6
+    ptrs[5] = None
+    assert _decode(gqa_lib, ptrs) == 3
+
+
+def test_decode_rejects_bad_shapes_and_values(gqa_lib):
+    assert _decode(gqa_lib, shape=(1, 8, 3, 64, 128)) == 1          # H % G != 0
+    assert _decode(gqa_lib, shape=(1, 8, 2, 80, 128)) == 2          # unsupported head dim
+    assert _decode(gqa_lib, shape=(0, 8, 2, 64, 128)) == 1          # B = 0
+    assert _decode(gqa_lib, shape=(1, 8, 2, 64, 0)) == 1            # Lmax = 0
+    assert _decode(gqa_lib, scale=float("nan")) == 1
+    assert _decode(gqa_lib, scale=float("inf")) == 1
+
+
+def test_decode_rejects_misaligned_pointers(gqa_lib):
+    for i in range(5):
+        ptrs = [FAKE] * 6
+        ptrs[i] = FAKE + 2
+        assert _decode(gqa_lib, ptrs) == 1, i
+    ptrs = [FAKE] * 6
+    ptrs[5] = FAKE + 16
+    assert _decode(gqa_lib, ptrs) == 3
+
+
+def test_decode_rejects_small_workspace(gqa_lib):
+    need = _ws(1, 8, 2, 64, 128)[1]
+    assert _decode(gqa_lib, ws_bytes=need - 1) == 3
+
+
+def test_decode_rejects_bad_options(gqa_lib):
+    o = gqa.DecodeOptions(7, 0)
+    assert _decode(gqa_lib, opts=o) == 1
+    o = gqa.DecodeOptions(0, 5000)
+    assert _decode(gqa_lib, opts=o) == 1
+    o = gqa.DecodeOptions(0, 0)
+    o.reserved[2] = 1
+    assert _decode(gqa_lib, opts=o) == 1
+    o = gqa.DecodeOptions(gqa.PATH_SIMT, 0)                          # H/G = 16 > simt limit
+    assert _decode(gqa_lib, shape=(1, 32, 2, 64, 128), opts=o) == 2
+
+
+def test_select_path(gqa_lib):
+    assert gqa_lib.gqa_decode_select_path(16, 32, 8, 128, 4096) in (gqa.PATH_SIMT, gqa.PATH_TCGEN05)
+    assert gqa_lib.gqa_decode_select_path(1, 8, 3, 64, 128) == -1
+    assert gqa_lib.gqa_decode_select_path(1, 8, 2, 96, 128) == -2
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-GPU answer")
+def test_decode_without_gpu_reports_device(gqa_lib):
+    assert _decode(gqa_lib) == 5
+
+
+def test_meanpool_rejects(gqa_lib):
+    lib = gqa_lib
+    assert lib.gqa_meanpool_kv(None, FAKE, 8, 2, 64, 512, None) == 1
+    assert lib.gqa_meanpool_kv(FAKE, None, 8, 2, 64, 512, None) == 1
+    assert lib.gqa_meanpool_kv(FAKE, FAKE, 8, 3, 64, 512, None) == 1
+    assert lib.gqa_meanpool_kv(FAKE, FAKE, 8, 16, 64, 512, None) == 1
+    assert lib.gqa_meanpool_kv(FAKE, FAKE, 8, 2, 0, 512, None) == 1
+    assert lib.gqa_meanpool_kv_strided(FAKE, FAKE, 0, 8, 2, 64, None) == 1
+    assert lib.gqa_meanpool_kv_strided(FAKE + 2, FAKE, 1, 8, 2, 64, None) == 1
+
+
+def test_read_flags_rejects(gqa_lib):
+    f = ctypes.c_uint32(0)
+    assert gqa_lib.gqa_decode_read_flags(None, ctypes.byref(f), 0, None) == 1
+    assert gqa_lib.gqa_decode_read_flags(FAKE + 8, ctypes.byref(f), 0, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        gqa.load(str(tmp_path / "missing.so"))

@@ -1,0 +1,216 @@
+"""GPU parity of gqa_decode (through the C ABI) against the float64 CPU oracle.
+
+Inputs are the seeded workloads of kv_cache_decode_06_b300.inputs; positions
+past each sequence's length hold bf16 NaN, so any read of them shows up as a
+non-finite output.  The tolerance is in gpu_helpers (1e-2 absolute and 2e-3
+row-relative).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import check_close, to_device
+from kv_cache_decode_06_b300 import gqa
+from kv_cache_decode_06_b300.inputs import (
+    CONFIGS, T5XXL_SWEEP_GS, DecodeConfig, make_decode_inputs,
+)
+
+pytestmark = pytest.mark.gpu
+
+PATHS = {"simt": gqa.PATH_SIMT, "tcgen05": gqa.PATH_TCGEN05}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(gqa_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return gqa_lib
+
+
+def supports(path, cfg):
+    n = cfg.n
+    if path == gqa.PATH_SIMT:
+        return n <= 8
+    return gqa.load() and n <= 64 and _tc_available()
+
+
+def _tc_available():
+    try:
+        c = DecodeConfig("probe", 99, B=1, H=8, G=1, d=64, Lmax=128, seq_lo=1, seq_hi=1)
+        inp = make_decode_inputs(c)
+        q, k, v, sl = to_device(inp)
+        gqa.decode(q, k, v, sl, path=gqa.PATH_TCGEN05)
+        return True
+    except gqa.GQAError as e:
+        if e.status == 2:
+            return False
+        raise
+
+
+def run(inp, path=gqa.PATH_AUTO, num_ctas=0, ws=None, out=None):
+    q, k, v, sl = to_device(inp)
+    o = gqa.decode(q, k, v, sl, out=out, workspace=ws, scale=float(inp.scale), path=path, num_ctas=num_ctas)
+    torch.cuda.synchronize()
+    return o.cpu().numpy()
+
+
+def oracle_out(inp, rows=None):
+    return oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale, rows=rows)
+
+
+# ----------------------------------------------------------- small shapes
+
+SMALL = [
+    # (B, H, G, d, Lmax, seq_lens)
+    (1, 8, 2, 64, 128, [128]),
+    (3, 8, 2, 64, 300, [1, 129, 300]),
+    (2, 4, 4, 128, 257, [256, 257]),
+    (4, 32, 8, 128, 1000, [1000, 1, 127, 513]),
+    (5, 16, 2, 64, 640, [0, 640, 3, 0, 385]),
+    (2, 8, 1, 128, 384, [384, 200]),
+    (3, 6, 2, 128, 131, [130, 131, 2]),
+    (2, 64, 8, 128, 1024, [1024, 777]),
+]
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "B{}H{}G{}d{}L{}".format(*s[:5]))
+def test_small_shapes(shape, path):
+    B, H, G, d, L, seq = shape
+    cfg = DecodeConfig("small", 50, B=B, H=H, G=G, d=d, Lmax=L)
+    if not supports(PATHS[path], cfg):
+        pytest.skip(f"{path} does not take H/G={cfg.n}")
+    inp = make_decode_inputs(cfg, seq_lens=seq)
+    got = run(inp, path=PATHS[path])
+    check_close(got, oracle_out(inp), what=f"{path} {shape}")
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
+def test_split_invariance(path):
+    """The answer does not depend on how the tiles are split across CTAs."""
+    cfg = DecodeConfig("split", 51, B=3, H=16, G=4, d=128, Lmax=2048)
+    if not supports(PATHS[path], cfg):
+        pytest.skip(path)
+    inp = make_decode_inputs(cfg, seq_lens=[2048, 700, 1290])
+    ref = oracle_out(inp)
+    outs = []
+    for ctas in (1, 2, 3, 7, 37, 148, 1024):
+        got = run(inp, path=PATHS[path], num_ctas=ctas)
+        check_close(got, ref, what=f"{path} ctas={ctas}")
+        outs.append(got)
+    spread = max(np.abs(o - outs[0]).max() for o in outs)
+    assert spread <= 1e-5
+
+
+def test_repeated_calls_reuse_workspace():
+    """Counters return to zero after each call: a reused workspace gives identical results."""
+    cfg = CONFIGS["mistral7b"].with_(B=4)
+    inp = make_decode_inputs(cfg)
+    q, k, v, sl = to_device(inp)
+    ws = gqa.alloc_workspace(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax)
+    a = gqa.decode(q, k, v, sl, workspace=ws).clone()
+    for _ in range(5):
+        b = gqa.decode(q, k, v, sl, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    counters = ws[256:256 + 4 * cfg.B * cfg.G].view(torch.int32)
+    assert int(counters.abs().sum()) == 0
+    assert gqa.read_flags(ws) == 0
+
+
+def test_out_of_range_seq_lens_are_clamped_and_flagged():
+    cfg = DecodeConfig("clamp", 52, B=3, H=8, G=2, d=64, Lmax=256)
+    inp = make_decode_inputs(cfg, seq_lens=[256, 10, 0])
+    q, k, v, _ = to_device(inp)
+    bad = torch.tensor([1000, 10, -5], dtype=torch.int32, device="cuda")
+    ws = gqa.alloc_workspace(3, 8, 2, 64, 256)
+    got = gqa.decode(q, k, v, bad, workspace=ws, scale=float(inp.scale)).cpu().numpy()
+    check_close(got, oracle_out(inp), what="clamped")
+    assert gqa.read_flags(ws, clear=True) == gqa.FLAG_SEQ_LEN_CLAMPED
+    assert gqa.read_flags(ws) == 0
+
+
+def test_guard_regions_untouched():
+    """out is written exactly in [B, H, d]; canaries around it stay."""
+    cfg = DecodeConfig("guard", 53, B=2, H=8, G=2, d=128, Lmax=300)
+    inp = make_decode_inputs(cfg, seq_lens=[300, 0])
+    q, k, v, sl = to_device(inp)
+    pad = 4096
+    buf = torch.full((pad + 2 * 8 * 128 + pad,), 12345.0, dtype=torch.float32, device="cuda")
+    out = buf[pad:pad + 2 * 8 * 128].view(2, 8, 128)
+    gqa.decode(q, k, v, sl, out=out, scale=float(inp.scale))
+    torch.cuda.synchronize()
+    b = buf.cpu().numpy()
+    assert np.all(b[:pad] == 12345.0) and np.all(b[-pad:] == 12345.0)
+    check_close(out.cpu().numpy(), oracle_out(inp), what="guard")
+
+
+def test_all_empty_sequences_give_zero():
+    cfg = DecodeConfig("empty", 54, B=3, H=8, G=2, d=64, Lmax=128)
+    inp = make_decode_inputs(cfg, seq_lens=[0, 0, 0])
+    got = run(inp)
+    assert np.array_equal(got, np.zeros_like(got))
+
+
+def test_meanpool_bit_exact_tiny_workload():
+    from kv_cache_decode_06_b300.inputs import MEANPOOL_TINY, make_meanpool_input
+    c = MEANPOOL_TINY
+    w = make_meanpool_input(c["H"], c["G"], c["h"], c["d_model"])
+    got = gqa.meanpool_kv(torch.from_numpy(w).cuda(), c["G"]).cpu().numpy()
+    ref = oracle.meanpool_f32(w, c["H"], c["G"])
+    assert got.shape == (2, 64, 512)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("H,G,h,dm", [(8, 8, 16, 32), (8, 1, 16, 32), (12, 4, 8, 24), (6, 2, 5, 7), (64, 8, 128, 64)])
+def test_meanpool_bit_exact_shapes(H, G, h, dm):
+    from kv_cache_decode_06_b300.inputs import make_meanpool_input
+    w = make_meanpool_input(H, G, h, dm, config_id=7)
+    got = gqa.meanpool_kv(torch.from_numpy(w).cuda(), G).cpu().numpy()
+    ref = oracle.meanpool_f32(w, H, G)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_meanpool_pages_layout_bit_exact():
+    """The pages' [d_model, H*h] projection pooled per column block."""
+    from kv_cache_decode_06_b300.inputs import make_meanpool_input
+    H, G, h, dm = 8, 2, 64, 512
+    w = make_meanpool_input(H, G, h, dm, outer=dm).reshape(dm, H, h)
+    got = gqa.meanpool_kv_strided(torch.from_numpy(w).cuda(), G).cpu().numpy()
+    ref = oracle.meanpool_f32(w, H, G, head_axis=1)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------------------------ full workloads
+
+def test_tiny_workload():
+    inp = make_decode_inputs(CONFIGS["tiny"])
+    for path in (gqa.PATH_AUTO, gqa.PATH_SIMT):
+        check_close(run(inp, path=path), oracle_out(inp), what="tiny")
+
+
+@pytest.mark.slow
+def test_mistral7b_workload_full():
+    inp = make_decode_inputs(CONFIGS["mistral7b"])
+    check_close(run(inp), oracle_out(inp), what="mistral7b")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("G", T5XXL_SWEEP_GS)
+def test_t5xxl_sweep_workload(G):
+    inp = make_decode_inputs(CONFIGS["t5xxl_sweep"].with_G(G))
+    check_close(run(inp), oracle_out(inp), what=f"t5xxl G={G}")
+
+
+@pytest.mark.slow
+def test_llama3_70b_workload():
+    cfg = CONFIGS["llama3_70b"]
+    inp = make_decode_inputs(cfg)
+    got = run(inp)
+    check_close(got, oracle_out(inp), what="llama3_70b")
+
+
+@pytest.mark.slow
+def test_long_ragged_workload():
+    inp = make_decode_inputs(CONFIGS["long_ragged"])
+    check_close(run(inp), oracle_out(inp), what="long_ragged")
