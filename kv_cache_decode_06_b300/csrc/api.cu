@@ -216,7 +216,7 @@ gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache
     if (path == GQA_PATH_SIMT) {
         e = gqa::launch_decode_simt(tk, tv, p, d, (int)ctas, st);
     } else {
-        const int rows = n <= 16 ? 16 : (n + 15) / 16 * 16;
+        const int rows = gqa::tc_rows_for(n);
         CUtensorMap tq;
         if (!make_q_map(&tq, q, B, H, d, rows)) return GQA_ERR_LAUNCH;
         e = gqa::launch_decode_tc(tk, tv, tq, p, d, (int)ctas, st);

@@ -1,16 +1,478 @@
 // GQA decode on the fifth-generation tensor cores (tcgen05 + TMEM).
+//
+// The query heads of one group form the N side of two small GEMMs per
+// 128-position tile, with the positions (scores) or the head dims (values) on
+// the M side, so every K/V tile read from HBM serves all n = H/G heads:
+//   S^T [128 pos x N]  = K_tile [128 x d] . Q_g^T [d x N]       (K-major A and B)
+//   O^T [d x N]        = V_tile^T [d x 128] . P^T [128 x N]     (MN-major A, K-major B)
+// N is n rounded up to 16 (the extra columns are never read).  Operands come
+// from 128-byte-swizzled shared memory written by TMA; accumulators live in
+// TMEM.  P is split into bf16 hi + lo parts (two MMAs), so the probabilities
+// enter the value GEMM with ~16 significant bits instead of 8.
+// ["Grouped-query attention (GQA)" concept page, "Implementation sketch",
+//  decode-step pseudocode; arxiv:2305.13245 §2.2]
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2-5 = softmax + epilogue (thread <-> TMEM lane: a position of
+// the tile for S, a head dim for O).  Per tile: the max over the tile's
+// positions is exchanged across the 4 warps, probabilities go to shared memory
+// as P, and the previous tile's O is folded into register accumulators with
+// its rescale factor (so TMEM never needs rescaling).  Work split, pieces and
+// the last-arriver combine are shared with the CUDA-core path.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "decode_common.cuh"
 #include "launch.h"
+#include "tc_ptx.cuh"
 
 namespace gqa {
 
-int tc_max_heads() { return 0; }
+namespace {
 
-cudaError_t launch_decode_tc(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const DecodeParams &,
-                             int, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+constexpr int kSmemLimit = 232448;   // 227 KB opt-in per CTA
+
+template <int D, int N>
+struct TcCfg {
+    static constexpr int kBoxes = D / kBoxCols;
+    static constexpr int kTileBytes = kBoxes * kBoxBytes;        // one K or V tile (128 positions)
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kQBytes = kBoxes * N * 128;             // one Q buffer (N rows x d)
+    static constexpr int kPBytes = 2 * N * 128;                  // one P part: N rows x 128 positions
+    static constexpr int kMisc = 8192 + (kMaxBatch + 1) * 4 + 1024;
+    static constexpr int kQBuf = (2 * kQBytes + 4 * kPBytes + 2 * kStageBytes + kMisc <= kSmemLimit) ? 2 : 1;
+    static constexpr int kFixed = kQBuf * kQBytes + 4 * kPBytes;
+    static constexpr int kStagesFit = (kSmemLimit - kMisc - kFixed) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+    static_assert(kStages >= 2, "shared memory too small for two stages");
+    static constexpr int kOffQ = kStages * kStageBytes;
+    static constexpr int kOffP = kOffQ + kQBuf * kQBytes;        // [2 buffers][hi, lo]
+    static constexpr int kOffRed = kOffP + 4 * kPBytes;          // f32 [2][4][N] tile maxima
+    static constexpr int kOffLred = kOffRed + 2 * 4 * N * 4;     // f32 [4][N] l partial sums
+    static constexpr int kOffPrefix = kOffLred + 4 * N * 4;      // i32 [kMaxBatch + 1]
+    static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 1) * 4;
+    static constexpr int kOffBar = (kOffScratch + 32 * 4 + 7) / 8 * 8;
+    // barriers: kfull[S] vfull[S] kvempty[S] qfull[QB] qempty[QB] sfull[2] sfree[2] pfull[2]
+    //           ofull[2] ofree[2] red[2] grp done
+    static constexpr int kNumBars = 3 * kStages + 2 * kQBuf + 12 + 2;
+    static constexpr int kOffFlags = kOffBar + kNumBars * 8;       // abort, last, tmem base
+    static constexpr int kSmemBytes = kOffFlags + 16 + 1024;
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory layout too large");
+    static constexpr int kThreads = 192;
+    static constexpr int kTmemCols = (4 * N <= 32) ? 32 : (4 * N <= 64) ? 64 : (4 * N <= 128) ? 128 : 256;
+    static constexpr int kPvM = (D == 128) ? 128 : 64;
+};
+
+struct GroupSync128 {
+    uint64_t *bar;
+    uint32_t phase;
+    __device__ bool operator()(const AbortState &ab) {
+        mbar_arrive(bar);
+        const bool ok = mbar_wait(bar, phase & 1u, ab);
+        ++phase;
+        return ok;
+    }
+};
+
+template <int D, int N>
+__global__ void __launch_bounds__(192, 1)
+    gqa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+    using C = TcCfg<D, N>;
+    constexpr int S = C::kStages, QB = C::kQBuf;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float *red = reinterpret_cast<float *>(smem + C::kOffRed);
+    float *lred = reinterpret_cast<float *>(smem + C::kOffLred);
+    int *prefix = reinterpret_cast<int *>(smem + C::kOffPrefix);
+    int *scratch = reinterpret_cast<int *>(smem + C::kOffScratch);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint64_t *kfull = bars, *vfull = kfull + S, *kvempty = vfull + S;
+    uint64_t *qfull = kvempty + S, *qempty = qfull + QB;
+    uint64_t *sfull = qempty + QB, *sfree = sfull + 2, *pfull = sfree + 2, *ofull = pfull + 2, *ofree = ofull + 2;
+    uint64_t *redbar = ofree + 2, *grp = redbar + 2, *done = grp + 1;
+    volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::kOffFlags);
+    volatile int *s_last = s_abort + 1;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::kOffFlags + 8);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = gridDim.x;
+    const AbortState ab{s_abort, p.flags};
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&kfull[s], 1);
+            mbar_init(&vfull[s], 1);
+            mbar_init(&kvempty[s], 1);
+        }
+        for (int s = 0; s < QB; ++s) {
+            mbar_init(&qfull[s], 1);
+            mbar_init(&qempty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sfull[s], 1);
+            mbar_init(&sfree[s], 128);
+            mbar_init(&pfull[s], 128);
+            mbar_init(&ofull[s], 1);
+            mbar_init(&ofree[s], 128);
+            mbar_init(&redbar[s], 4);
+        }
+        mbar_init(grp, 128);
+        mbar_init(done, 1);
+        *s_abort = 0;
+        *s_last = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_q);
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, C::kTmemCols);
+        tmem_relinquish();
+    }
+    build_prefix(p.seq_lens, p.B, p.Lmax, prefix, scratch, p.flags);   // ends with __syncthreads
+    tc_fence_after_sync();
+    const uint32_t tmem = *s_tmem;
+
+    const int G = p.G, n = p.n;
+    const long long W = (long long)G * prefix[p.B];
+    const int Pw = (int)(W < P ? W : P);
+    long long u0 = 0, u1 = 0;
+    if ((int)blockIdx.x < Pw) {
+        u0 = range_start(blockIdx.x, W, Pw);
+        u1 = range_start(blockIdx.x + 1, W, Pw);
+    }
+    const int ntiles = (int)(u1 - u0);
+    int issued = 0, qissued = 0;
+
+    if (warp == 0) {
+        // ================================================================ producer
+        if (lane == 0 && ntiles > 0) {
+            const uint64_t pol_kv = l2_policy_evict_first();
+            const uint64_t pol_q = l2_policy_evict_last();
+            Cursor cur = cursor_at(u0, prefix, p.B, G);
+            int piece = 0;
+            for (int i = 0; i < ntiles; ++i) {
+                const bool first = (i == 0) || (cur.j == 0);
+                const bool last = (i + 1 == ntiles) || (cur.j + 1 == cur.tiles);
+                if (first) {
+                    const int qb = piece % QB;
+                    if (piece >= QB && !mbar_wait(&qempty[qb], ((piece / QB) - 1) & 1, ab)) break;
+                    mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
+                    uint8_t *qdst = smem + C::kOffQ + qb * C::kQBytes;
+                    const int y = cur.b * p.H + cur.g * n;
+#pragma unroll
+                    for (int c = 0; c < C::kBoxes; ++c)
+                        tma_load_2d(qdst + c * N * 128, &tm_q, c * kBoxCols, y, &qfull[qb], pol_q);
+                    ++qissued;
+                }
+                const int st = i % S;
+                if (i >= S && !mbar_wait(&kvempty[st], ((i / S) - 1) & 1, ab)) break;
+                uint8_t *kdst = smem + st * C::kStageBytes;
+                uint8_t *vdst = kdst + C::kTileBytes;
+                const int z = cur.b * G + cur.g, y = cur.j * kTile;
+                mbar_arrive_expect_tx(&kfull[st], C::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < C::kBoxes; ++c)
+                    tma_load_3d(kdst + c * kBoxBytes, &tm_k, c * kBoxCols, y, z, &kfull[st], pol_kv);
+                mbar_arrive_expect_tx(&vfull[st], C::kTileBytes);
+#pragma unroll
+                for (int c = 0; c < C::kBoxes; ++c)
+                    tma_load_3d(vdst + c * kBoxBytes, &tm_v, c * kBoxCols, y, z, &vfull[st], pol_kv);
+                ++issued;
+                if (last) ++piece;
+                cursor_next(cur, prefix, p.B, G);
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================================ MMA issuer
+        if (lane == 0 && ntiles > 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(128, N, false, false);
+            constexpr uint32_t idPV = idesc_bf16_f32(C::kPvM, N, true, false);
+            const uint32_t sbase = smem_addr(smem);
+            Cursor cur = cursor_at(u0, prefix, p.B, G);
+            int piece = 0;
+            bool ok = true;
+            // PV of tile i (after its P is ready)
+            auto issue_pv = [&](int i) -> bool {
+                const int st = i % S, bi = i & 1;
+                if (!mbar_wait(&vfull[st], (i / S) & 1, ab)) return false;
+                if (!mbar_wait(&pfull[bi], (i >> 1) & 1, ab)) return false;
+                if (i >= 2 && !mbar_wait(&ofree[bi], ((i >> 1) - 1) & 1, ab)) return false;
+                tc_fence_after_sync();
+                const uint32_t vb = sbase + st * C::kStageBytes + C::kTileBytes;
+                const uint32_t d_o = tmem + 2 * N + bi * N;
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t pb = sbase + C::kOffP + (bi * 2 + part) * C::kPBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        umma_bf16(d_o, sdesc_sw128(vb + kk * 2048, kBoxBytes, 1024),
+                                  sdesc_sw128(pb + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024), idPV,
+                                  (part | kk) != 0);
+                }
+                umma_commit(&ofull[bi]);
+                umma_commit(&kvempty[st]);
+                return true;
+            };
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const bool first = (i == 0) || (cur.j == 0);
+                const bool last = (i + 1 == ntiles) || (cur.j + 1 == cur.tiles);
+                const int st = i % S, bi = i & 1, qb = piece % QB;
+                if (first && !mbar_wait(&qfull[qb], (piece / QB) & 1, ab)) break;
+                if (!mbar_wait(&kfull[st], (i / S) & 1, ab)) break;
+                if (i >= 2 && !mbar_wait(&sfree[bi], ((i >> 1) - 1) & 1, ab)) break;
+                tc_fence_after_sync();
+                const uint32_t kb = sbase + st * C::kStageBytes;
+                const uint32_t qbase = sbase + C::kOffQ + qb * C::kQBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_bf16(tmem + bi * N, sdesc_sw128(kb + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
+                              sdesc_sw128(qbase + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024), idS, kk != 0);
+                umma_commit(&sfull[bi]);
+                if (last) {
+                    umma_commit(&qempty[qb]);
+                    ++piece;
+                }
+                if (i >= 1) ok = issue_pv(i - 1);
+                cursor_next(cur, prefix, p.B, G);
+            }
+            if (ok && !*s_abort) issue_pv(ntiles - 1);
+            umma_commit(done);
+            mbar_wait_teardown(done, 0);
+        }
+    } else {
+        // ================================================================ softmax + epilogue
+        const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
+        const int r = q4 * 32 + lane;            // tile position (S) / head dim (O, d = 128)
+        const int tg = tid - 64;                 // 0..127 within the group
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        // dim held in the O accumulator by this thread (M = 64 puts 16 rows in each quadrant)
+        const int odim = (D == 128) ? r : q4 * 16 + lane;
+        const bool has_dim = (D == 128) || lane < 16;
+        zero_empty_sequences<D>(p, prefix, P, tg, 128);
+        GroupSync128 gsync{grp, 0};
+        float m_run[N], l_part[N], acc[N], alpha_prev[N];
+        Cursor cur = (ntiles > 0) ? cursor_at(u0, prefix, p.B, G) : Cursor{0, 0, 0, 1};
+        int seq_b = 0;
+        long long piece_u0 = u0;
+        bool pending = false;     // O of the previous tile not folded in yet
+        bool ok = true;
+
+        // fold O of tile i into acc with the factor that tile's softmax computed
+        auto fold_o = [&](int i) -> bool {
+            const int bi = i & 1;
+            if (!mbar_wait(&ofull[bi], (i >> 1) & 1, ab)) return false;
+            tc_fence_after_sync();
+            uint32_t o[N];
+            tmem_ld_32x32b<N>(tmem + lane_off + 2 * N + bi * N, o);
+            tmem_wait_ld();
+            tc_fence_before_sync();
+            mbar_arrive(&ofree[bi]);
+#pragma unroll
+            for (int h = 0; h < N; ++h) acc[h] = fmaf(acc[h], alpha_prev[h], __uint_as_float(o[h]));
+            return true;
+        };
+
+        for (int i = 0; i < ntiles && ok; ++i) {
+            const long long u = u0 + i;
+            const bool first = (i == 0) || (cur.j == 0);
+            const bool last = (i + 1 == ntiles) || (cur.j + 1 == cur.tiles);
+            const int st = i % S, bi = i & 1;
+            if (first) {
+                piece_u0 = u;
+                seq_b = clamp_seq(__ldg(p.seq_lens + cur.b), p.Lmax);
+#pragma unroll
+                for (int h = 0; h < N; ++h) {
+                    m_run[h] = -INFINITY;
+                    l_part[h] = 0.f;
+                    acc[h] = 0.f;
+                    alpha_prev[h] = 0.f;
+                }
+            }
+            // ---- scores of this tile: S^T row r
+            if (!mbar_wait(&sfull[bi], (i >> 1) & 1, ab)) { ok = false; break; }
+            tc_fence_after_sync();
+            uint32_t sraw[N];
+            tmem_ld_32x32b<N>(tmem + lane_off + bi * N, sraw);
+            tmem_wait_ld();
+            tc_fence_before_sync();
+            mbar_arrive(&sfree[bi]);
+            const int valid_cnt = seq_b - cur.j * kTile;          // >= 1
+            const bool valid = r < valid_cnt;
+            float x[N];
+#pragma unroll
+            for (int h = 0; h < N; ++h) {
+                x[h] = valid ? __uint_as_float(sraw[h]) * p.scale_log2 : -INFINITY;
+                float m = x[h];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                if (lane == 0) red[(bi * 4 + q4) * N + h] = m;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&redbar[bi]);
+            if (!mbar_wait(&redbar[bi], (i >> 1) & 1, ab)) { ok = false; break; }
+            float alpha[N];
+#pragma unroll
+            for (int h = 0; h < N; ++h) {
+                const float* rr = red + bi * 4 * N + h;
+                const float tmax = fmaxf(fmaxf(rr[0], rr[N]), fmaxf(rr[2 * N], rr[3 * N]));
+                const float m_new = fmaxf(m_run[h], tmax);
+                alpha[h] = exp2f(m_run[h] - m_new);              // 0 on the first tile of a piece
+                x[h] = exp2f(x[h] - m_new);                      // 0 at invalid positions
+                l_part[h] = fmaf(l_part[h], alpha[h], x[h]);
+                m_run[h] = m_new;
+            }
+            // ---- fold the previous tile's O (its value GEMM has had a softmax to finish)
+            if (pending) {
+                if (!fold_o(i - 1)) { ok = false; break; }
+                pending = false;
+            }
+#pragma unroll
+            for (int h = 0; h < N; ++h) alpha_prev[h] = alpha[h];
+            // ---- the last tile of a sequence: clear V rows past the end (they may hold NaN)
+            if (valid_cnt < kTile) {
+                if (!mbar_wait(&vfull[st], (i / S) & 1, ab)) { ok = false; break; }
+                if (!valid) {
+                    uint8_t *vrow = smem + st * C::kStageBytes + C::kTileBytes + r * 128;
+#pragma unroll
+                    for (int c = 0; c < C::kBoxes; ++c) {
+                        uint4 *w = reinterpret_cast<uint4 *>(vrow + c * kBoxBytes);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) w[k] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            }
+            // ---- probabilities to shared memory as bf16 hi + lo (K-major, 128-byte swizzle)
+            {
+                uint8_t *phi = smem + C::kOffP + (bi * 2 + 0) * C::kPBytes + (r >> 6) * (N * 128);
+                uint8_t *plo = phi + C::kPBytes;
+                const int c = r & 63;
+#pragma unroll
+                for (int h = 0; h < N; ++h) {
+                    if (h < n) {
+                        const int off = h * 128 + ((((c >> 3) ^ (h & 7))) << 4) + (c & 7) * 2;
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(x[h]);
+                        const __nv_bfloat16 lo = __float2bfloat16_rn(x[h] - __bfloat162float(hi));
+                        *reinterpret_cast<__nv_bfloat16 *>(phi + off) = hi;
+                        *reinterpret_cast<__nv_bfloat16 *>(plo + off) = lo;
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&pfull[bi]);
+            pending = true;
+
+            if (last) {
+                if (!fold_o(i)) { ok = false; break; }
+                pending = false;
+                // ---- l = sum over the 128 position slots
+#pragma unroll
+                for (int h = 0; h < N; ++h) {
+                    float s = l_part[h];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                    if (lane == 0) lred[q4 * N + h] = s;
+                }
+                if (!gsync(ab)) { ok = false; break; }
+                const int seg = cur.b * G + cur.g;
+                const long long seg_a = (long long)G * prefix[cur.b] + (long long)cur.g * cur.tiles;
+                const bool owned = (piece_u0 == seg_a) && (cur.j + 1 == cur.tiles);
+                float *orow = p.out + ((size_t)cur.b * p.H + (size_t)cur.g * n) * D;
+                float *sp = slot_ptr(p, blockIdx.x + seg, D);
+#pragma unroll
+                for (int h = 0; h < N; ++h) {
+                    if (h < n) {
+                        const float L = lred[h] + lred[N + h] + lred[2 * N + h] + lred[3 * N + h];
+                        if (owned) {
+                            if (has_dim) orow[h * D + odim] = acc[h] / L;
+                        } else {
+                            if (has_dim) sp[2 * n + h * D + odim] = acc[h];
+                            if (tg == 0) {
+                                sp[h] = m_run[h];
+                                sp[n + h] = L;
+                            }
+                        }
+                    }
+                }
+                if (!owned) {
+                    __threadfence();
+                    if (!gsync(ab)) { ok = false; break; }
+                    const int c_lo = cta_of_tile(seg_a, W, Pw);
+                    const int c_hi = cta_of_tile(seg_a + cur.tiles - 1, W, Pw);
+                    if (tg == 0) {
+                        const int prev = atomicAdd(p.counters + seg, 1);
+                        *s_last = (prev == c_hi - c_lo) ? 1 : 0;
+                    }
+                    if (!gsync(ab)) { ok = false; break; }
+                    if (*s_last) {
+                        __threadfence();
+                        combine_segment<D>(p, c_lo + seg, c_hi - c_lo + 1, cur.b, cur.g, tg, 128);
+                        if (tg == 0) atomicExch(p.counters + seg, 0);
+                    }
+                }
+                if (!gsync(ab)) { ok = false; break; }   // lred and s_last are reused by the next piece
+            }
+            cursor_next(cur, prefix, p.B, G);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0 && lane == 0 && *s_abort) {
+        // let copies in flight land before the CTA's shared memory is released
+        for (int k = issued > S ? issued - S : 0; k < issued; ++k) {
+            mbar_wait_teardown(&kfull[k % S], (k / S) & 1);
+            mbar_wait_teardown(&vfull[k % S], (k / S) & 1);
+        }
+        for (int k = qissued > QB ? qissued - QB : 0; k < qissued; ++k)
+            mbar_wait_teardown(&qfull[k % QB], (k / QB) & 1);
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D, int N>
+cudaError_t launch_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const DecodeParams &p,
+                        int ctas, cudaStream_t stream) {
+    using C = TcCfg<D, N>;
+    auto kern = gqa_decode_tc_kernel<D, N>;
+    static unsigned long long attr_set = 0;   // one bit per device; setting twice is harmless
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(attr_set & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set |= bit;
+    }
+    kern<<<ctas, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, tq, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int tc_max_heads() { return 64; }
+
+int tc_rows_for(int n) { return n <= 16 ? 16 : (n <= 32 ? 32 : 64); }
+
+cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
+                             const DecodeParams &p, int D, int ctas, cudaStream_t stream) {
+    const int rows = tc_rows_for(p.n);
+    if (D == 128) {
+        if (rows == 16) return launch_tc_t<128, 16>(tk, tv, tq, p, ctas, stream);
+        if (rows == 32) return launch_tc_t<128, 32>(tk, tv, tq, p, ctas, stream);
+        return launch_tc_t<128, 64>(tk, tv, tq, p, ctas, stream);
+    }
+    if (rows == 16) return launch_tc_t<64, 16>(tk, tv, tq, p, ctas, stream);
+    if (rows == 32) return launch_tc_t<64, 32>(tk, tv, tq, p, ctas, stream);
+    return launch_tc_t<64, 64>(tk, tv, tq, p, ctas, stream);
 }
 
 }  // namespace gqa

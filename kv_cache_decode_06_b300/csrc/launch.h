@@ -13,6 +13,7 @@ cudaError_t launch_decode_simt(const CUtensorMap &tk, const CUtensorMap &tv, con
                                int ctas, cudaStream_t stream);
 
 int tc_max_heads();
+int tc_rows_for(int n);   // rows of the q tensor-map box (n rounded up to 16, 32 or 64)
 cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
                              const DecodeParams &p, int D, int ctas, cudaStream_t stream);
 

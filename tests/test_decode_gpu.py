@@ -175,7 +175,7 @@ def test_meanpool_pages_layout_bit_exact():
     """The pages' [d_model, H*h] projection pooled per column block."""
     from kv_cache_decode_06_b300.inputs import make_meanpool_input
     H, G, h, dm = 8, 2, 64, 512
-    w = make_meanpool_input(H, G, h, dm, outer=dm).reshape(dm, H, h)
+    w = make_meanpool_input(H, G, h, 1, outer=dm)          # [d_model, H, h] = [d_model, H*h]
     got = gqa.meanpool_kv_strided(torch.from_numpy(w).cuda(), G).cpu().numpy()
     ref = oracle.meanpool_f32(w, H, G, head_axis=1)
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
