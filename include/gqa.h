@@ -147,6 +147,37 @@ int gqa_decode_select_path(int B, int H, int G, int d, int Lmax);
 gqa_status gqa_decode_read_flags(void *workspace, uint32_t *flags, int clear, void *stream);
 
 /*
+ * gqa_decode for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a packaging variant of gqa_decode.
+ *
+ * Who needs it: callers with no way to hand over a workspace, for example a
+ * plugin that only receives its input and output tensors from a host framework
+ * that owns all device memory, a runtime that reserves its memory once at
+ * start-up and may not allocate afterwards, or a latency-critical loop that
+ * cannot pay for cudaMalloc's implicit device synchronisation.
+ *
+ * Instead of a caller workspace it uses a scratch array compiled into the
+ * library: GQA_NOALLOC_WORKSPACE_BYTES of device memory that every GPU loading
+ * the library holds until the process exits.  Arguments, layouts, results and
+ * error codes are those of gqa_decode, except:
+ *   - shapes whose gqa_decode_workspace_size exceeds GQA_NOALLOC_WORKSPACE_BYTES
+ *     return GQA_ERR_WORKSPACE and enqueue nothing;
+ *   - the first call on a device looks up the scratch address on that device
+ *     (make it before any stream capture on that device);
+ *   - every call clears the flag word and the counters of the scratch on
+ *     `stream` before the kernel (cudaMemsetAsync, no allocation);
+ *   - all calls share the one array: calls that overlap on the GPU (other
+ *     streams, other host threads) race and corrupt each other's results, so
+ *     order them on one stream or synchronise between them.
+ * It never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+#define GQA_NOALLOC_WORKSPACE_BYTES (8u << 20)
+
+gqa_status gqa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *seq_lens, float *out,
+                              int B, int H, int G, int d, int Lmax, float scale, void *stream);
+
+/*
  * Mean-pool conversion of K (or V) projection heads into G groups.
  * ["Grouped-query attention (GQA)" concept page, "Converted and uptrained
  *  checkpoints" and the conversion pseudocode; arxiv:2305.13245 §2.1]

@@ -131,6 +131,10 @@ int auto_path(int H, int G, int d) {
 
 }  // namespace
 
+namespace gqa {
+size_t decode_workspace_zero_prefix(int B, int G) { return kHeaderBytes + counters_bytes(B, G); }
+}  // namespace gqa
+
 extern "C" {
 
 const char *gqa_status_string(int status) {

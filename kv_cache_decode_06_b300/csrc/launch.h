@@ -17,6 +17,10 @@ int tc_rows_for(int n);   // rows of the q tensor-map box (n rounded up to 16, 3
 cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
                              const DecodeParams &p, int D, int ctas, cudaStream_t stream);
 
+// Leading bytes of a decode workspace that must be zero before a call on a
+// fresh (or differently shaped) workspace: the flag word and the counters.
+size_t decode_workspace_zero_prefix(int B, int G);
+
 cudaError_t launch_meanpool(const float *w_in, float *w_out, long long outer, int H, int G, long long inner,
                             cudaStream_t stream);
 

@@ -28,7 +28,9 @@ FLAG_WAIT_TIMEOUT = 0x2
 
 # Every symbol include/gqa.h declares.
 EXPORTS = ("gqa_status_string", "gqa_abi_version", "gqa_decode_workspace_size", "gqa_decode", "gqa_decode_ex",
-           "gqa_decode_select_path", "gqa_decode_read_flags", "gqa_meanpool_kv", "gqa_meanpool_kv_strided")
+           "gqa_decode_select_path", "gqa_decode_read_flags", "gqa_meanpool_kv", "gqa_meanpool_kv_strided",
+           "gqa_decode_noalloc")
+NOALLOC_WORKSPACE_BYTES = 8 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +72,8 @@ def load(path: Optional[str] = None):
         lib.gqa_decode_select_path.argtypes = [I, I, I, I, I]
         lib.gqa_decode_read_flags.restype = I
         lib.gqa_decode_read_flags.argtypes = [V, ctypes.POINTER(ctypes.c_uint32), I, V]
+        lib.gqa_decode_noalloc.restype = I
+        lib.gqa_decode_noalloc.argtypes = [V, V, V, V, V, I, I, I, I, I, F, V]
         lib.gqa_meanpool_kv.restype = I
         lib.gqa_meanpool_kv.argtypes = [V, V, I, I, I, I, V]
         lib.gqa_meanpool_kv_strided.restype = I
@@ -149,6 +153,32 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_le
                                 out.data_ptr(), workspace.data_ptr(), workspace.numel(), B, H, G, d, Lmax,
                                 float(scale), _stream_handle(stream, dev), ctypes.byref(opts)),
            "gqa_decode")
+    return out
+
+
+def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens: torch.Tensor,
+                   out: torch.Tensor, scale: Optional[float] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """:func:`decode` without a workspace, for callers that cannot allocate device memory.
+
+    The library's own scratch array (8 MiB per GPU) stands in for the
+    workspace, so ``out`` must be passed in.  Calls that overlap on the GPU
+    share that array and race; shapes needing more scratch raise GQAError
+    (GQA_ERR_WORKSPACE).
+    """
+    dev = q.device
+    B, H, d = q.shape
+    _, G, Lmax, _ = k_cache.shape
+    for t, name, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
+                        (v_cache, "v_cache", torch.bfloat16), (seq_lens, "seq_lens", torch.int32),
+                        (out, "out", torch.float32)):
+        _require(t, name, dt, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(load().gqa_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seq_lens.data_ptr(),
+                                     out.data_ptr(), B, H, G, d, Lmax, float(scale),
+                                     _stream_handle(stream, dev)),
+           f"gqa_decode_noalloc (scratch limit {NOALLOC_WORKSPACE_BYTES} bytes)")
     return out
 
 
