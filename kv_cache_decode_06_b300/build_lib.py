@@ -1,9 +1,12 @@
 """Build the CUDA library ``libgqa_b300.so`` in-tree with nvcc for sm_103a.
 
-Usage: ``python -m kv_cache_decode_06_b300.build_lib [--force] [--verbose]``.
+Usage: ``python -m kv_cache_decode_06_b300.build_lib [--force] [--verbose] [--trace]``.
 The shared library lands next to this file and is what the Python binding and
 any C caller load.  ``-Xptxas -v`` output (registers, spills, shared memory) is
-printed with ``--verbose``.
+printed with ``--verbose``.  ``--trace`` builds ``libgqa_b300_trace.so`` instead:
+the same library compiled with -DGQA_TRACE, whose tensor-core decode kernel
+records a per-CTA timeline of its pipeline events (clock64 stamps) in a device
+array that ``gqa_trace_copy(dst, bytes)`` copies to the host.
 """
 from __future__ import annotations
 
@@ -20,6 +23,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libgqa_b300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
+TRACE_LIB_PATH = os.path.join(HERE, "libgqa_b300_trace.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -38,24 +42,28 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \
         glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
     return any(os.path.getmtime(f) > t for f in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not _stale():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    lib = TRACE_LIB_PATH if trace else LIB_PATH
+    if not force and not _stale(lib):
+        return lib
+    build_dir = BUILD_DIR + ("_trace" if trace else "")
+    os.makedirs(build_dir, exist_ok=True)
     objs = []
     extra = ["-Xptxas", "-v"] if verbose else []
+    if trace:
+        extra += ["-DGQA_TRACE"]
     procs = []
     for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
         objs.append(obj)
@@ -69,18 +77,19 @@ def build(force: bool = False, verbose: bool = False) -> str:
             sys.stdout.write("FAILED: " + " ".join(cmd) + "\n")
     if failed:
         raise RuntimeError("nvcc failed building libgqa_b300.so")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"], check=True)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib)
+    return lib
 
 
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
+    ap.add_argument("--trace", action="store_true")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose))
+    print(build(force=a.force, verbose=a.verbose, trace=a.trace))
 
 
 if __name__ == "__main__":

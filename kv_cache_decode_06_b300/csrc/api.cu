@@ -77,7 +77,7 @@ size_t counters_bytes(int B, int G) { return align_up((size_t)B * G * sizeof(int
 size_t workspace_bytes_for(int B, int H, int G, int d) {
     const int n = H / G;
     const size_t slots = (size_t)GQA_MAX_CTAS + (size_t)B * G;
-    return kHeaderBytes + counters_bytes(B, G) + slots * (size_t)n * (d + 2) * sizeof(float);
+    return kHeaderBytes + counters_bytes(B, G) + slots * (size_t)gqa::slot_floats(n, d) * sizeof(float);
 }
 
 gqa_status check_shape(int B, int H, int G, int d, int Lmax) {

@@ -137,33 +137,105 @@ __device__ void zero_empty_sequences(const DecodeParams &p, const int *prefix, i
     }
 }
 
+// Partial slot layout (floats): m[n] | l[n] | pad to a multiple of 4 | acc[n][D].
+// The acc block starts 16-byte aligned so it can be read as float4.
+__host__ __device__ constexpr int slot_acc_offset(int n) { return (2 * n + 3) & ~3; }
+__host__ __device__ constexpr long long slot_floats(int n, int D) { return slot_acc_offset(n) + (long long)n * D; }
+
 __device__ __forceinline__ float *slot_ptr(const DecodeParams &p, int slot, int D) {
-    return p.partials + (size_t)slot * p.n * (D + 2);
+    return p.partials + (size_t)slot * (size_t)slot_floats(p.n, D);
 }
 
-// Merge every piece of segment (b, g) from its slots and write the n output rows.
-// Called by `nthreads` threads with ids 0..nthreads-1 after the caller has made
-// the other pieces' writes visible (__threadfence after the last arrival).
-template <int D>
-__device__ void combine_segment(const DecodeParams &p, int first_slot, int count, int b, int g, int tid,
-                                int nthreads) {
-    const int n = p.n;
-    const size_t stride = (size_t)n * (D + 2);
-    const float *base = p.partials + (size_t)first_slot * stride;
-    float *orow = p.out + ((size_t)b * p.H + (size_t)g * n) * D;
-    for (int idx = tid; idx < n * D; idx += nthreads) {
-        const int h = idx / D, dim = idx - h * D;
-        float M = -INFINITY;
-        for (int k = 0; k < count; ++k) M = fmaxf(M, __ldcg(base + k * stride + h));
-        float L = 0.f, A = 0.f;
-        for (int k = 0; k < count; ++k) {
-            const float *sl = base + k * stride;
-            const float w = exp2f(__ldcg(sl + h) - M);
-            L = fmaf(__ldcg(sl + n + h), w, L);
-            A = fmaf(__ldcg(sl + 2 * n + h * D + dim), w, A);
-        }
-        orow[idx] = A / L;
+// 2^x with the hardware approximation (relative error ~2^-22); 2^-inf = +0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Synchronisation of the 128 compute threads through an mbarrier with a bounded
+// wait, so an aborting CTA can never hang in it.
+struct GroupSync {
+    uint64_t *bar;
+    uint32_t phase;
+    __device__ bool operator()(const AbortState &ab) {
+        mbar_arrive(bar);
+        const bool ok = mbar_wait(bar, phase & 1u, ab);
+        ++phase;
+        return ok;
     }
+};
+
+// Merge the `count` pieces of segment (b, g), stored in consecutive slots from
+// `first_slot`, and write its n output rows:
+//   M_h = max_k m_kh,  L_h = sum_k l_kh 2^(m_kh - M_h),
+//   out[h, :] = (sum_k acc_k[h, :] 2^(m_kh - M_h)) / L_h.
+// Run by the 128 compute threads (tid 0..127) after the caller has made the
+// other pieces' writes visible (a fence after observing the last arrival).
+// `scratch` holds 2 * n floats of shared memory.  Returns false if the CTA is
+// aborting.  Reads go to L2 (ld.cg): the partials were written by other SMs.
+template <int D>
+__device__ bool combine_segment(const DecodeParams &p, int first_slot, int count, int b, int g, int tid,
+                                float *scratch, GroupSync &sync, const AbortState &ab) {
+    const int n = p.n;
+    const long long stride = slot_floats(n, D);
+    const int aoff = slot_acc_offset(n);
+    const float *base = p.partials + (size_t)first_slot * (size_t)stride;
+    const int warp = tid >> 5, lane = tid & 31;
+    // ---- per head: global maximum and normaliser (warp w takes heads w, w+4, ...)
+    for (int h = warp; h < n; h += 4) {
+        float mk = -INFINITY, M = -INFINITY;
+        if (lane < count) mk = __ldcg(base + (size_t)lane * stride + h);
+        M = mk;
+        for (int k = lane + 32; k < count; k += 32) M = fmaxf(M, __ldcg(base + (size_t)k * stride + h));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = 0.f;
+        if (lane < count) L = __ldcg(base + (size_t)lane * stride + n + h) * ex2(mk - M);
+        for (int k = lane + 32; k < count; k += 32) {
+            const float *sk = base + (size_t)k * stride;
+            L = fmaf(__ldcg(sk + n + h), ex2(__ldcg(sk + h) - M), L);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (lane == 0) {
+            scratch[h] = M;
+            scratch[n + h] = L;
+        }
+    }
+    if (!sync(ab)) return false;
+    // ---- outputs, four consecutive dims of one head per float4
+    float4 *orow = reinterpret_cast<float4 *>(p.out + ((size_t)b * p.H + (size_t)g * n) * D);
+    const int nd4 = n * D / 4;
+    for (int e = tid; e < nd4; e += 128) {
+        const int h = (e * 4) / D;
+        const float M = scratch[h];
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        int k = 0;
+        for (; k + 2 <= count; k += 2) {
+            const float *s0 = base + (size_t)k * stride, *s1 = s0 + stride;
+            const float m0 = __ldcg(s0 + h), m1 = __ldcg(s1 + h);
+            const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(s0 + aoff) + e);
+            const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(s1 + aoff) + e);
+            const float w0 = ex2(m0 - M), w1 = ex2(m1 - M);
+            a.x = fmaf(v1.x, w1, fmaf(v0.x, w0, a.x));
+            a.y = fmaf(v1.y, w1, fmaf(v0.y, w0, a.y));
+            a.z = fmaf(v1.z, w1, fmaf(v0.z, w0, a.z));
+            a.w = fmaf(v1.w, w1, fmaf(v0.w, w0, a.w));
+        }
+        if (k < count) {
+            const float *s0 = base + (size_t)k * stride;
+            const float w0 = ex2(__ldcg(s0 + h) - M);
+            const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(s0 + aoff) + e);
+            a.x = fmaf(v0.x, w0, a.x);
+            a.y = fmaf(v0.y, w0, a.y);
+            a.z = fmaf(v0.z, w0, a.z);
+            a.w = fmaf(v0.w, w0, a.w);
+        }
+        const float L = scratch[n + h];
+        orow[e] = make_float4(a.x / L, a.y / L, a.z / L, a.w / L);
+    }
+    return true;
 }
 
 }  // namespace gqa

@@ -45,19 +45,6 @@ struct SimtCfg {
     static constexpr int kSmemBytes = kOffFlags + 16 + 1024;               // + alignment slack
 };
 
-// Named-barrier-free sync of the 128 compute threads: an mbarrier with a
-// bounded wait, so an aborting CTA can never hang here.
-struct GroupSync {
-    uint64_t *bar;
-    uint32_t phase;
-    __device__ bool operator()(const AbortState &ab) {
-        mbar_arrive(bar);
-        const bool ok = mbar_wait(bar, phase & 1u, ab);
-        ++phase;
-        return ok;
-    }
-};
-
 template <int D, int NMAX>
 __global__ void __launch_bounds__(SimtCfg<D, NMAX>::kThreads, 1)
     gqa_decode_simt_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -200,8 +187,8 @@ __global__ void __launch_bounds__(SimtCfg<D, NMAX>::kThreads, 1)
                     for (int o = 16; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
                     const float m_new = fmaxf(m_run[h], mt);
                     const bool none = (m_new == -INFINITY);     // no valid position seen yet
-                    const float alpha = none ? 1.f : exp2f(m_run[h] - m_new);
-                    const float pr = none ? 0.f : exp2f(x - m_new);
+                    const float alpha = none ? 1.f : ex2(m_run[h] - m_new);
+                    const float pr = none ? 0.f : ex2(x - m_new);
                     m_run[h] = m_new;
                     l_lane[h] = fmaf(l_lane[h], alpha, pr);
 #pragma unroll
@@ -272,7 +259,7 @@ __global__ void __launch_bounds__(SimtCfg<D, NMAX>::kThreads, 1)
                     float L = 0.f, A = 0.f;
 #pragma unroll
                     for (int w = 0; w < C::kWarps; ++w) {
-                        const float sc = exp2f(m_s[w * NMAX + h] - M);   // 0 for a warp with no position
+                        const float sc = ex2(m_s[w * NMAX + h] - M);   // 0 for a warp with no position
                         L = fmaf(l_s[w * NMAX + h], sc, L);
                         A = fmaf(acc_s[(w * NMAX + h) * D + dim], sc, A);
                     }
@@ -283,22 +270,25 @@ __global__ void __launch_bounds__(SimtCfg<D, NMAX>::kThreads, 1)
                             sp[h] = M;
                             sp[n + h] = L;
                         }
-                        sp[2 * n + idx] = A;
+                        sp[slot_acc_offset(n) + idx] = A;
                     }
                 }
                 if (!owned) {
-                    __threadfence();
+                    // every thread's partial writes reach L2 before thread 0 announces them (the
+                    // barrier orders them before thread 0's fence, which is cumulative)
                     if (!gsync(ab)) break;
                     const int c_lo = cta_of_tile(seg_a, W, Pw);
                     const int c_hi = cta_of_tile(seg_a + cur.tiles - 1, W, Pw);
                     if (tid == 0) {
+                        __threadfence();
                         const int prev = atomicAdd(p.counters + seg, 1);
                         *s_last = (prev == c_hi - c_lo) ? 1 : 0;
                     }
                     if (!gsync(ab)) break;
                     if (*s_last) {
                         __threadfence();
-                        combine_segment<D>(p, c_lo + seg, c_hi - c_lo + 1, cur.b, cur.g, tid, C::kWarps * 32);
+                        if (!combine_segment<D>(p, c_lo + seg, c_hi - c_lo + 1, cur.b, cur.g, tid, m_s, gsync, ab))
+                            break;
                         if (tid == 0) atomicExch(p.counters + seg, 0);
                     }
                 }

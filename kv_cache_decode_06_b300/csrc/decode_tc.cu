@@ -14,15 +14,22 @@
 //
 // Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
 // owner, warps 2-5 = softmax + epilogue (thread <-> TMEM lane: a position of
-// the tile for S, a head dim for O).  Per tile the softmax group
+// the tile for S, a head dim for O).
+//
+// Producer and MMA issuer are event loops: each issues the next operation
+// whose inputs are ready.  K slot s is handed back as soon as the score GEMM of
+// its tile has read it, V slot s after the value GEMM, so K loads run ahead of
+// V loads and more bytes are in flight.  Per tile the softmax group
 //   1. loads its S row, reduces the per-head maximum over the 128 positions
 //      (transposed butterfly in the warp, then the 4 warps via shared memory),
 //   2. writes P(i) and hands it to the MMA warp,
 //   3. folds the previous tile's O into register accumulators with that tile's
 //      rescale factor (so TMEM never needs rescaling).
-// The MMA warp issues each GEMM as soon as its own inputs are ready, so the value
-// GEMM of tile i never waits for tile i+1's data.  Work split, pieces and the
-// last-arriver combine are shared with the CUDA-core path.
+// Work split, pieces and the last-arriver combine are shared with the CUDA-core
+// path (decode_common.cuh).
+//
+// Build with -DGQA_TRACE for a per-CTA timeline (clock64 stamps of every
+// pipeline event, see the slot map at TraceSlot) readable with gqa_trace_copy.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -31,43 +38,98 @@
 #include "launch.h"
 #include "tc_ptx.cuh"
 
+#ifdef GQA_TRACE
+namespace gqa {
+constexpr int kTraceSlots = 1024;
+__device__ unsigned long long g_trace[1024 * kTraceSlots];
+}  // namespace gqa
+#define GQA_TRACE_AT(slot, value)                                                                         \
+    do {                                                                                                  \
+        if ((slot) < gqa::kTraceSlots)                                                                    \
+            gqa::g_trace[(size_t)blockIdx.x * gqa::kTraceSlots + (slot)] = (unsigned long long)(value);  \
+    } while (0)
+extern "C" int gqa_trace_copy(void *dst, size_t bytes) {
+    if (bytes > sizeof(gqa::g_trace)) bytes = sizeof(gqa::g_trace);
+    return (int)cudaMemcpyFromSymbol(dst, gqa::g_trace, bytes);
+}
+#else
+#define GQA_TRACE_AT(slot, value) \
+    do {                          \
+    } while (0)
+#endif
+
 namespace gqa {
 
 namespace {
 
+// Trace slots per CTA (clock64 unless noted).  Per-tile slots hold tiles 0..127.
+enum TraceSlot {
+    kTrGlobalStart = 0,   // %globaltimer at entry (ns)
+    kTrStart = 1,         // entry
+    kTrSetup = 2,         // barriers, TMEM and the tile prefix ready
+    kTrEnd = 3,           // exit
+    kTrTiles = 4,         // tiles of this CTA (a count)
+    kTrGlobalEnd = 5,     // %globaltimer at exit (ns)
+    kTrFirstQ = 6,        // first Q copy issued
+    kTrFirstK = 7,        // first K copy issued
+    kTrKIssue = 16,       // + i: K copy of tile i issued
+    kTrSIssue = 144,      // + i: score GEMM of tile i issued
+    kTrPvIssue = 272,     // + i: value GEMM of tile i issued
+    kTrSFull = 400,       // + i: softmax saw S(i)
+    kTrMax = 528,         // + i: tile maximum agreed
+    kTrPFull = 656,       // + i: P(i) handed over
+    kTrFold = 784,        // + i: previous O folded
+    kTrPieceEnd = 912     // + 2k / + 2k + 1: start / end of the k-th piece epilogue
+};
+
 constexpr int kSmemLimit = 232448;   // 227 KB opt-in per CTA
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
 // D = head dim, N = MMA N (>= 16), NH = heads held per thread (power of two >= n).
 template <int D, int N, int NH>
 struct TcCfg {
     static constexpr int kBoxes = D / kBoxCols;
     static constexpr int kTileBytes = kBoxes * kBoxBytes;        // one K or V tile (128 positions)
-    static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQBytes = kBoxes * N * 128;             // one Q buffer (N rows x d)
     static constexpr int kPBytes = 2 * N * 128;                  // one P part: N rows x 128 positions
-    static constexpr int kMisc = 8192 + (kMaxBatch + 1) * 4 + 1024;
-    static constexpr int kQBuf = (2 * kQBytes + 4 * kPBytes + 2 * kStageBytes + kMisc <= kSmemLimit) ? 2 : 1;
-    static constexpr int kFixed = kQBuf * kQBytes + 4 * kPBytes;
-    static constexpr int kStagesFit = (kSmemLimit - kMisc - kFixed) / kStageBytes;
-    static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+    // small shared state, in floats
+    static constexpr int kRedF = 2 * 4 * NH;                     // [2][4 warps][NH] tile maxima
+    static constexpr int kLredF = 4 * NH;                        // [4 warps][NH] l sums
+    static constexpr int kMF = 3 * NH;                           // [3][NH] running max after tile i
+    static constexpr int kAF = 3 * NH;                           // [3][NH] rescale factor of tile i
+    static constexpr int kCombF = 2 * NH;                        // combine scratch (M, L per head)
+    static constexpr int kSmallBytes = 4 * (kRedF + kLredF + kMF + kAF + kCombF) + 32 * 4 + (kMaxBatch + 1) * 4;
+    static constexpr int bar_bytes(int S, int QB) { return (4 * S + 2 * QB + 12 + 2) * 8 + 16; }
+    static constexpr int fixed_bytes(int S, int QB) {
+        return QB * kQBytes + 4 * kPBytes + kSmallBytes + bar_bytes(S, QB) + 1024 /* alignment slack */;
+    }
+    static constexpr int stages_for(int QB) { return cmin(8, (kSmemLimit - fixed_bytes(8, QB)) / (2 * kTileBytes)); }
+    static constexpr int kQBuf = stages_for(2) >= 3 || stages_for(1) == stages_for(2) ? 2 : 1;
+    static constexpr int kStages = stages_for(kQBuf);
     static_assert(kStages >= 2, "shared memory too small for two stages");
-    static constexpr int kOffQ = kStages * kStageBytes;
-    static constexpr int kOffP = kOffQ + kQBuf * kQBytes;        // [2 buffers][hi, lo]
-    static constexpr int kOffRed = kOffP + 4 * kPBytes;          // f32 [2][4][NH] per-warp tile maxima
-    static constexpr int kOffLred = kOffRed + 2 * 4 * NH * 4;    // f32 [4][NH] per-warp l sums
-    static constexpr int kOffM = kOffLred + 4 * NH * 4;          // f32 [3][NH] running max after tile i
-    static constexpr int kOffA = kOffM + 3 * NH * 4;             // f32 [3][NH] rescale factor of tile i
-    static constexpr int kOffPrefix = kOffA + 3 * NH * 4;        // i32 [kMaxBatch + 1]
-    static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 1) * 4;
+    // layout (offsets from the 1024-aligned base)
+    static constexpr int kOffK = 0;                                       // [S] K tiles
+    static constexpr int kOffV = kStages * kTileBytes;                    // [S] V tiles
+    static constexpr int kOffQ = 2 * kStages * kTileBytes;                // [QB] Q buffers
+    static constexpr int kOffP = kOffQ + kQBuf * kQBytes;                 // [2 buffers][hi, lo]
+    static constexpr int kOffRed = kOffP + 4 * kPBytes;
+    static constexpr int kOffLred = kOffRed + kRedF * 4;
+    static constexpr int kOffM = kOffLred + kLredF * 4;
+    static constexpr int kOffA = kOffM + kMF * 4;
+    static constexpr int kOffComb = kOffA + kAF * 4;
+    static constexpr int kOffPrefix = kOffComb + kCombF * 4;              // i32 [kMaxBatch + 1]
+    static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 1) * 4;  // i32 [32]
     static constexpr int kOffBar = (kOffScratch + 32 * 4 + 7) / 8 * 8;
-    // barriers: kfull[S] vfull[S] kvempty[S] qfull[QB] qempty[QB] sfull[2] sfree[2] pfull[2]
-    //           ofull[2] ofree[2] red[2] grp done
-    static constexpr int kNumBars = 3 * kStages + 2 * kQBuf + 12 + 2;
+    // barriers: kfull[S] vfull[S] kempty[S] vempty[S] qfull[QB] qempty[QB] sfull[2] sfree[2]
+    //           pfull[2] ofull[2] ofree[2] red[2] grp done
+    static constexpr int kNumBars = 4 * kStages + 2 * kQBuf + 12 + 2;
     static constexpr int kOffFlags = kOffBar + kNumBars * 8;     // abort, last, tmem base
     static constexpr int kSmemBytes = kOffFlags + 16 + 1024;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory layout too large");
+    static_assert(NH < 4 || (kOffRed % 16 == 0 && kOffLred % 16 == 0 && kOffM % 16 == 0 && kOffA % 16 == 0),
+                  "float4 alignment");
     static constexpr int kThreads = 192;
     static constexpr int kTmemCols = (4 * N <= 32) ? 32 : (4 * N <= 64) ? 64 : (4 * N <= 128) ? 128 : 256;
     static constexpr int kPvM = (D == 128) ? 128 : 64;
@@ -114,16 +176,66 @@ __device__ __forceinline__ void butterfly_store(const float (&v)[NH], int lane, 
     }
 }
 
-struct GroupSync128 {
-    uint64_t *bar;
-    uint32_t phase;
-    __device__ bool operator()(const AbortState &ab) {
-        mbar_arrive(bar);
-        const bool ok = mbar_wait(bar, phase & 1u, ab);
-        ++phase;
-        return ok;
+// out[h] = op(src[0*NH + h], src[1*NH + h], src[2*NH + h], src[3*NH + h]) for the
+// four warps' per-head values, read as float4 where NH allows.
+template <int NH, bool kMax>
+__device__ __forceinline__ void reduce4(const float *src, float (&out)[NH]) {
+    if constexpr (NH >= 4) {
+#pragma unroll
+        for (int h = 0; h < NH; h += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(src + h);
+            const float4 b = *reinterpret_cast<const float4 *>(src + NH + h);
+            const float4 c = *reinterpret_cast<const float4 *>(src + 2 * NH + h);
+            const float4 d = *reinterpret_cast<const float4 *>(src + 3 * NH + h);
+            if (kMax) {
+                out[h] = fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x));
+                out[h + 1] = fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y));
+                out[h + 2] = fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z));
+                out[h + 3] = fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w));
+            } else {
+                out[h] = (a.x + b.x) + (c.x + d.x);
+                out[h + 1] = (a.y + b.y) + (c.y + d.y);
+                out[h + 2] = (a.z + b.z) + (c.z + d.z);
+                out[h + 3] = (a.w + b.w) + (c.w + d.w);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+            const float a = src[h], b = src[NH + h], c = src[2 * NH + h], d = src[3 * NH + h];
+            out[h] = kMax ? fmaxf(fmaxf(a, b), fmaxf(c, d)) : (a + b) + (c + d);
+        }
     }
-};
+}
+
+template <int NH>
+__device__ __forceinline__ void load_vec(const float *src, float (&out)[NH]) {
+    if constexpr (NH >= 4) {
+#pragma unroll
+        for (int h = 0; h < NH; h += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(src + h);
+            out[h] = a.x;
+            out[h + 1] = a.y;
+            out[h + 2] = a.z;
+            out[h + 3] = a.w;
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) out[h] = src[h];
+    }
+}
+
+template <int NH>
+__device__ __forceinline__ void store_vec(float *dst, const float (&v)[NH]) {
+    if constexpr (NH >= 4) {
+#pragma unroll
+        for (int h = 0; h < NH; h += 4)
+            *reinterpret_cast<float4 *>(dst + h) = make_float4(v[h], v[h + 1], v[h + 2], v[h + 3]);
+    } else {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) dst[h] = v[h];
+    }
+}
 
 template <int D, int N, int NH>
 __global__ void __launch_bounds__(192, 1)
@@ -137,11 +249,12 @@ __global__ void __launch_bounds__(192, 1)
     float *lred = reinterpret_cast<float *>(smem + C::kOffLred);
     float *mrun_s = reinterpret_cast<float *>(smem + C::kOffM);
     float *alpha_s = reinterpret_cast<float *>(smem + C::kOffA);
+    float *comb = reinterpret_cast<float *>(smem + C::kOffComb);
     int *prefix = reinterpret_cast<int *>(smem + C::kOffPrefix);
     int *scratch = reinterpret_cast<int *>(smem + C::kOffScratch);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
-    uint64_t *kfull = bars, *vfull = kfull + S, *kvempty = vfull + S;
-    uint64_t *qfull = kvempty + S, *qempty = qfull + QB;
+    uint64_t *kfull = bars, *vfull = kfull + S, *kempty = vfull + S, *vempty = kempty + S;
+    uint64_t *qfull = vempty + S, *qempty = qfull + QB;
     uint64_t *sfull = qempty + QB, *sfree = sfull + 2, *pfull = sfree + 2, *ofull = pfull + 2, *ofree = ofull + 2;
     uint64_t *redbar = ofree + 2, *grp = redbar + 2, *done = grp + 1;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::kOffFlags);
@@ -151,12 +264,17 @@ __global__ void __launch_bounds__(192, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = gridDim.x;
     const AbortState ab{s_abort, p.flags};
+    if (tid == 64) {
+        GQA_TRACE_AT(kTrGlobalStart, globaltimer_ns());
+        GQA_TRACE_AT(kTrStart, clock64());
+    }
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&kfull[s], 1);
             mbar_init(&vfull[s], 1);
-            mbar_init(&kvempty[s], 1);
+            mbar_init(&kempty[s], 1);
+            mbar_init(&vempty[s], 1);
         }
         for (int s = 0; s < QB; ++s) {
             mbar_init(&qfull[s], 1);
@@ -188,6 +306,7 @@ __global__ void __launch_bounds__(192, 1)
     build_prefix(p.seq_lens, p.B, p.Lmax, prefix, scratch, p.flags);   // ends with __syncthreads
     tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
+    if (tid == 64) GQA_TRACE_AT(kTrSetup, clock64());
 
     const int G = p.G, n = p.n;
     const long long W = (long long)G * prefix[p.B];
@@ -198,45 +317,81 @@ __global__ void __launch_bounds__(192, 1)
         u1 = range_start(blockIdx.x + 1, W, Pw);
     }
     const int ntiles = (int)(u1 - u0);
-    int issued = 0, qissued = 0;
+    if (tid == 64) GQA_TRACE_AT(kTrTiles, ntiles);
+    int kissued = 0, vissued = 0, qissued = 0;
 
     if (warp == 0) {
         // ================================================================ producer
         if (lane == 0 && ntiles > 0) {
             const uint64_t pol_kv = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
-            Cursor cur = cursor_at(u0, prefix, p.B, G);
+            Cursor kc = cursor_at(u0, prefix, p.B, G);
+            Cursor vc = kc;
             int piece = 0;
-            for (int i = 0; i < ntiles; ++i) {
-                const bool first = (i == 0) || (cur.j == 0);
-                const bool last = (i + 1 == ntiles) || (cur.j + 1 == cur.tiles);
-                if (first) {
-                    const int qb = piece % QB;
-                    if (piece >= QB && !mbar_wait(&qempty[qb], ((piece / QB) - 1) & 1, ab)) break;
-                    mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
-                    uint8_t *qdst = smem + C::kOffQ + qb * C::kQBytes;
-                    const int y = cur.b * p.H + cur.g * n;
+            uint32_t idle = 0;
+            uint64_t idle_t0 = 0;
+            while (vissued < ntiles) {
+                bool progress = false;
+                // ---- K of tile kissued (and Q when it starts a piece)
+                if (kissued < ntiles) {
+                    const int i = kissued;
+                    const bool first = (i == 0) || (kc.j == 0);
+                    const bool last = (i + 1 == ntiles) || (kc.j + 1 == kc.tiles);
+                    const int st = i % S, qb = piece % QB;
+                    if ((!first || piece < QB || mbar_test_wait(&qempty[qb], ((piece / QB) - 1) & 1)) &&
+                        (i < S || mbar_test_wait(&kempty[st], ((i / S) - 1) & 1))) {
+                        if (first) {
+                            mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
+                            uint8_t *qdst = smem + C::kOffQ + qb * C::kQBytes;
+                            const int y = kc.b * p.H + kc.g * n;
 #pragma unroll
-                    for (int c = 0; c < C::kBoxes; ++c)
-                        tma_load_2d(qdst + c * N * 128, &tm_q, c * kBoxCols, y, &qfull[qb], pol_q);
-                    ++qissued;
+                            for (int c = 0; c < C::kBoxes; ++c)
+                                tma_load_2d(qdst + c * N * 128, &tm_q, c * kBoxCols, y, &qfull[qb], pol_q);
+                            ++qissued;
+                            if (i == 0) GQA_TRACE_AT(kTrFirstQ, clock64());
+                        }
+                        uint8_t *kdst = smem + C::kOffK + st * C::kTileBytes;
+                        const int z = kc.b * G + kc.g, y = kc.j * kTile;
+                        mbar_arrive_expect_tx(&kfull[st], C::kTileBytes);
+#pragma unroll
+                        for (int c = 0; c < C::kBoxes; ++c)
+                            tma_load_3d(kdst + c * kBoxBytes, &tm_k, c * kBoxCols, y, z, &kfull[st], pol_kv);
+                        if (i == 0) GQA_TRACE_AT(kTrFirstK, clock64());
+                        if (i < 128) GQA_TRACE_AT(kTrKIssue + i, clock64());
+                        ++kissued;
+                        if (last) ++piece;
+                        cursor_next(kc, prefix, p.B, G);
+                        progress = true;
+                    }
                 }
-                const int st = i % S;
-                if (i >= S && !mbar_wait(&kvempty[st], ((i / S) - 1) & 1, ab)) break;
-                uint8_t *kdst = smem + st * C::kStageBytes;
-                uint8_t *vdst = kdst + C::kTileBytes;
-                const int z = cur.b * G + cur.g, y = cur.j * kTile;
-                mbar_arrive_expect_tx(&kfull[st], C::kTileBytes);
+                // ---- V of tile vissued (never ahead of its K)
+                if (vissued < kissued) {
+                    const int i = vissued, st = i % S;
+                    if (i < S || mbar_test_wait(&vempty[st], ((i / S) - 1) & 1)) {
+                        uint8_t *vdst = smem + C::kOffV + st * C::kTileBytes;
+                        const int z = vc.b * G + vc.g, y = vc.j * kTile;
+                        mbar_arrive_expect_tx(&vfull[st], C::kTileBytes);
 #pragma unroll
-                for (int c = 0; c < C::kBoxes; ++c)
-                    tma_load_3d(kdst + c * kBoxBytes, &tm_k, c * kBoxCols, y, z, &kfull[st], pol_kv);
-                mbar_arrive_expect_tx(&vfull[st], C::kTileBytes);
-#pragma unroll
-                for (int c = 0; c < C::kBoxes; ++c)
-                    tma_load_3d(vdst + c * kBoxBytes, &tm_v, c * kBoxCols, y, z, &vfull[st], pol_kv);
-                ++issued;
-                if (last) ++piece;
-                cursor_next(cur, prefix, p.B, G);
+                        for (int c = 0; c < C::kBoxes; ++c)
+                            tma_load_3d(vdst + c * kBoxBytes, &tm_v, c * kBoxCols, y, z, &vfull[st], pol_kv);
+                        ++vissued;
+                        cursor_next(vc, prefix, p.B, G);
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    idle = 0;
+                } else {
+                    if (idle == 0) idle_t0 = globaltimer_ns();
+                    if ((++idle & 63u) == 0) {
+                        if (*s_abort) break;
+                        if (globaltimer_ns() - idle_t0 > kWaitLimitNs) {
+                            *s_abort = 1;
+                            atomicOr(p.flags, 0x2u /* GQA_FLAG_WAIT_TIMEOUT */);
+                            break;
+                        }
+                    }
+                }
             }
         }
     } else if (warp == 1) {
@@ -260,7 +415,7 @@ __global__ void __launch_bounds__(192, 1)
                         mbar_test_wait(&kfull[st], (s_i / S) & 1) &&
                         (s_i < 2 || mbar_test_wait(&sfree[bi], ((s_i >> 1) - 1) & 1))) {
                         tc_fence_after_sync();
-                        const uint32_t kb = sbase + st * C::kStageBytes;
+                        const uint32_t kb = sbase + C::kOffK + st * C::kTileBytes;
                         const uint32_t qbase = sbase + C::kOffQ + qb * C::kQBytes;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk)
@@ -269,10 +424,12 @@ __global__ void __launch_bounds__(192, 1)
                                       sdesc_sw128(qbase + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024), idS,
                                       kk != 0);
                         umma_commit(&sfull[bi]);
+                        umma_commit(&kempty[st]);
                         if (last) {
                             umma_commit(&qempty[qb]);
                             ++piece;
                         }
+                        if (s_i < 128) GQA_TRACE_AT(kTrSIssue + s_i, clock64());
                         cursor_next(cur, prefix, p.B, G);
                         ++s_i;
                         progress = true;
@@ -284,7 +441,7 @@ __global__ void __launch_bounds__(192, 1)
                     if (mbar_test_wait(&vfull[st], (pv_i / S) & 1) && mbar_test_wait(&pfull[bi], (pv_i >> 1) & 1) &&
                         (pv_i < 2 || mbar_test_wait(&ofree[bi], ((pv_i >> 1) - 1) & 1))) {
                         tc_fence_after_sync();
-                        const uint32_t vb = sbase + st * C::kStageBytes + C::kTileBytes;
+                        const uint32_t vb = sbase + C::kOffV + st * C::kTileBytes;
                         const uint32_t d_o = tmem + 2 * N + bi * N;
 #pragma unroll
                         for (int part = 0; part < 2; ++part) {
@@ -296,7 +453,8 @@ __global__ void __launch_bounds__(192, 1)
                                           (part | kk) != 0);
                         }
                         umma_commit(&ofull[bi]);
-                        umma_commit(&kvempty[st]);
+                        umma_commit(&vempty[st]);
+                        if (pv_i < 128) GQA_TRACE_AT(kTrPvIssue + pv_i, clock64());
                         ++pv_i;
                         progress = true;
                     }
@@ -328,12 +486,12 @@ __global__ void __launch_bounds__(192, 1)
         const int odim = (D == 128) ? r : q4 * 16 + lane;
         const bool has_dim = (D == 128) || lane < 16;
         zero_empty_sequences<D>(p, prefix, P, tg, 128);
-        GroupSync128 gsync{grp, 0};
+        GroupSync gsync{grp, 0};
         float l_part[NH], acc[NH];
         Cursor cur = (ntiles > 0) ? cursor_at(u0, prefix, p.B, G) : Cursor{0, 0, 0, 1};
         int seq_b = 0;
         long long piece_u0 = u0;
-        int piece_i0 = 0;
+        int piece_i0 = 0, npe = 0;
         bool ok = true;
 
         // fold O of tile i into acc with that tile's rescale factor
@@ -346,7 +504,8 @@ __global__ void __launch_bounds__(192, 1)
             tmem_wait_ld();
             tc_fence_before_sync();
             mbar_arrive(&ofree[bi]);
-            const float *al = alpha_s + (i % 3) * NH;
+            float al[NH];
+            load_vec<NH>(alpha_s + (i % 3) * NH, al);
 #pragma unroll
             for (int h = 0; h < NH; ++h) acc[h] = fmaf(acc[h], al[h], __uint_as_float(o[h]));
             return true;
@@ -369,6 +528,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             // ---- scores of this tile: S^T row r (heads 0..NH-1)
             if (!mbar_wait(&sfull[bi], (i >> 1) & 1, ab)) { ok = false; break; }
+            if (tg == 0 && i < 128) GQA_TRACE_AT(kTrSFull + i, clock64());
             tc_fence_after_sync();
             uint32_t sraw[NH];
             tmem_ld_32x32b<NH>(tmem + lane_off + bi * N, sraw);
@@ -388,28 +548,35 @@ __global__ void __launch_bounds__(192, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&redbar[bi]);
             if (!mbar_wait(&redbar[bi], (i >> 1) & 1, ab)) { ok = false; break; }
-            const float *mprev = mrun_s + ((i + 2) % 3) * NH;    // state after tile i-1
-            float *mcur = mrun_s + (i % 3) * NH;
-            float *acur = alpha_s + (i % 3) * NH;
+            if (tg == 0 && i < 128) GQA_TRACE_AT(kTrMax + i, clock64());
+            float m_new[NH], alpha[NH];
+            reduce4<NH, true>(red + bi * 4 * NH, m_new);        // tile maximum per head
+            if (i == piece_i0) {
+#pragma unroll
+                for (int h = 0; h < NH; ++h) alpha[h] = 0.f;      // nothing to rescale yet
+            } else {
+                float m_old[NH];
+                load_vec<NH>(mrun_s + ((i + 2) % 3) * NH, m_old);   // state after tile i-1
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                    m_new[h] = fmaxf(m_old[h], m_new[h]);        // finite: every tile has a valid position
+                    alpha[h] = ex2(m_old[h] - m_new[h]);
+                }
+            }
 #pragma unroll
             for (int h = 0; h < NH; ++h) {
-                const float *rr = red + bi * 4 * NH + h;
-                const float tmax = fmaxf(fmaxf(rr[0], rr[NH]), fmaxf(rr[2 * NH], rr[3 * NH]));
-                const float m_old = (i == piece_i0) ? -INFINITY : mprev[h];
-                const float m_new = fmaxf(m_old, tmax);           // finite: every tile has a valid position
-                const float alpha = exp2f(m_old - m_new);         // 0 on the first tile of a piece
-                x[h] = exp2f(x[h] - m_new);                       // 0 at invalid positions
-                l_part[h] = fmaf(l_part[h], alpha, x[h]);
-                if (tg == 0) {
-                    mcur[h] = m_new;
-                    acur[h] = alpha;
-                }
+                x[h] = ex2(x[h] - m_new[h]);                     // 0 at invalid positions
+                l_part[h] = fmaf(l_part[h], alpha[h], x[h]);
+            }
+            if (tg == 0) {
+                store_vec<NH>(mrun_s + (i % 3) * NH, m_new);
+                store_vec<NH>(alpha_s + (i % 3) * NH, alpha);
             }
             // ---- the last tile of a sequence: clear V rows past the end (they may hold NaN)
             if (valid_cnt < kTile) {
                 if (!mbar_wait(&vfull[st], (i / S) & 1, ab)) { ok = false; break; }
                 if (!valid) {
-                    uint8_t *vrow = smem + st * C::kStageBytes + C::kTileBytes + r * 128;
+                    uint8_t *vrow = smem + C::kOffV + st * C::kTileBytes + r * 128;
 #pragma unroll
                     for (int c = 0; c < C::kBoxes; ++c) {
                         uint4 *w = reinterpret_cast<uint4 *>(vrow + c * kBoxBytes);
@@ -436,52 +603,69 @@ __global__ void __launch_bounds__(192, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(&pfull[bi]);
+            if (tg == 0 && i < 128) GQA_TRACE_AT(kTrPFull + i, clock64());
             // ---- fold the previous tile's O (its GEMM ran while this tile's softmax did)
             if (i > piece_i0 && !fold_o(i - 1)) { ok = false; break; }
+            if (tg == 0 && i < 128) GQA_TRACE_AT(kTrFold + i, clock64());
 
             if (last) {
+                if (tg == 0) GQA_TRACE_AT(kTrPieceEnd + 2 * npe, clock64());
                 // ---- l = sum over the 128 position slots, per head
                 butterfly_reduce<NH, false>(l_part, lane);
                 butterfly_store<NH, C::kHalve>(l_part, lane, lred + q4 * NH);
                 if (!gsync(ab)) { ok = false; break; }        // also publishes tile i's alpha
                 if (!fold_o(i)) { ok = false; break; }
+                float L[NH];
+                reduce4<NH, false>(lred, L);
                 const int seg = cur.b * G + cur.g;
                 const long long seg_a = (long long)G * prefix[cur.b] + (long long)cur.g * cur.tiles;
                 const bool owned = (piece_u0 == seg_a) && (cur.j + 1 == cur.tiles);
-                float *orow = p.out + ((size_t)cur.b * p.H + (size_t)cur.g * n) * D;
-                float *sp = slot_ptr(p, blockIdx.x + seg, D);
+                if (owned) {
+                    float *orow = p.out + ((size_t)cur.b * p.H + (size_t)cur.g * n) * D;
 #pragma unroll
-                for (int h = 0; h < NH; ++h) {
-                    if (h < n) {
-                        const float L = lred[h] + lred[NH + h] + lred[2 * NH + h] + lred[3 * NH + h];
-                        if (owned) {
-                            if (has_dim) orow[h * D + odim] = acc[h] / L;
-                        } else {
-                            if (has_dim) sp[2 * n + h * D + odim] = acc[h];
-                            if (tg == 0) {
+                    for (int h = 0; h < NH; ++h)
+                        if (h < n && has_dim) orow[h * D + odim] = acc[h] / L[h];
+                } else {
+                    float *sp = slot_ptr(p, blockIdx.x + seg, D);
+                    const int aoff = slot_acc_offset(n);
+#pragma unroll
+                    for (int h = 0; h < NH; ++h)
+                        if (h < n && has_dim) sp[aoff + h * D + odim] = acc[h];
+                    if (tg == 0) {
+                        float mcur[NH];
+                        load_vec<NH>(mrun_s + (i % 3) * NH, mcur);
+#pragma unroll
+                        for (int h = 0; h < NH; ++h) {
+                            if (h < n) {
                                 sp[h] = mcur[h];
-                                sp[n + h] = L;
+                                sp[n + h] = L[h];
                             }
                         }
                     }
-                }
-                if (!owned) {
-                    __threadfence();
+                    // The barrier orders every thread's partial writes before thread 0's
+                    // fence, which is cumulative: they are visible before the arrival count.
                     if (!gsync(ab)) { ok = false; break; }
                     const int c_lo = cta_of_tile(seg_a, W, Pw);
                     const int c_hi = cta_of_tile(seg_a + cur.tiles - 1, W, Pw);
                     if (tg == 0) {
+                        __threadfence();
                         const int prev = atomicAdd(p.counters + seg, 1);
                         *s_last = (prev == c_hi - c_lo) ? 1 : 0;
                     }
                     if (!gsync(ab)) { ok = false; break; }
                     if (*s_last) {
                         __threadfence();
-                        combine_segment<D>(p, c_lo + seg, c_hi - c_lo + 1, cur.b, cur.g, tg, 128);
+                        if (!combine_segment<D>(p, c_lo + seg, c_hi - c_lo + 1, cur.b, cur.g, tg, comb, gsync, ab)) {
+                            ok = false;
+                            break;
+                        }
                         if (tg == 0) atomicExch(p.counters + seg, 0);
                     }
                 }
-                if (!gsync(ab)) { ok = false; break; }   // lred and s_last are reused by the next piece
+                // lred, s_last and comb are next written after the next tile's max barrier,
+                // which every thread reaches only after its reads here.
+                if (tg == 0) GQA_TRACE_AT(kTrPieceEnd + 2 * npe + 1, clock64());
+                ++npe;
             }
             cursor_next(cur, prefix, p.B, G);
         }
@@ -489,12 +673,16 @@ __global__ void __launch_bounds__(192, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    if (tid == 64) {
+        GQA_TRACE_AT(kTrEnd, clock64());
+        GQA_TRACE_AT(kTrGlobalEnd, globaltimer_ns());
+    }
     if (warp == 0 && lane == 0 && *s_abort) {
         // let copies in flight land before the CTA's shared memory is released
-        for (int k = issued > S ? issued - S : 0; k < issued; ++k) {
+        for (int k = kissued > S ? kissued - S : 0; k < kissued; ++k)
             mbar_wait_teardown(&kfull[k % S], (k / S) & 1);
+        for (int k = vissued > S ? vissued - S : 0; k < vissued; ++k)
             mbar_wait_teardown(&vfull[k % S], (k / S) & 1);
-        }
         for (int k = qissued > QB ? qissued - QB : 0; k < qissued; ++k)
             mbar_wait_teardown(&qfull[k % QB], (k / QB) & 1);
     }
