@@ -4,10 +4,16 @@
 
 One step = one gqa_decode call on the workload's whole batch (one layer), with
 the bf16 KV cache resident in HBM.  GB/s counts algorithmic bytes only: the
-valid K and V rows, sum_b seq_lens[b] * G * d * 2 bytes * 2.  L2 is flushed
-(a 256 MiB write) before every timed step, outside the timed events.  The step
-time is measured with CUDA events on the launching stream; the step is a single
-kernel launch, so the same events time the dominant kernel.
+valid K and V rows, sum_b seq_lens[b] * G * d * 2 bytes * 2.
+
+L2: inputs larger than L2.  The K/V caches are held in C copies and step i
+reads copy i % C, with C chosen so that the C - 1 steps between two reads of a
+copy stream at least three L2 capacities of other data; no step finds its
+cache in L2.  (A write-flush between steps is not used: the dirty lines it
+leaves slow the next kernel down by write-back traffic that is not its own.)
+The K steps run back to back on one stream between one pair of CUDA events;
+the step is a single kernel launch, so total time / K is that kernel's average
+launch-to-launch duration.
 
 Under torchrun (N > 1) every rank runs an independent replica of the step on
 its own GPU (nothing is sharded); value = bytes of all ranks / max time.
@@ -38,7 +44,7 @@ from kv_cache_decode_06_b300.inputs import CONFIGS, T5XXL_SWEEP_GS, make_decode_
 
 METRIC = "GQA decode KV-cache HBM GB/s (% of B300 peak) and decode steps/s, 1 GPU"
 UNIT = "GB/s"
-L2_FLUSH_BYTES = 256 << 20
+L2_COPIES_SPAN = 3            # L2 capacities streamed between two reads of one cache copy
 FALLBACK_HBM_GBS = 6400.0
 
 
@@ -194,7 +200,7 @@ def config_dict(cfg, inp, extra=None):
     d = {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "G": cfg.G, "d": cfg.d, "Lmax": cfg.Lmax,
          "seq_lens": (list(cfg.fixed_seq) if cfg.fixed_seq else f"U[{cfg.seq_lo},{cfg.seq_hi}] seeded"),
          "kv_bytes_per_step": inp.kv_bytes, "inputs": "N(0,1) -> bf16, seeded",
-         "l2": "flushed before every timed step (256 MiB write, outside the timed events)"}
+         "l2": "inputs larger than L2: no step finds its K/V cache in L2"}
     if extra:
         d.update(extra)
     return d
@@ -203,7 +209,7 @@ def config_dict(cfg, inp, extra=None):
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="mistral7b",
                     help="mistral7b | llama3_70b | long_ragged | tiny | t5xxl_sweep_G<1..64>")
@@ -240,37 +246,38 @@ def main() -> None:
     k = torch.from_numpy(inp.k).view(torch.bfloat16).to(dev)
     v = torch.from_numpy(inp.v).view(torch.bfloat16).to(dev)
     sl = torch.from_numpy(inp.seq_lens).to(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(3, math.ceil(L2_COPIES_SPAN * l2 / inp.kv_bytes) + 1)
+    ks = [k] + [k.clone() for _ in range(copies - 1)]
+    vs = [v] + [v.clone() for _ in range(copies - 1)]
     out = torch.empty((cfg.B, cfg.H, cfg.d), dtype=torch.float32, device=dev)
     ws = gqa.alloc_workspace(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax, dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     scale = float(inp.scale)
     path = args.path or gqa.select_path(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax)
 
-    def step():
-        gqa.decode(q, k, v, sl, out=out, workspace=ws, scale=scale, stream=stream, path=path)
+    def step(i):
+        c = i % copies
+        gqa.decode(q, ks[c], vs[c], sl, out=out, workspace=ws, scale=scale, stream=stream, path=path)
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize()
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
+        t0.record(stream)
         for i in range(args.steps):
-            flush.zero_()
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
+            step(i)
+        t1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    durs = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = float(sum(durs))
+    total_ms = float(t0.elapsed_time(t1))
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -346,14 +353,19 @@ def main() -> None:
         "vs_baseline": None, "dtype": "bf16" if path == gqa.PATH_TCGEN05 else "f32", "data": "synthetic",
         "steps_per_s": world * 1e3 / ms_per_step,
         "config": config_dict(cfg, inp, extra={"path": "tcgen05" if path == gqa.PATH_TCGEN05 else "simt",
-                                               "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"}),
+                                               "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                                               "cache_copies": copies,
+                                               "l2": f"inputs larger than L2: K/V caches held in {copies} copies, "
+                                                     f"step i reads copy i % {copies}, so >= {L2_COPIES_SPAN} L2 "
+                                                     "capacities of other KV data stream between two reads of a copy",
+                                               "timing": "K steps back to back between one pair of CUDA events"}),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps,
                 "what": "H2D of q, k_cache, v_cache (whole buffers), seq_lens from pinned host memory + "
                         "gqa.decode + D2H of out, per step"},
-        "gpu_launches": args.steps,
+        "gpu_launches": 2 * args.steps,   # decode kernel + split-combine kernel per step
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)

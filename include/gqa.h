@@ -25,7 +25,8 @@
  *   - Host-checkable errors return before anything is enqueued.  A failed
  *     launch returns GQA_ERR_LAUNCH.
  *   - Thread safety: calls from several host threads are safe; two calls that
- *     share a workspace must not overlap on the device.
+ *     share a workspace must not overlap on the device (calls on one stream
+ *     never do).
  */
 #ifndef GQA_B300_GQA_H
 #define GQA_B300_GQA_H
@@ -72,13 +73,12 @@ int gqa_abi_version(void);
  * depend on seq_lens or on the device.  Writes *bytes and returns GQA_OK, or
  * returns the status gqa_decode would return for the same shape.
  *
- * The workspace holds split-combine partial results (one (m, l, acc) triple per
- * query head per piece of a sequence), one arrival counter per (batch, K/V head)
- * and one flag word.  It MUST be zero-filled before its first use (for example
- * cudaMemsetAsync(ws, 0, bytes, stream)).  Every completed gqa_decode call
- * leaves the counters at zero again, so later calls with the same B and G need
- * no reset; before a call with another (B, G), zero it again (the counters sit
- * at a shape-dependent offset).  The flag word is only ever OR-ed into.
+ * The workspace holds a flag word and the split-combine partial results (one
+ * (m, l, acc) triple per query head per piece of a sequence).  It MUST be
+ * zero-filled before its first use (for example cudaMemsetAsync(ws, 0, bytes,
+ * stream)) so that the flag word starts clear; nothing else in it needs
+ * resetting between calls, whatever their shapes.  The flag word is only ever
+ * OR-ed into.
  */
 gqa_status gqa_decode_workspace_size(int B, int H, int G, int d, int Lmax, size_t *bytes);
 
@@ -112,8 +112,15 @@ gqa_status gqa_decode_workspace_size(int B, int H, int G, int d, int Lmax, size_
  * scale     score scale, normally 1/sqrt(d), used as given (fp32)
  *
  * Arithmetic: exact bf16 products accumulated in fp32, softmax in fp32 with a
- * running maximum, fp32 output.  Error bound vs the exact result: see the design
- * notes (max abs <= 1e-2 and row-relative <= 2e-3 on the benchmark workloads).
+ * running maximum, fp32 output.  Measured against a float64 evaluation of the
+ * definition: max abs error <= 1e-2 and, per output row, max error <= 2e-3 of
+ * the row's largest |value| on the benchmark workloads.
+ *
+ * Two kernels are enqueued: the split decode kernel and the split-combine
+ * kernel that merges the sequences the work split cut across thread blocks.
+ * Both use programmatic stream serialisation: each may start its on-chip
+ * set-up while the previous kernel on `stream` drains, and touches global
+ * memory only after that kernel has completed.
  */
 gqa_status gqa_decode(const void *q, const void *k_cache, const void *v_cache,
                       const int32_t *seq_lens, float *out,
@@ -164,8 +171,8 @@ gqa_status gqa_decode_read_flags(void *workspace, uint32_t *flags, int clear, vo
  *     return GQA_ERR_WORKSPACE and enqueue nothing;
  *   - the first call on a device looks up the scratch address on that device
  *     (make it before any stream capture on that device);
- *   - every call clears the flag word and the counters of the scratch on
- *     `stream` before the kernel (cudaMemsetAsync, no allocation);
+ *   - every call clears the scratch's flag word on `stream` before the
+ *     kernels (cudaMemsetAsync, no allocation);
  *   - all calls share the one array: calls that overlap on the GPU (other
  *     streams, other host threads) race and corrupt each other's results, so
  *     order them on one stream or synchronise between them.

@@ -72,12 +72,12 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr size_t kHeaderBytes = 256;
 
-size_t counters_bytes(int B, int G) { return align_up((size_t)B * G * sizeof(int), 256); }
-
+// Workspace: a 256-byte header (the flag word) and the partial slots, one per
+// static piece (slot c + s < GQA_MAX_CTAS + B*G).
 size_t workspace_bytes_for(int B, int H, int G, int d) {
     const int n = H / G;
     const size_t slots = (size_t)GQA_MAX_CTAS + (size_t)B * G;
-    return kHeaderBytes + counters_bytes(B, G) + slots * (size_t)gqa::slot_floats(n, d) * sizeof(float);
+    return kHeaderBytes + slots * (size_t)gqa::slot_floats(n, d) * sizeof(float);
 }
 
 gqa_status check_shape(int B, int H, int G, int d, int Lmax) {
@@ -132,7 +132,11 @@ int auto_path(int H, int G, int d) {
 }  // namespace
 
 namespace gqa {
-size_t decode_workspace_zero_prefix(int B, int G) { return kHeaderBytes + counters_bytes(B, G); }
+size_t decode_workspace_zero_prefix(int B, int G) {
+    (void)B;
+    (void)G;
+    return kHeaderBytes;
+}
 }  // namespace gqa
 
 extern "C" {
@@ -206,8 +210,7 @@ gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache
     p.seq_lens = seq_lens;
     p.out = out;
     p.flags = reinterpret_cast<unsigned int *>(ws);
-    p.counters = reinterpret_cast<int *>(ws + kHeaderBytes);
-    p.partials = reinterpret_cast<float *>(ws + kHeaderBytes + counters_bytes(B, G));
+    p.partials = reinterpret_cast<float *>(ws + kHeaderBytes);
     p.B = B;
     p.H = H;
     p.G = G;
@@ -229,6 +232,9 @@ gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache
         e = gqa::launch_decode_tc(tk, tv, tq, p, d, (int)ctas, st);
     }
     if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return GQA_ERR_LAUNCH;
+    // merge the segments the work split cut across CTAs (a no-op grid when none is)
+    e = gqa::launch_split_combine(p, d, (int)ctas, st);
     return e == cudaSuccess ? GQA_OK : GQA_ERR_LAUNCH;
 }
 

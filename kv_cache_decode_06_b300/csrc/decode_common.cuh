@@ -1,4 +1,4 @@
-// Work decomposition and split-combine shared by the decode kernels.
+// Work decomposition shared by the decode kernels and the split-combine.
 //
 // Work unit: a tile of 128 consecutive cache positions of one (sequence b,
 // K/V head g) pair, a "segment".  Segment s = b*G + g holds
@@ -11,14 +11,14 @@
 //
 // A CTA's range cuts segments into "pieces".  A piece that covers its whole
 // segment is finished in place (out = acc / l).  Otherwise the piece's partial
-// softmax state (m, l, acc) goes to a workspace slot and the CTA bumps the
-// segment's arrival counter; the CTA that arrives last merges every piece of
-// the segment and resets the counter to zero.  Nobody waits for anybody: the
-// merge is done by whoever comes last.
+// softmax state (m, l, acc) goes to a workspace slot, and the split-combine
+// kernel, which runs when the decode grid has completed, merges the pieces of
+// every split segment.  The decode kernel has no atomics, counters or fences.
 //
 // Partial slot of the piece of segment s cut by CTA c: slot = c + s.  This is
 // one-to-one: if c < c' then every segment of c is <= every segment of c', so
-// c + s = c' + s' with c < c' would need s > s'.
+// c + s = c' + s' with c < c' would need s > s'.  The pieces of segment s lie in
+// slots c_lo + s .. c_hi + s, c_lo and c_hi the CTAs of its first and last tile.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -38,7 +38,6 @@ struct DecodeParams {
     const int32_t *seq_lens;  // [B]
     float *out;               // [B, H, D]
     unsigned int *flags;      // workspace flag word
-    int *counters;            // [B*G] arrival counters (zero between calls)
     float *partials;          // slots of n*(D+2) floats: m[n], l[n], acc[n][D]
     int B, H, G, n, Lmax;
     float scale_log2;         // scale * log2(e): scores are kept in base-2 units
@@ -86,8 +85,9 @@ __device__ __forceinline__ void cursor_next(Cursor &c, const int *prefix, int B,
     if (c.b < B) c.tiles = prefix[c.b + 1] - prefix[c.b];
 }
 
-// Block-wide: clamps seq_lens into [0, Lmax] and writes the tile prefix sums.
-// `scratch` needs 32 ints.  Ends with __syncthreads().
+// Block-wide: clamps seq_lens into [0, Lmax] and writes the tile prefix sums;
+// with a flag word, CTA 0 records a clamp in it.  `scratch` needs 32 ints.
+// Ends with __syncthreads().
 __device__ inline void build_prefix(const int32_t *seq_lens, int B, int Lmax, int *prefix, int *scratch,
                              unsigned int *flags) {
     const int tid = threadIdx.x, nth = blockDim.x;
@@ -122,7 +122,7 @@ __device__ inline void build_prefix(const int32_t *seq_lens, int B, int Lmax, in
         run += tiles_of(clamp_seq(__ldg(seq_lens + b), Lmax));
     }
     if (tid == 0) prefix[B] = total;
-    if (bad && blockIdx.x == 0) atomicOr(flags, 0x1u /* GQA_FLAG_SEQ_LEN_CLAMPED */);
+    if (bad && flags && blockIdx.x == 0) atomicOr(flags, 0x1u /* GQA_FLAG_SEQ_LEN_CLAMPED */);
     __syncthreads();
 }
 
@@ -146,6 +146,11 @@ __device__ __forceinline__ float *slot_ptr(const DecodeParams &p, int slot, int 
     return p.partials + (size_t)slot * (size_t)slot_floats(p.n, D);
 }
 
+// First tile of the cursor's segment in the tile list.
+__device__ __forceinline__ long long segment_start(const Cursor &c, const int *prefix, int G) {
+    return (long long)G * prefix[c.b] + (long long)c.g * c.tiles;
+}
+
 // 2^x with the hardware approximation (relative error ~2^-22); 2^-inf = +0.
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -165,77 +170,5 @@ struct GroupSync {
         return ok;
     }
 };
-
-// Merge the `count` pieces of segment (b, g), stored in consecutive slots from
-// `first_slot`, and write its n output rows:
-//   M_h = max_k m_kh,  L_h = sum_k l_kh 2^(m_kh - M_h),
-//   out[h, :] = (sum_k acc_k[h, :] 2^(m_kh - M_h)) / L_h.
-// Run by the 128 compute threads (tid 0..127) after the caller has made the
-// other pieces' writes visible (a fence after observing the last arrival).
-// `scratch` holds 2 * n floats of shared memory.  Returns false if the CTA is
-// aborting.  Reads go to L2 (ld.cg): the partials were written by other SMs.
-template <int D>
-__device__ bool combine_segment(const DecodeParams &p, int first_slot, int count, int b, int g, int tid,
-                                float *scratch, GroupSync &sync, const AbortState &ab) {
-    const int n = p.n;
-    const long long stride = slot_floats(n, D);
-    const int aoff = slot_acc_offset(n);
-    const float *base = p.partials + (size_t)first_slot * (size_t)stride;
-    const int warp = tid >> 5, lane = tid & 31;
-    // ---- per head: global maximum and normaliser (warp w takes heads w, w+4, ...)
-    for (int h = warp; h < n; h += 4) {
-        float mk = -INFINITY, M = -INFINITY;
-        if (lane < count) mk = __ldcg(base + (size_t)lane * stride + h);
-        M = mk;
-        for (int k = lane + 32; k < count; k += 32) M = fmaxf(M, __ldcg(base + (size_t)k * stride + h));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float L = 0.f;
-        if (lane < count) L = __ldcg(base + (size_t)lane * stride + n + h) * ex2(mk - M);
-        for (int k = lane + 32; k < count; k += 32) {
-            const float *sk = base + (size_t)k * stride;
-            L = fmaf(__ldcg(sk + n + h), ex2(__ldcg(sk + h) - M), L);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        if (lane == 0) {
-            scratch[h] = M;
-            scratch[n + h] = L;
-        }
-    }
-    if (!sync(ab)) return false;
-    // ---- outputs, four consecutive dims of one head per float4
-    float4 *orow = reinterpret_cast<float4 *>(p.out + ((size_t)b * p.H + (size_t)g * n) * D);
-    const int nd4 = n * D / 4;
-    for (int e = tid; e < nd4; e += 128) {
-        const int h = (e * 4) / D;
-        const float M = scratch[h];
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        int k = 0;
-        for (; k + 2 <= count; k += 2) {
-            const float *s0 = base + (size_t)k * stride, *s1 = s0 + stride;
-            const float m0 = __ldcg(s0 + h), m1 = __ldcg(s1 + h);
-            const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(s0 + aoff) + e);
-            const float4 v1 = __ldcg(reinterpret_cast<const float4 *>(s1 + aoff) + e);
-            const float w0 = ex2(m0 - M), w1 = ex2(m1 - M);
-            a.x = fmaf(v1.x, w1, fmaf(v0.x, w0, a.x));
-            a.y = fmaf(v1.y, w1, fmaf(v0.y, w0, a.y));
-            a.z = fmaf(v1.z, w1, fmaf(v0.z, w0, a.z));
-            a.w = fmaf(v1.w, w1, fmaf(v0.w, w0, a.w));
-        }
-        if (k < count) {
-            const float *s0 = base + (size_t)k * stride;
-            const float w0 = ex2(__ldcg(s0 + h) - M);
-            const float4 v0 = __ldcg(reinterpret_cast<const float4 *>(s0 + aoff) + e);
-            a.x = fmaf(v0.x, w0, a.x);
-            a.y = fmaf(v0.y, w0, a.y);
-            a.z = fmaf(v0.z, w0, a.z);
-            a.w = fmaf(v0.w, w0, a.w);
-        }
-        const float L = scratch[n + h];
-        orow[e] = make_float4(a.x / L, a.y / L, a.z / L, a.w / L);
-    }
-    return true;
-}
 
 }  // namespace gqa

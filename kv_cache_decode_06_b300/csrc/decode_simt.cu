@@ -10,7 +10,8 @@
 //   softmax: running max m[h] per warp (base-2 units), lane-private running sum
 //            l[h], probabilities p[h][t] to a warp-private buffer;
 //   values:  lane = output dims, acc[h][dims] += p[h][t] * v[t][dims].
-// At the end of a piece the four warps' (m, l, acc) are merged in shared memory.
+// At the end of a piece the four warps' (m, l, acc) are merged in shared memory
+// and written out, or left as a partial for the split-combine kernel.
 // ["Grouped-query attention (GQA)" concept page, "Implementation sketch",
 //  decode-step pseudocode; arxiv:2305.13245 §2.2]
 #include <cuda.h>
@@ -63,7 +64,6 @@ __global__ void __launch_bounds__(SimtCfg<D, NMAX>::kThreads, 1)
     uint64_t *empty = full + C::kStages;
     uint64_t *grp = empty + C::kStages;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::kOffFlags);
-    volatile int *s_last = s_abort + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = gridDim.x;
@@ -76,13 +76,16 @@ __global__ void __launch_bounds__(SimtCfg<D, NMAX>::kThreads, 1)
         }
         mbar_init(grp, C::kWarps * 32);
         *s_abort = 0;
-        *s_last = 0;
         fence_mbar_init();
     }
     if (tid == C::kWarps * 32) {
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
     }
+    // Inputs and outputs are touched only once the grids this one depends on
+    // have completed.
+    griddep_wait();
+    griddep_launch_dependents();
     build_prefix(p.seq_lens, p.B, p.Lmax, prefix, scratch, p.flags);  // ends with __syncthreads
 
     const int G = p.G, n = p.n;
@@ -273,26 +276,7 @@ __global__ void __launch_bounds__(SimtCfg<D, NMAX>::kThreads, 1)
                         sp[slot_acc_offset(n) + idx] = A;
                     }
                 }
-                if (!owned) {
-                    // every thread's partial writes reach L2 before thread 0 announces them (the
-                    // barrier orders them before thread 0's fence, which is cumulative)
-                    if (!gsync(ab)) break;
-                    const int c_lo = cta_of_tile(seg_a, W, Pw);
-                    const int c_hi = cta_of_tile(seg_a + cur.tiles - 1, W, Pw);
-                    if (tid == 0) {
-                        __threadfence();
-                        const int prev = atomicAdd(p.counters + seg, 1);
-                        *s_last = (prev == c_hi - c_lo) ? 1 : 0;
-                    }
-                    if (!gsync(ab)) break;
-                    if (*s_last) {
-                        __threadfence();
-                        if (!combine_segment<D>(p, c_lo + seg, c_hi - c_lo + 1, cur.b, cur.g, tid, m_s, gsync, ab))
-                            break;
-                        if (tid == 0) atomicExch(p.counters + seg, 0);
-                    }
-                }
-                if (!gsync(ab)) break;   // merge buffers and s_last are reused by the next piece
+                if (!gsync(ab)) break;   // the merge buffers are reused by the next piece
                 ++piece;
             }
             cursor_next(cur, prefix, p.B, G);
@@ -321,8 +305,7 @@ cudaError_t launch_simt_t(const CUtensorMap &tk, const CUtensorMap &tv, const De
         if (e != cudaSuccess) return e;
         attr_set |= bit;
     }
-    kern<<<ctas, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, ctas, C::kThreads, C::kSmemBytes, stream, tk, tv, p);
 }
 
 }  // namespace

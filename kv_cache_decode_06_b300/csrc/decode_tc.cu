@@ -25,8 +25,9 @@
 //   2. writes P(i) and hands it to the MMA warp,
 //   3. folds the previous tile's O into register accumulators with that tile's
 //      rescale factor (so TMEM never needs rescaling).
-// Work split, pieces and the last-arriver combine are shared with the CUDA-core
-// path (decode_common.cuh).
+// Work split and pieces are shared with the CUDA-core path (decode_common.cuh);
+// pieces that are not a whole segment leave their partial state in the
+// workspace for the split-combine kernel (combine.cu).
 //
 // Build with -DGQA_TRACE for a per-CTA timeline (clock64 stamps of every
 // pipeline event, see the slot map at TraceSlot) readable with gqa_trace_copy.
@@ -99,8 +100,7 @@ struct TcCfg {
     static constexpr int kLredF = 4 * NH;                        // [4 warps][NH] l sums
     static constexpr int kMF = 3 * NH;                           // [3][NH] running max after tile i
     static constexpr int kAF = 3 * NH;                           // [3][NH] rescale factor of tile i
-    static constexpr int kCombF = 2 * NH;                        // combine scratch (M, L per head)
-    static constexpr int kSmallBytes = 4 * (kRedF + kLredF + kMF + kAF + kCombF) + 32 * 4 + (kMaxBatch + 1) * 4;
+    static constexpr int kSmallBytes = 4 * (kRedF + kLredF + kMF + kAF) + 32 * 4 + (kMaxBatch + 1) * 4;
     static constexpr int bar_bytes(int S, int QB) { return (4 * S + 2 * QB + 12 + 2) * 8 + 16; }
     static constexpr int fixed_bytes(int S, int QB) {
         return QB * kQBytes + 4 * kPBytes + kSmallBytes + bar_bytes(S, QB) + 1024 /* alignment slack */;
@@ -118,14 +118,13 @@ struct TcCfg {
     static constexpr int kOffLred = kOffRed + kRedF * 4;
     static constexpr int kOffM = kOffLred + kLredF * 4;
     static constexpr int kOffA = kOffM + kMF * 4;
-    static constexpr int kOffComb = kOffA + kAF * 4;
-    static constexpr int kOffPrefix = kOffComb + kCombF * 4;              // i32 [kMaxBatch + 1]
+    static constexpr int kOffPrefix = kOffA + kAF * 4;                    // i32 [kMaxBatch + 1]
     static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 1) * 4;  // i32 [32]
     static constexpr int kOffBar = (kOffScratch + 32 * 4 + 7) / 8 * 8;
     // barriers: kfull[S] vfull[S] kempty[S] vempty[S] qfull[QB] qempty[QB] sfull[2] sfree[2]
     //           pfull[2] ofull[2] ofree[2] red[2] grp done
     static constexpr int kNumBars = 4 * kStages + 2 * kQBuf + 12 + 2;
-    static constexpr int kOffFlags = kOffBar + kNumBars * 8;     // abort, last, tmem base
+    static constexpr int kOffFlags = kOffBar + kNumBars * 8;     // abort, tmem base
     static constexpr int kSmemBytes = kOffFlags + 16 + 1024;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory layout too large");
     static_assert(NH < 4 || (kOffRed % 16 == 0 && kOffLred % 16 == 0 && kOffM % 16 == 0 && kOffA % 16 == 0),
@@ -249,7 +248,6 @@ __global__ void __launch_bounds__(192, 1)
     float *lred = reinterpret_cast<float *>(smem + C::kOffLred);
     float *mrun_s = reinterpret_cast<float *>(smem + C::kOffM);
     float *alpha_s = reinterpret_cast<float *>(smem + C::kOffA);
-    float *comb = reinterpret_cast<float *>(smem + C::kOffComb);
     int *prefix = reinterpret_cast<int *>(smem + C::kOffPrefix);
     int *scratch = reinterpret_cast<int *>(smem + C::kOffScratch);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
@@ -258,7 +256,6 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t *sfull = qempty + QB, *sfree = sfull + 2, *pfull = sfree + 2, *ofull = pfull + 2, *ofree = ofull + 2;
     uint64_t *redbar = ofree + 2, *grp = redbar + 2, *done = grp + 1;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::kOffFlags);
-    volatile int *s_last = s_abort + 1;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::kOffFlags + 8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -291,7 +288,6 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(grp, 128);
         mbar_init(done, 1);
         *s_abort = 0;
-        *s_last = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -303,6 +299,10 @@ __global__ void __launch_bounds__(192, 1)
         tmem_alloc(s_tmem, C::kTmemCols);
         tmem_relinquish();
     }
+    // Everything above is on-chip; inputs and outputs are touched only once the
+    // grids this one depends on have completed.
+    griddep_wait();
+    griddep_launch_dependents();
     build_prefix(p.seq_lens, p.B, p.Lmax, prefix, scratch, p.flags);   // ends with __syncthreads
     tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
@@ -642,28 +642,9 @@ __global__ void __launch_bounds__(192, 1)
                             }
                         }
                     }
-                    // The barrier orders every thread's partial writes before thread 0's
-                    // fence, which is cumulative: they are visible before the arrival count.
-                    if (!gsync(ab)) { ok = false; break; }
-                    const int c_lo = cta_of_tile(seg_a, W, Pw);
-                    const int c_hi = cta_of_tile(seg_a + cur.tiles - 1, W, Pw);
-                    if (tg == 0) {
-                        __threadfence();
-                        const int prev = atomicAdd(p.counters + seg, 1);
-                        *s_last = (prev == c_hi - c_lo) ? 1 : 0;
-                    }
-                    if (!gsync(ab)) { ok = false; break; }
-                    if (*s_last) {
-                        __threadfence();
-                        if (!combine_segment<D>(p, c_lo + seg, c_hi - c_lo + 1, cur.b, cur.g, tg, comb, gsync, ab)) {
-                            ok = false;
-                            break;
-                        }
-                        if (tg == 0) atomicExch(p.counters + seg, 0);
-                    }
                 }
-                // lred, s_last and comb are next written after the next tile's max barrier,
-                // which every thread reaches only after its reads here.
+                // lred is next written after the next tile's max barrier, which every
+                // thread reaches only after its reads here.
                 if (tg == 0) GQA_TRACE_AT(kTrPieceEnd + 2 * npe + 1, clock64());
                 ++npe;
             }
@@ -707,8 +688,7 @@ cudaError_t launch_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUte
         if (e != cudaSuccess) return e;
         attr_set |= bit;
     }
-    kern<<<ctas, C::kThreads, C::kSmemBytes, stream>>>(tk, tv, tq, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, ctas, C::kThreads, C::kSmemBytes, stream, tk, tv, tq, p);
 }
 
 template <int D>

@@ -4,9 +4,30 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "decode_common.cuh"
 
 namespace gqa {
+
+// Launch with programmatic stream serialisation: the kernel may start while the
+// previous kernel on the stream drains; it waits for it (griddepcontrol.wait)
+// before touching global memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 int simt_max_heads();
 cudaError_t launch_decode_simt(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int D,
@@ -17,9 +38,13 @@ int tc_rows_for(int n);   // rows of the q tensor-map box (n rounded up to 16, 3
 cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
                              const DecodeParams &p, int D, int ctas, cudaStream_t stream);
 
-// Leading bytes of a decode workspace that must be zero before a call on a
-// fresh (or differently shaped) workspace: the flag word and the counters.
+// Leading bytes of a decode workspace that must be zero before its first call:
+// the flag word.
 size_t decode_workspace_zero_prefix(int B, int G);
+
+// The split-combine kernel (combine.cu), launched after a decode kernel of
+// grid_main CTAs.
+cudaError_t launch_split_combine(const DecodeParams &p, int D, int grid_main, cudaStream_t stream);
 
 cudaError_t launch_meanpool(const float *w_in, float *w_out, long long outer, int H, int G, long long inner,
                             cudaStream_t stream);

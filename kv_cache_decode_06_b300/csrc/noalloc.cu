@@ -67,9 +67,9 @@ extern "C" gqa_status gqa_decode_noalloc(const void *q, const void *k_cache, con
     void *ws = nullptr;
     const gqa_status a = scratch_address(&ws);
     if (a != GQA_OK) return a;
-    // The counters must start at zero.  A completed call leaves them at zero, but
-    // a call of another (B, G) finds them at other offsets, so clear the flag word
-    // and the counters of this shape every time (on the caller's stream).
+    // Clear the flag word every time (on the caller's stream): the scratch is
+    // shared by every call, and a flag left by an earlier call would otherwise
+    // stay set.  Nothing else in the workspace needs resetting.
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, gqa::decode_workspace_zero_prefix(B, G), st) != cudaSuccess) {
         cudaGetLastError();

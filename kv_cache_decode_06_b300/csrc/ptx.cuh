@@ -146,6 +146,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Blocks until the grids this one depends on (launched before it on the stream
+// with programmatic serialisation) have completed and their memory is visible.
+// A no-op when the grid was launched without that attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the grid launched after this one on the stream start its prologue early.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ misc
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;

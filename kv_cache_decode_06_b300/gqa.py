@@ -127,9 +127,8 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_le
     """One GQA decode step: q [B,H,d] bf16, caches [B,G,Lmax,d] bf16, seq_lens [B] int32 -> out [B,H,d] fp32.
 
     Enqueued on ``stream`` (default: the current stream); returns ``out``.
-    ``workspace`` must come from :func:`alloc_workspace` (zero-filled), or be
-    reused from an earlier call with the same B and G (the counters it holds
-    are back at zero after every call); for another (B, G), zero it again.
+    ``workspace`` must come from :func:`alloc_workspace` (zero-filled) and may be
+    reused by later calls of any shape that fits it.
     """
     dev = q.device
     B, H, d = q.shape

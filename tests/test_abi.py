@@ -59,7 +59,7 @@ def test_workspace_size_for_every_workload(gqa_lib):
     for c in cfgs:
         st, n = _ws(c.B, c.H, c.G, c.d, c.Lmax)
         assert st == 0 and n > 0
-        # partial slots: (GQA_MAX_CTAS + B*G) * n * (d + 2) floats, plus header and counters
+        # partial slots: (GQA_MAX_CTAS + B*G) * n * (d + 2) floats (plus padding), plus the header
         assert n >= (1024 + c.B * c.G) * c.n * (c.d + 2) * 4
         assert n < 64 * 2 ** 20
 

@@ -1,11 +1,13 @@
 """CPU check of the decode kernels' work split, written from the same rules.
 
 The kernels give CTA c of P the tiles [c*W/P, (c+1)*W/P) of the (b, g, j)-ordered
-tile list, cut segments into pieces, store a piece's partial state in slot
-c + (b*G + g), and let the last of a segment's pieces merge it.  This test
+tile list, cut segments into pieces and store a piece's partial state in slot
+c + (b*G + g); the split-combine kernel's CTA c merges the segment cut at the
+start of decode CTA c's range when that is the segment's first cut.  This test
 replays those rules in Python for many shapes and checks that every tile is
-processed exactly once, slots are distinct and inside the workspace, the merge
-owner sees every piece, and TMA coordinates stay within the tensor map.
+processed exactly once, slots are distinct and inside the workspace, every
+split segment is merged exactly once from exactly its pieces, and TMA
+coordinates stay within the tensor map.
 """
 import random
 
@@ -100,6 +102,21 @@ def schedule(seq, G, P, Lmax):
         seg_a = G * prefix[b] + g * tiles[b]
         c_lo, c_hi = cta_of_tile(seg_a), cta_of_tile(seg_a + tiles[b] - 1)
         assert sorted(cs) == list(range(c_lo, c_hi + 1)) and c_hi > c_lo
+    # split-combine: CTA c merges the segment cut at the start of decode CTA c's
+    # range when that is the segment's first cut; every split segment exactly once
+    merged = {}
+    for c in range(1, P):
+        a = c * W // P
+        b, g, j, tb = cursor_at(a)
+        seg_a = G * prefix[b] + g * tb
+        if seg_a == a or cta_of_tile(seg_a) != c - 1:
+            continue
+        seg = b * G + g
+        assert seg not in merged
+        merged[seg] = (cta_of_tile(seg_a), cta_of_tile(seg_a + tb - 1))
+    assert set(merged) == set(pieces)
+    for seg, (c_lo, c_hi) in merged.items():
+        assert sorted(pieces[seg]) == list(range(c_lo, c_hi + 1))
     # work balance: ranges differ by at most one tile and none is empty
     sizes = [(c + 1) * W // P - c * W // P for c in range(P)]
     assert max(sizes) - min(sizes) <= 1 and min(sizes) >= 1
