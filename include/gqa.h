@@ -70,15 +70,20 @@ int gqa_abi_version(void);
 
 /*
  * Bytes of device workspace gqa_decode needs for this shape.  The value does not
- * depend on seq_lens or on the device.  Writes *bytes and returns GQA_OK, or
- * returns the status gqa_decode would return for the same shape.
+ * depend on seq_lens or on the device; it grows with B*G and with Lmax (slots
+ * for the dynamically claimed part of long work lists, at most 8192 of them).
+ * Writes *bytes and returns GQA_OK, or returns the status gqa_decode would
+ * return for the same shape.
  *
- * The workspace holds a flag word and the split-combine partial results (one
- * (m, l, acc) triple per query head per piece of a sequence).  It MUST be
- * zero-filled before its first use (for example cudaMemsetAsync(ws, 0, bytes,
- * stream)) so that the flag word starts clear; nothing else in it needs
- * resetting between calls, whatever their shapes.  The flag word is only ever
- * OR-ed into.
+ * Layout: a 256-byte header (the flag word, the claim ticket and the failed-
+ * claim count of the dynamic work pool) followed by the split-combine partial
+ * results (one (m, l, acc) triple per query head per piece of a sequence).
+ * It MUST be zero-filled before its first use (for example
+ * cudaMemsetAsync(ws, 0, bytes, stream)) so that the header starts clear.
+ * Every call leaves the two pool counters at zero again, so nothing needs
+ * resetting between calls, whatever their shapes — except after a call that
+ * set GQA_FLAG_WAIT_TIMEOUT: zero the header (its first 256 bytes) again before
+ * the next call.  The flag word is only ever OR-ed into.
  */
 gqa_status gqa_decode_workspace_size(int B, int H, int G, int d, int Lmax, size_t *bytes);
 

@@ -14,6 +14,7 @@
 namespace {
 
 using gqa::DecodeParams;
+static_assert(gqa::kMaxCtas == GQA_MAX_CTAS, "CTA limit mismatch");
 
 constexpr int kMaxHeadsPerGroup = 64;
 constexpr int kMaxHeads = 4096;
@@ -72,11 +73,23 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr size_t kHeaderBytes = 256;
 
-// Workspace: a 256-byte header (the flag word) and the partial slots, one per
-// static piece (slot c + s < GQA_MAX_CTAS + B*G).
-size_t workspace_bytes_for(int B, int H, int G, int d) {
+constexpr long long kMaxDynTiles = 8192;   // dynamic-pool tiles the workspace holds slots for, at most
+
+// Dynamic-pool capacity (tiles) for a shape: a quarter of the most 128-position
+// tiles it can have, at most kMaxDynTiles, a whole number of chunks.
+int dyn_cap_for(int B, int G, int Lmax) {
+    const long long w_max = (long long)B * G * ((Lmax + gqa::kTile - 1) / gqa::kTile);
+    long long cap = (w_max + 3) / 4;
+    if (cap > kMaxDynTiles) cap = kMaxDynTiles;
+    return (int)(cap - cap % gqa::kChunk);
+}
+
+// Workspace: a 256-byte header (flag word, dynamic-pool ticket, failed-claim
+// count) and the partial slots: one per static piece (slot c + s <
+// GQA_MAX_CTAS + B*G), then one per dynamic-pool tile.
+size_t workspace_bytes_for(int B, int H, int G, int d, int Lmax) {
     const int n = H / G;
-    const size_t slots = (size_t)GQA_MAX_CTAS + (size_t)B * G;
+    const size_t slots = (size_t)GQA_MAX_CTAS + (size_t)B * G + (size_t)dyn_cap_for(B, G, Lmax);
     return kHeaderBytes + slots * (size_t)gqa::slot_floats(n, d) * sizeof(float);
 }
 
@@ -93,12 +106,15 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // Cache viewed as a 3-D tensor [B*G][Lmax][d] of bf16, loaded in boxes of
 // 64 columns (128 bytes, 128-byte swizzle) x 128 positions x 1.  Positions past
-// Lmax read as zero.
-bool make_cache_map(CUtensorMap *map, const void *base, int B, int G, int d, int Lmax) {
+// Lmax read as zero.  Paired (d = 64, Lmax even): viewed as [B*G][Lmax/2][128],
+// rows of two consecutive positions, so a box of 128 rows and 64 columns holds
+// the even (column 0) or the odd (column 64) positions of 256.
+bool make_cache_map(CUtensorMap *map, const void *base, int B, int G, int d, int Lmax, bool paired) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Lmax, (cuuint64_t)B * G};
-    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)Lmax * d * 2};
+    const int cols = paired ? 2 * d : d, rows = paired ? Lmax / 2 : Lmax;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)B * G};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)Lmax * d * 2};
     const cuuint32_t box[3] = {(cuuint32_t)gqa::kBoxCols, (cuuint32_t)gqa::kTile, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
@@ -159,7 +175,7 @@ gqa_status gqa_decode_workspace_size(int B, int H, int G, int d, int Lmax, size_
     if (!bytes) return GQA_ERR_INVALID_ARG;
     const gqa_status s = check_shape(B, H, G, d, Lmax);
     if (s != GQA_OK) return s;
-    *bytes = workspace_bytes_for(B, H, G, d);
+    *bytes = workspace_bytes_for(B, H, G, d, Lmax);
     return GQA_OK;
 }
 
@@ -185,7 +201,7 @@ gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache
         if (r != 0) return GQA_ERR_INVALID_ARG;
     if (o.num_ctas < 0 || o.num_ctas > GQA_MAX_CTAS) return GQA_ERR_INVALID_ARG;
     if (o.path < 0 || o.path > GQA_PATH_TCGEN05) return GQA_ERR_INVALID_ARG;
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < workspace_bytes_for(B, H, G, d))
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < workspace_bytes_for(B, H, G, d, Lmax))
         return GQA_ERR_WORKSPACE;
 
     const int n = H / G;
@@ -197,8 +213,10 @@ gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache
     s = device_info(&dev);
     if (s != GQA_OK) return s;
 
+    const bool paired = path == GQA_PATH_TCGEN05 && gqa::tc_paired(d, Lmax, n);
+    const int tile_pos = paired ? 2 * gqa::kTile : gqa::kTile;
     // One CTA per SM, never more than there are tiles.
-    const long long tiles_max = (long long)B * G * ((Lmax + gqa::kTile - 1) / gqa::kTile);
+    const long long tiles_max = (long long)B * G * ((Lmax + tile_pos - 1) / tile_pos);
     long long ctas = o.num_ctas ? o.num_ctas : dev.sms;
     if (ctas > GQA_MAX_CTAS) ctas = GQA_MAX_CTAS;
     if (ctas > tiles_max) ctas = tiles_max;
@@ -210,6 +228,12 @@ gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache
     p.seq_lens = seq_lens;
     p.out = out;
     p.flags = reinterpret_cast<unsigned int *>(ws);
+    p.ticket = reinterpret_cast<unsigned int *>(ws + 4);
+    p.fails = reinterpret_cast<unsigned int *>(ws + 8);
+    // The CUDA-core path splits statically; so does the paired d=64 tcgen05 form, whose
+    // piece ends (two GEMM parts per tile) cost more than per-SM balancing wins back.
+    p.dyn_cap = (path == GQA_PATH_TCGEN05 && !paired) ? dyn_cap_for(B, G, Lmax) : 0;
+    p.tile_shift = paired ? 8 : 7;
     p.partials = reinterpret_cast<float *>(ws + kHeaderBytes);
     p.B = B;
     p.H = H;
@@ -219,7 +243,7 @@ gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache
     p.scale_log2 = scale * 1.4426950408889634f;
 
     CUtensorMap tk, tv;
-    if (!make_cache_map(&tk, k_cache, B, G, d, Lmax) || !make_cache_map(&tv, v_cache, B, G, d, Lmax))
+    if (!make_cache_map(&tk, k_cache, B, G, d, Lmax, paired) || !make_cache_map(&tv, v_cache, B, G, d, Lmax, paired))
         return GQA_ERR_LAUNCH;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
@@ -229,7 +253,7 @@ gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache
         const int rows = gqa::tc_rows_for(n);
         CUtensorMap tq;
         if (!make_q_map(&tq, q, B, H, d, rows)) return GQA_ERR_LAUNCH;
-        e = gqa::launch_decode_tc(tk, tv, tq, p, d, (int)ctas, st);
+        e = gqa::launch_decode_tc(tk, tv, tq, p, d, paired, (int)ctas, st);
     }
     if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return GQA_ERR_LAUNCH;

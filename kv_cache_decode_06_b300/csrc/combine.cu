@@ -12,12 +12,14 @@
 //  decode-step pseudocode; arxiv:2305.13245 §2.2]
 //
 // Launched right after the decode kernel with programmatic stream
-// serialisation: its CTAs build the tile prefix (from seq_lens, which the
-// decode kernel does not write) while the decode grid drains, then wait for it
-// to complete.  CTA c handles the segment cut at the start of decode CTA c's
-// range, if that is the segment's first cut; every split segment has exactly
-// one first cut.  A thread owns four consecutive dims of one head and loads the
-// pieces in batches of eight, each batch one round trip to L2, merging online.
+// serialisation: its CTAs build the tile prefix and the work split (from
+// seq_lens, which the decode kernel does not write) while the decode grid
+// drains, then wait for it to complete.  The CTAs take segments in a
+// grid-stride loop; a segment whose single piece covered it whole was written by
+// the decode kernel, the others are merged here from the slots the work split
+// assigns to their pieces.  A thread owns four consecutive dims of one head and
+// loads the pieces in batches of eight, each batch one round trip to L2,
+// merging online.
 #include <cuda_runtime.h>
 
 #include "decode_common.cuh"
@@ -33,78 +35,78 @@ constexpr int kBatch = 8;   // pieces per round trip
 template <int D>
 __global__ void __launch_bounds__(kCombThreads) gqa_split_combine_kernel(const DecodeParams p, int grid_main) {
     __shared__ int prefix[kMaxBatch + 1];
-    __shared__ int scratch[32];
-    build_prefix(p.seq_lens, p.B, p.Lmax, prefix, scratch, nullptr);   // ends with __syncthreads
-    griddep_wait();   // the decode grid has completed: its partials are visible
-
+    __shared__ int scratch[33];
+    build_prefix(p.seq_lens, p.B, p.Lmax, p.tile_shift, prefix, scratch, nullptr);   // ends with __syncthreads
     const int G = p.G, n = p.n;
-    const long long W = (long long)G * prefix[p.B];
-    const int Pw = (int)(W < grid_main ? W : grid_main);
-    const int c = blockIdx.x;
-    if (c == 0 || c >= Pw) return;
-    const long long a = range_start(c, W, Pw);
-    const Cursor cur = cursor_at(a, prefix, p.B, G);
-    const long long seg_a = segment_start(cur, prefix, G);
-    if (seg_a == a) return;                           // decode CTA c starts a new segment: no cut here
-    const int c_lo = cta_of_tile(seg_a, W, Pw);
-    if (c_lo != c - 1) return;                        // an earlier cut of this segment merges it
-    const int c_hi = cta_of_tile(seg_a + cur.tiles - 1, W, Pw);
-    const int s = cur.b * G + cur.g, count = c_hi - c_lo + 1;
+    const WorkSplit split = make_split((long long)G * prefix[p.B], grid_main,
+                                       pool_tail_tiles(prefix, p.B, G, scratch[32]), p.dyn_cap);
+    griddep_wait();   // the decode grid has completed: its partials are visible
 
     const size_t stride = (size_t)slot_floats(n, D);
     const int aoff = slot_acc_offset(n);
-    const float *base = p.partials + (size_t)(c_lo + s) * stride;   // the pieces' slots are consecutive
-    float4 *orow = reinterpret_cast<float4 *>(p.out + ((size_t)cur.b * p.H + (size_t)cur.g * n) * D);
     const int nd4 = n * D / 4;
-    for (int e = threadIdx.x; e < nd4; e += kCombThreads) {
-        const int h = (e * 4) / D;
-        float M = -INFINITY, L = 0.f;
-        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k0 = 0; k0 < count; k0 += kBatch) {
-            float mk[kBatch], lk[kBatch];
-            float4 vk[kBatch];
+    for (int s = blockIdx.x; s < p.B * G; s += gridDim.x) {
+        const int b = s / G, g = s - b * G;
+        const int T = prefix[b + 1] - prefix[b];
+        if (T == 0) continue;
+        const long long a = (long long)G * prefix[b] + (long long)g * T;
+        const SegmentSlots sl = segment_slots(p, split, prefix, s, a, T);
+        const int count = sl.count();
+        if (count < 2) continue;   // one piece covered the segment: the decode kernel wrote it
+        float4 *orow = reinterpret_cast<float4 *>(p.out + ((size_t)b * p.H + (size_t)g * n) * D);
+        for (int e = threadIdx.x; e < nd4; e += kCombThreads) {
+            const int h = (e * 4) / D;
+            float M = -INFINITY, L = 0.f;
+            float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k0 = 0; k0 < count; k0 += kBatch) {
+                float mk[kBatch], lk[kBatch];
+                float4 vk[kBatch];
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                if (k0 + j < count) {
-                    const float *sk = base + (size_t)(k0 + j) * stride;
-                    mk[j] = __ldcg(sk + h);
-                    lk[j] = __ldcg(sk + n + h);
-                    vk[j] = __ldcg(reinterpret_cast<const float4 *>(sk + aoff) + e);
-                } else {
-                    mk[j] = -INFINITY;
-                    lk[j] = 0.f;
-                    vk[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < kBatch; ++j) {
+                    if (k0 + j < count) {
+                        const float *sk = p.partials + (size_t)sl(k0 + j) * stride;
+                        mk[j] = __ldcg(sk + h);
+                        lk[j] = __ldcg(sk + n + h);
+                        vk[j] = __ldcg(reinterpret_cast<const float4 *>(sk + aoff) + e);
+                    } else {
+                        mk[j] = -INFINITY;
+                        lk[j] = 0.f;
+                        vk[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
-            }
-            float Mb = M;
+                float Mb = M;
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) Mb = fmaxf(Mb, mk[j]);   // finite: every piece has a position
-            const float sc = ex2(M - Mb);                              // 0 on the first batch
-            L *= sc;
-            A.x *= sc;
-            A.y *= sc;
-            A.z *= sc;
-            A.w *= sc;
+                for (int j = 0; j < kBatch; ++j) Mb = fmaxf(Mb, mk[j]);   // finite: every piece has a position
+                const float sc = ex2(M - Mb);                              // 0 on the first batch
+                L *= sc;
+                A.x *= sc;
+                A.y *= sc;
+                A.z *= sc;
+                A.w *= sc;
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const float w = ex2(mk[j] - Mb);                       // 0 for the padding entries
-                L = fmaf(lk[j], w, L);
-                A.x = fmaf(vk[j].x, w, A.x);
-                A.y = fmaf(vk[j].y, w, A.y);
-                A.z = fmaf(vk[j].z, w, A.z);
-                A.w = fmaf(vk[j].w, w, A.w);
+                for (int j = 0; j < kBatch; ++j) {
+                    const float w = ex2(mk[j] - Mb);                       // 0 for the padding entries
+                    L = fmaf(lk[j], w, L);
+                    A.x = fmaf(vk[j].x, w, A.x);
+                    A.y = fmaf(vk[j].y, w, A.y);
+                    A.z = fmaf(vk[j].z, w, A.z);
+                    A.w = fmaf(vk[j].w, w, A.w);
+                }
+                M = Mb;
             }
-            M = Mb;
+            orow[e] = make_float4(A.x / L, A.y / L, A.z / L, A.w / L);
         }
-        orow[e] = make_float4(A.x / L, A.y / L, A.z / L, A.w / L);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_split_combine(const DecodeParams &p, int D, int grid_main, cudaStream_t stream) {
-    if (D == 128) return launch_pdl(gqa_split_combine_kernel<128>, grid_main, kCombThreads, 0, stream, p, grid_main);
-    return launch_pdl(gqa_split_combine_kernel<64>, grid_main, kCombThreads, 0, stream, p, grid_main);
+    // one CTA per segment, at most 4096 (the others loop over the rest)
+    const int segs = p.B * p.G;
+    const int grid = segs < 4 * kMaxCtas ? segs : 4 * kMaxCtas;
+    if (D == 128) return launch_pdl(gqa_split_combine_kernel<128>, grid, kCombThreads, 0, stream, p, grid_main);
+    return launch_pdl(gqa_split_combine_kernel<64>, grid, kCombThreads, 0, stream, p, grid_main);
 }
 
 }  // namespace gqa

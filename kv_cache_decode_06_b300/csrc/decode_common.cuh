@@ -1,24 +1,34 @@
 // Work decomposition shared by the decode kernels and the split-combine.
 //
-// Work unit: a tile of 128 consecutive cache positions of one (sequence b,
-// K/V head g) pair, a "segment".  Segment s = b*G + g holds
-// tiles_b = ceil(seq_lens[b] / 128) tiles.  All tiles of all segments form one
-// list in (b, g, j) order, W tiles long.  CTA c of P processes the contiguous
-// range [c*W/P, (c+1)*W/P): every CTA gets the same number of tiles (+-1), however
-// ragged the sequence lengths are, and the whole grid is one wave.  When there
-// are fewer tiles than CTAs, only the first W CTAs take tiles (P = min(grid, W)),
-// so no working range is empty.
+// Work unit: a tile of 128 (or, in the paired d = 64 layout, 256) consecutive
+// cache positions of one (sequence b, K/V head g) pair, a "segment".  Segment
+// s = b*G + g holds tiles_b = ceil(seq_lens[b] / tile) tiles.  All tiles of all
+// segments form one list in (b, g, j) order, W tiles long.
 //
-// A CTA's range cuts segments into "pieces".  A piece that covers its whole
-// segment is finished in place (out = acc / l).  Otherwise the piece's partial
-// softmax state (m, l, acc) goes to a workspace slot, and the split-combine
-// kernel, which runs when the decode grid has completed, merges the pieces of
-// every split segment.  The decode kernel has no atomics, counters or fences.
+// Static part.  The first Ws tiles are split evenly: CTA c of Pw = min(grid, Ws)
+// takes the contiguous range [c*Ws/Pw, (c+1)*Ws/Pw), the same number of tiles
+// (+-1) however ragged the lengths are; the grid is one wave.
 //
-// Partial slot of the piece of segment s cut by CTA c: slot = c + s.  This is
+// Dynamic part.  The last Wd = W - Ws tiles form a pool of chunks of `chunk`
+// tiles that CTAs claim, once their static range is issued, with an atomic
+// ticket: the memory bandwidth an SM gets varies by tens of percent, and the
+// CTAs that stream faster take more chunks, so the grid finishes together.
+// Every CTA makes exactly one failing claim; the one whose failing claim is the
+// grid's last resets the ticket for the next call.  Only trailing sequences
+// whose segments hold at most 16 chunks enter the pool, which bounds the pieces
+// of a segment, and the pool never exceeds the workspace's capacity.
+//
+// A range (static or chunk) cuts segments into "pieces".  A piece that covers
+// its whole segment is finished in place (out = acc / l).  Otherwise its
+// partial softmax state (m, l, acc) goes to a workspace slot, and the
+// split-combine kernel, which runs when the decode grid has completed, merges
+// the pieces of every split segment, enumerating them from the split alone.
+//
+// Partial slots.  Static piece of segment s cut by CTA c: slot c + s.  This is
 // one-to-one: if c < c' then every segment of c is <= every segment of c', so
-// c + s = c' + s' with c < c' would need s > s'.  The pieces of segment s lie in
-// slots c_lo + s .. c_hi + s, c_lo and c_hi the CTAs of its first and last tile.
+// c + s = c' + s' with c < c' would need s > s'; these slots are below
+// kMaxCtas + B*G.  Chunk j's p-th piece (a chunk of `chunk` tiles meets at most
+// `chunk` segments): slot kMaxCtas + B*G + j*chunk + p.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -28,22 +38,30 @@
 
 namespace gqa {
 
-constexpr int kTile = 128;          // cache positions per tile
+constexpr int kTile = 128;          // tensor-map rows per tile (128 positions, or 128 position pairs)
 constexpr int kBoxCols = 64;        // bf16 elements per 128-byte swizzled row
 constexpr int kBoxBytes = kTile * 128;
 constexpr int kMaxBatch = 1024;
+constexpr int kMaxCtas = 1024;        // GQA_MAX_CTAS
+constexpr int kChunk = 4;             // tiles per dynamic-pool chunk
+constexpr int kPoolSegChunks = 16;    // longest segment (in chunks) that may enter the pool
+constexpr int kPoolMinTilesPerCta = 64;   // tiles per CTA below which the split is static only
 
 struct DecodeParams {
     const __nv_bfloat16 *q;   // [B, H, D]
     const int32_t *seq_lens;  // [B]
     float *out;               // [B, H, D]
     unsigned int *flags;      // workspace flag word
+    unsigned int *ticket;     // dynamic-pool claims (zero between calls)
+    unsigned int *fails;      // failing claims (zero between calls)
+    int dyn_cap;              // pool tiles the workspace has slots for (0: no pool)
+    int tile_shift;           // log2(cache positions per tile): 7, or 8 for the paired d = 64 layout
     float *partials;          // slots of n*(D+2) floats: m[n], l[n], acc[n][D]
     int B, H, G, n, Lmax;
     float scale_log2;         // scale * log2(e): scores are kept in base-2 units
 };
 
-__device__ __forceinline__ int tiles_of(int seq) { return (seq + kTile - 1) / kTile; }
+__device__ __forceinline__ int tiles_of(int seq, int shift) { return (seq + (1 << shift) - 1) >> shift; }
 
 __device__ __forceinline__ int clamp_seq(int s, int Lmax) { return s < 0 ? 0 : (s > Lmax ? Lmax : s); }
 
@@ -54,6 +72,35 @@ __device__ __forceinline__ long long range_start(int c, long long W, int P) {
 // The CTA whose range holds tile t (0 <= t < W).
 __device__ __forceinline__ int cta_of_tile(long long t, long long W, int P) {
     return (int)(((t + 1) * P - 1) / W);
+}
+
+// The split of the W tiles between the static ranges and the dynamic pool.
+struct WorkSplit {
+    long long W, Ws;   // all tiles; statically split tiles
+    int Pw;            // CTAs with a static range
+    int nchunks;       // chunks in the pool (0: no dynamic part)
+};
+
+// grid = launched CTAs.  The pool takes a quarter of the tiles, at most
+// `pool_max` (the short trailing segments) and `cap` (workspace slots), and only
+// when there are at least kPoolMinTilesPerCta tiles per CTA: every chunk ends a
+// piece (about a microsecond of pipeline drain), which pays only when the
+// static ranges are long enough for per-SM bandwidth differences to add up to
+// more than that.  cap = 0 disables it.
+__device__ __forceinline__ WorkSplit make_split(long long W, int grid, long long pool_max, int cap) {
+    WorkSplit w;
+    w.W = W;
+    long long Wd = 0;
+    if (cap > 0 && W >= (long long)kPoolMinTilesPerCta * grid) {
+        Wd = W / 4;
+        if (Wd > pool_max) Wd = pool_max;
+        if (Wd > cap) Wd = cap;
+        Wd -= Wd % kChunk;
+    }
+    w.Ws = W - Wd;
+    w.nchunks = (int)(Wd / kChunk);
+    w.Pw = (int)(w.Ws < grid ? w.Ws : grid);
+    return w;
 }
 
 struct Cursor {
@@ -85,12 +132,19 @@ __device__ __forceinline__ void cursor_next(Cursor &c, const int *prefix, int B,
     if (c.b < B) c.tiles = prefix[c.b + 1] - prefix[c.b];
 }
 
+// First tile of the cursor's segment in the tile list.
+__device__ __forceinline__ long long segment_start(const Cursor &c, const int *prefix, int G) {
+    return (long long)G * prefix[c.b] + (long long)c.g * c.tiles;
+}
+
 // Block-wide: clamps seq_lens into [0, Lmax] and writes the tile prefix sums;
-// with a flag word, CTA 0 records a clamp in it.  `scratch` needs 32 ints.
-// Ends with __syncthreads().
-__device__ inline void build_prefix(const int32_t *seq_lens, int B, int Lmax, int *prefix, int *scratch,
-                             unsigned int *flags) {
+// with a flag word, CTA 0 records a clamp in it.  `scratch` needs 33 ints;
+// scratch[32] receives the last sequence whose segments are too long for the
+// dynamic pool (-1 if none).  Ends with __syncthreads().
+__device__ inline void build_prefix(const int32_t *seq_lens, int B, int Lmax, int shift, int *prefix, int *scratch,
+                                    unsigned int *flags) {
     const int tid = threadIdx.x, nth = blockDim.x;
+    if (tid == 0) scratch[32] = -1;
     const int per = (B + nth - 1) / nth;
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
     int local = 0;
@@ -98,7 +152,7 @@ __device__ inline void build_prefix(const int32_t *seq_lens, int B, int Lmax, in
     for (int b = b0; b < b1; ++b) {
         const int s = __ldg(seq_lens + b);
         bad |= (s < 0 || s > Lmax);
-        local += tiles_of(clamp_seq(s, Lmax));
+        local += tiles_of(clamp_seq(s, Lmax), shift);
     }
     // exclusive scan of `local` over the block
     const int lane = tid & 31, warp = tid >> 5, nwarps = (nth + 31) >> 5;
@@ -116,11 +170,14 @@ __device__ inline void build_prefix(const int32_t *seq_lens, int B, int Lmax, in
         if (w < warp) before += x;
         total += x;
     }
-    int run = before + incl - local;
+    int run = before + incl - local, last_long = -1;
     for (int b = b0; b < b1; ++b) {
         prefix[b] = run;
-        run += tiles_of(clamp_seq(__ldg(seq_lens + b), Lmax));
+        const int tb = tiles_of(clamp_seq(__ldg(seq_lens + b), Lmax), shift);
+        run += tb;
+        if (tb > kPoolSegChunks * kChunk) last_long = b;
     }
+    if (last_long >= 0) atomicMax(scratch + 32, last_long);
     if (tid == 0) prefix[B] = total;
     if (bad && flags && blockIdx.x == 0) atomicOr(flags, 0x1u /* GQA_FLAG_SEQ_LEN_CLAMPED */);
     __syncthreads();
@@ -146,9 +203,57 @@ __device__ __forceinline__ float *slot_ptr(const DecodeParams &p, int slot, int 
     return p.partials + (size_t)slot * (size_t)slot_floats(p.n, D);
 }
 
-// First tile of the cursor's segment in the tile list.
-__device__ __forceinline__ long long segment_start(const Cursor &c, const int *prefix, int G) {
-    return (long long)G * prefix[c.b] + (long long)c.g * c.tiles;
+// Tiles after the last sequence too long for the pool (build_prefix's scratch[32]).
+__device__ __forceinline__ long long pool_tail_tiles(const int *prefix, int B, int G, int last_long) {
+    return (long long)G * (prefix[B] - prefix[last_long + 1]);
+}
+
+// Slot of the p-th piece of dynamic chunk j.
+__device__ __forceinline__ int chunk_slot(const DecodeParams &p, int j, int piece) {
+    return kMaxCtas + p.B * p.G + j * kChunk + piece;
+}
+
+// Slots of every piece of one segment, in tile order: `ns` static pieces in
+// slots s0, s0 + 1, ..., then `nd` chunk pieces: d0 for the first, then
+// d1, d1 + kChunk, d1 + 2 * kChunk, ... (later chunks start inside the segment,
+// so their piece index is 0).
+struct SegmentSlots {
+    int ns, s0, nd, d0, d1;
+    __device__ __forceinline__ int count() const { return ns + nd; }
+    __device__ __forceinline__ int operator()(int k) const {
+        if (k < ns) return s0 + k;
+        k -= ns;
+        return k == 0 ? d0 : d1 + (k - 1) * kChunk;
+    }
+};
+
+// The pieces of segment s = b*G + g, which starts at tile a and holds T tiles.
+__device__ __forceinline__ SegmentSlots segment_slots(const DecodeParams &p, const WorkSplit &w, const int *prefix,
+                                                      int s, long long a, int T) {
+    SegmentSlots r{0, 0, 0, 0, 0};
+    const long long e = a + T;   // one past the last tile
+    if (a < w.Ws) {
+        const long long hi = (e < w.Ws ? e : w.Ws) - 1;
+        const int c_lo = cta_of_tile(a, w.Ws, w.Pw), c_hi = cta_of_tile(hi, w.Ws, w.Pw);
+        r.ns = c_hi - c_lo + 1;
+        r.s0 = c_lo + s;
+    }
+    if (e > w.Ws) {
+        const long long lo = a > w.Ws ? a : w.Ws;
+        const int j_lo = (int)((lo - w.Ws) / kChunk), j_hi = (int)((e - 1 - w.Ws) / kChunk);
+        // the segment's piece index in chunk j_lo = segments met in the chunk before
+        // it (segment numbers skip empty sequences, so count them by walking)
+        Cursor c0 = cursor_at(w.Ws + (long long)j_lo * kChunk, prefix, p.B, p.G);
+        int p_lo = 0;
+        while (c0.b * p.G + c0.g != s && p_lo < kChunk) {
+            c0 = cursor_at(segment_start(c0, prefix, p.G) + c0.tiles, prefix, p.B, p.G);
+            ++p_lo;
+        }
+        r.nd = j_hi - j_lo + 1;
+        r.d0 = chunk_slot(p, j_lo, p_lo);
+        r.d1 = chunk_slot(p, j_lo + 1, 0);
+    }
+    return r;
 }
 
 // 2^x with the hardware approximation (relative error ~2^-22); 2^-inf = +0.

@@ -40,8 +40,8 @@ struct SimtCfg {
     static constexpr int kOffM = kOffAcc + kWarps * NMAX * D * 4;          // f32 [W][NMAX]
     static constexpr int kOffL = kOffM + kWarps * NMAX * 4;                // f32 [W][NMAX]
     static constexpr int kOffPrefix = kOffL + kWarps * NMAX * 4;           // i32 [kMaxBatch + 1]
-    static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 1) * 4;   // i32 [32]
-    static constexpr int kOffBar = (kOffScratch + 32 * 4 + 7) / 8 * 8;    // u64 full[S], empty[S], grp
+    static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 1) * 4;   // i32 [33]
+    static constexpr int kOffBar = (kOffScratch + 33 * 4 + 7) / 8 * 8;    // u64 full[S], empty[S], grp
     static constexpr int kOffFlags = kOffBar + (2 * kStages + 1) * 8;      // abort, last
     static constexpr int kSmemBytes = kOffFlags + 16 + 1024;               // + alignment slack
 };
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(SimtCfg<D, NMAX>::kThreads, 1)
     // have completed.
     griddep_wait();
     griddep_launch_dependents();
-    build_prefix(p.seq_lens, p.B, p.Lmax, prefix, scratch, p.flags);  // ends with __syncthreads
+    build_prefix(p.seq_lens, p.B, p.Lmax, 7, prefix, scratch, p.flags);  // ends with __syncthreads
 
     const int G = p.G, n = p.n;
     const long long W = (long long)G * prefix[p.B];

@@ -12,9 +12,9 @@
 // ["Grouped-query attention (GQA)" concept page, "Implementation sketch",
 //  decode-step pseudocode; arxiv:2305.13245 §2.2]
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
-// owner, warps 2-5 = softmax + epilogue (thread <-> TMEM lane: a position of
-// the tile for S, a head dim for O).
+// Warp roles (224 threads): warp 0 = TMA producer, warp 1 = score-GEMM issuer and
+// TMEM owner, warp 6 = value-GEMM issuer, warps 2-5 = softmax + epilogue
+// (thread <-> TMEM lane: a position of the tile for S, a head dim for O).
 //
 // Producer and MMA issuer are event loops: each issues the next operation
 // whose inputs are ready.  K slot s is handed back as soon as the score GEMM of
@@ -23,8 +23,9 @@
 //   1. loads its S row, reduces the per-head maximum over the 128 positions
 //      (transposed butterfly in the warp, then the 4 warps via shared memory),
 //   2. writes P(i) and hands it to the MMA warp,
-//   3. folds the previous tile's O into register accumulators with that tile's
-//      rescale factor (so TMEM never needs rescaling).
+//   3. folds the O of the tile two steps back into register accumulators with
+//      that tile's rescale factor (so TMEM never needs rescaling); O is triple
+//      buffered in TMEM, so a value GEMM has two softmax steps to finish.
 // Work split and pieces are shared with the CUDA-core path (decode_common.cuh);
 // pieces that are not a whole segment leave their partial state in the
 // workspace for the split-combine kernel (combine.cu).
@@ -77,9 +78,9 @@ enum TraceSlot {
     kTrSIssue = 144,      // + i: score GEMM of tile i issued
     kTrPvIssue = 272,     // + i: value GEMM of tile i issued
     kTrSFull = 400,       // + i: softmax saw S(i)
-    kTrMax = 528,         // + i: tile maximum agreed
+    kTrKReady = 528,      // + i: the MMA issuer first sees K(i) landed
     kTrPFull = 656,       // + i: P(i) handed over
-    kTrFold = 784,        // + i: previous O folded
+    kTrVReady = 784,      // + i: the MMA issuer first sees V(i) landed
     kTrPieceEnd = 912     // + 2k / + 2k + 1: start / end of the k-th piece epilogue
 };
 
@@ -88,50 +89,90 @@ constexpr int kSmemLimit = 232448;   // 227 KB opt-in per CTA
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
+constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512; }
+
+constexpr int kRing = 4;   // work ranges in flight from the producer to the other roles
+
+// One work range (the static range or a claimed chunk) as the producer hands it on.
+struct RangeEntry {
+    long long ub;   // first tile
+    int len;        // tiles
+    int chunk;      // chunk id, -1 for the static range, -2 = no more work
+};
+
 // D = head dim, N = MMA N (>= 16), NH = heads held per thread (power of two >= n).
-template <int D, int N, int NH>
+// kPair (D = 64 only): the cache is read as rows of two positions (256 bytes), a
+// tile is 128 such rows = 256 positions in two column boxes (even positions,
+// odd positions), and scores and values run as two GEMMs per tile, one per box.
+// A tile then moves as many bytes as a D = 128 tile, so the per-tile work of
+// the softmax group is spread over twice the positions.
+template <int D, bool kPair, int N, int NH>
 struct TcCfg {
-    static constexpr int kBoxes = D / kBoxCols;
-    static constexpr int kTileBytes = kBoxes * kBoxBytes;        // one K or V tile (128 positions)
-    static constexpr int kQBytes = kBoxes * N * 128;             // one Q buffer (N rows x d)
-    static constexpr int kPBytes = 2 * N * 128;                  // one P part: N rows x 128 positions
+    static_assert(!kPair || D == 64, "the paired layout is for D = 64");
+    static constexpr int kColBoxes = (D == 128 || kPair) ? 2 : 1;   // 64-column boxes per tile row
+    static constexpr int kQBoxes = D / kBoxCols;                     // 64-column boxes per q row
+    static constexpr int kParts = kPair ? 2 : 1;                     // score GEMMs per tile
+    static constexpr int kTileShift = kPair ? 8 : 7;                 // log2(positions per tile)
+    static constexpr int kTilePos = 1 << kTileShift;
+    static constexpr int kTileBytes = kColBoxes * kBoxBytes;         // one K or V tile
+    static constexpr int kQBytes = kQBoxes * N * 128;                // one Q buffer (N rows x d)
+    // N of the value GEMM: with M = 64 (D = 64) N may be 8, which halves the P
+    // buffers when a group has at most 8 heads
+    static constexpr int kNPV = (D == 64 && NH <= 8) ? 8 : N;
+    static constexpr int kPBytes = 2 * kNPV * 128;                   // one P part: kNPV rows x 128 positions
+    static constexpr int kPBufBytes = 2 * kParts * kPBytes;          // one P buffer: [part][hi, lo]
     // small shared state, in floats
     static constexpr int kRedF = 2 * 4 * NH;                     // [2][4 warps][NH] tile maxima
     static constexpr int kLredF = 4 * NH;                        // [4 warps][NH] l sums
     static constexpr int kMF = 3 * NH;                           // [3][NH] running max after tile i
-    static constexpr int kAF = 3 * NH;                           // [3][NH] rescale factor of tile i
-    static constexpr int kSmallBytes = 4 * (kRedF + kLredF + kMF + kAF) + 32 * 4 + (kMaxBatch + 1) * 4;
-    static constexpr int bar_bytes(int S, int QB) { return (4 * S + 2 * QB + 12 + 2) * 8 + 16; }
-    static constexpr int fixed_bytes(int S, int QB) {
-        return QB * kQBytes + 4 * kPBytes + kSmallBytes + bar_bytes(S, QB) + 1024 /* alignment slack */;
+    static constexpr int kAF = 4 * NH;                           // [4][NH] rescale factor of tile i
+    static constexpr int kSmallBytes = 4 * (kRedF + kLredF + kMF + kAF) + 33 * 4 + (kMaxBatch + 1) * 4 + kRing * 16;
+    static constexpr int bar_bytes(int SK, int SV, int QB) { return (2 * SK + 2 * SV + 2 * QB + 14 + 2 + 2 * kRing) * 8 + 16; }
+    static constexpr int fixed_bytes(int QB) {
+        return QB * kQBytes + 2 * kPBufBytes + kSmallBytes + bar_bytes(8, 8, QB) + 1024 /* alignment slack */;
     }
-    static constexpr int stages_for(int QB) { return cmin(8, (kSmemLimit - fixed_bytes(8, QB)) / (2 * kTileBytes)); }
-    static constexpr int kQBuf = stages_for(2) >= 3 || stages_for(1) == stages_for(2) ? 2 : 1;
-    static constexpr int kStages = stages_for(kQBuf);
-    static_assert(kStages >= 2, "shared memory too small for two stages");
+    // K and V rings: as deep as shared memory allows (at most 8), V one deeper when
+    // a single extra tile still fits (V slots are held until the value GEMM is done)
+    static constexpr int avail(int QB) { return kSmemLimit - fixed_bytes(QB); }
+    static constexpr int pairs_for(int QB) { return cmin(8, avail(QB) / (2 * kTileBytes)); }
+    static constexpr int kQBuf = pairs_for(2) >= 3 || pairs_for(1) == pairs_for(2) ? 2 : 1;
+    static constexpr int kSK = pairs_for(kQBuf);
+    static constexpr int kSV = (kSK < 8 && avail(kQBuf) - 2 * kSK * kTileBytes >= kTileBytes) ? kSK + 1 : kSK;
+    static_assert(kSK >= 2, "shared memory too small for two stages");
+    // P buffers: three when they fit beside the rings (the softmax then waits for the
+    // value GEMM three tiles back before reusing one), else two
+    static constexpr int layout_bytes(int pbuf) {
+        return (kSK + kSV) * kTileBytes + kQBuf * kQBytes + pbuf * kPBufBytes + kSmallBytes + 8 +
+               (2 * kSK + 2 * kSV + 2 * kQBuf + 12 + pbuf + 2 + 2 * kRing) * 8 + 16 + 1024;
+    }
+    static constexpr int kPBuf = layout_bytes(3) <= kSmemLimit ? 3 : 2;
     // layout (offsets from the 1024-aligned base)
-    static constexpr int kOffK = 0;                                       // [S] K tiles
-    static constexpr int kOffV = kStages * kTileBytes;                    // [S] V tiles
-    static constexpr int kOffQ = 2 * kStages * kTileBytes;                // [QB] Q buffers
-    static constexpr int kOffP = kOffQ + kQBuf * kQBytes;                 // [2 buffers][hi, lo]
-    static constexpr int kOffRed = kOffP + 4 * kPBytes;
+    static constexpr int kOffK = 0;                                       // [SK] K tiles
+    static constexpr int kOffV = kSK * kTileBytes;                        // [SV] V tiles
+    static constexpr int kOffQ = kOffV + kSV * kTileBytes;                // [QB] Q buffers
+    static constexpr int kOffP = kOffQ + kQBuf * kQBytes;                 // [PB buffers][part][hi, lo]
+    static constexpr int kOffRed = kOffP + kPBuf * kPBufBytes;
     static constexpr int kOffLred = kOffRed + kRedF * 4;
     static constexpr int kOffM = kOffLred + kLredF * 4;
     static constexpr int kOffA = kOffM + kMF * 4;
     static constexpr int kOffPrefix = kOffA + kAF * 4;                    // i32 [kMaxBatch + 1]
-    static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 1) * 4;  // i32 [32]
-    static constexpr int kOffBar = (kOffScratch + 32 * 4 + 7) / 8 * 8;
-    // barriers: kfull[S] vfull[S] kempty[S] vempty[S] qfull[QB] qempty[QB] sfull[2] sfree[2]
-    //           pfull[2] ofull[2] ofree[2] red[2] grp done
-    static constexpr int kNumBars = 4 * kStages + 2 * kQBuf + 12 + 2;
+    static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 1) * 4;  // i32 [33]
+    static constexpr int kOffRing = (kOffScratch + 33 * 4 + 15) / 16 * 16;  // RangeEntry [kRing]
+    static constexpr int kOffBar = kOffRing + kRing * 16;
+    // barriers: kfull[SK] kempty[SK] vfull[SV] vempty[SV] qfull[QB] qempty[QB] sfull[2] sfree[2]
+    //           pfull[PB] ofull[3] ofree[3] red[2] grp done
+    static constexpr int kNumBars = 2 * kSK + 2 * kSV + 2 * kQBuf + 12 + kPBuf + 2 + 2 * kRing;
     static constexpr int kOffFlags = kOffBar + kNumBars * 8;     // abort, tmem base
     static constexpr int kSmemBytes = kOffFlags + 16 + 1024;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory layout too large");
     static_assert(NH < 4 || (kOffRed % 16 == 0 && kOffLred % 16 == 0 && kOffM % 16 == 0 && kOffA % 16 == 0),
                   "float4 alignment");
-    static constexpr int kThreads = 192;
-    static constexpr int kTmemCols = (4 * N <= 32) ? 32 : (4 * N <= 64) ? 64 : (4 * N <= 128) ? 128 : 256;
-    static constexpr int kPvM = (D == 128) ? 128 : 64;
+    static constexpr int kThreads = 224;
+    // TMEM: S accumulators [2][part][N] then O accumulators [3][kNPV] (O is folded two tiles behind)
+    static constexpr int kOCol = 2 * kParts * N;
+    static constexpr int kTmemCols = pow2_cols(kOCol + 3 * kNPV);
+    static_assert(kOCol + 3 * kNPV <= 512, "TMEM columns");
+    static constexpr int kPvM = D;
     // butterfly: number of head-halving steps (the rest are plain reductions)
     static constexpr int kHalve = ilog2(NH) < 5 ? ilog2(NH) : 5;
 };
@@ -236,12 +277,12 @@ __device__ __forceinline__ void store_vec(float *dst, const float (&v)[NH]) {
     }
 }
 
-template <int D, int N, int NH>
-__global__ void __launch_bounds__(192, 1)
+template <int D, bool kPair, int N, int NH>
+__global__ void __launch_bounds__(224, 1)
     gqa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
-    using C = TcCfg<D, N, NH>;
-    constexpr int S = C::kStages, QB = C::kQBuf;
+    using C = TcCfg<D, kPair, N, NH>;
+    constexpr int SK = C::kSK, SV = C::kSV, QB = C::kQBuf, NP = C::kParts, PB = C::kPBuf;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *red = reinterpret_cast<float *>(smem + C::kOffRed);
@@ -251,10 +292,11 @@ __global__ void __launch_bounds__(192, 1)
     int *prefix = reinterpret_cast<int *>(smem + C::kOffPrefix);
     int *scratch = reinterpret_cast<int *>(smem + C::kOffScratch);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
-    uint64_t *kfull = bars, *vfull = kfull + S, *kempty = vfull + S, *vempty = kempty + S;
-    uint64_t *qfull = vempty + S, *qempty = qfull + QB;
-    uint64_t *sfull = qempty + QB, *sfree = sfull + 2, *pfull = sfree + 2, *ofull = pfull + 2, *ofree = ofull + 2;
-    uint64_t *redbar = ofree + 2, *grp = redbar + 2, *done = grp + 1;
+    uint64_t *kfull = bars, *kempty = kfull + SK, *vfull = kempty + SK, *vempty = vfull + SV;
+    uint64_t *qfull = vempty + SV, *qempty = qfull + QB;
+    uint64_t *sfull = qempty + QB, *sfree = sfull + 2, *pfull = sfree + 2, *ofull = pfull + PB, *ofree = ofull + 3;
+    uint64_t *redbar = ofree + 3, *grp = redbar + 2, *done = grp + 1, *rfull = done + 1, *rempty = rfull + kRing;
+    RangeEntry *ring = reinterpret_cast<RangeEntry *>(smem + C::kOffRing);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::kOffFlags);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::kOffFlags + 8);
 
@@ -267,10 +309,12 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
+        for (int s = 0; s < SK; ++s) {
             mbar_init(&kfull[s], 1);
-            mbar_init(&vfull[s], 1);
             mbar_init(&kempty[s], 1);
+        }
+        for (int s = 0; s < SV; ++s) {
+            mbar_init(&vfull[s], 1);
             mbar_init(&vempty[s], 1);
         }
         for (int s = 0; s < QB; ++s) {
@@ -280,13 +324,19 @@ __global__ void __launch_bounds__(192, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&sfull[s], 1);
             mbar_init(&sfree[s], 128);
-            mbar_init(&pfull[s], 128);
-            mbar_init(&ofull[s], 1);
-            mbar_init(&ofree[s], 128);
             mbar_init(&redbar[s], 4);
         }
+        for (int s = 0; s < PB; ++s) mbar_init(&pfull[s], 128);
+        for (int s = 0; s < 3; ++s) {
+            mbar_init(&ofull[s], 1);
+            mbar_init(&ofree[s], 128);
+        }
         mbar_init(grp, 128);
-        mbar_init(done, 1);
+        for (int s = 0; s < kRing; ++s) {
+            mbar_init(&rfull[s], 1);
+            mbar_init(&rempty[s], 2 + 128);   // both MMA issuers and the 128 softmax threads
+        }
+        mbar_init(done, 2);   // one commit from each MMA issuer
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -303,49 +353,90 @@ __global__ void __launch_bounds__(192, 1)
     // grids this one depends on have completed.
     griddep_wait();
     griddep_launch_dependents();
-    build_prefix(p.seq_lens, p.B, p.Lmax, prefix, scratch, p.flags);   // ends with __syncthreads
+    build_prefix(p.seq_lens, p.B, p.Lmax, C::kTileShift, prefix, scratch, p.flags);   // ends with __syncthreads
     tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
     if (tid == 64) GQA_TRACE_AT(kTrSetup, clock64());
 
     const int G = p.G, n = p.n;
-    const long long W = (long long)G * prefix[p.B];
-    const int Pw = (int)(W < P ? W : P);
-    long long u0 = 0, u1 = 0;
-    if ((int)blockIdx.x < Pw) {
-        u0 = range_start(blockIdx.x, W, Pw);
-        u1 = range_start(blockIdx.x + 1, W, Pw);
-    }
-    const int ntiles = (int)(u1 - u0);
-    if (tid == 64) GQA_TRACE_AT(kTrTiles, ntiles);
+    const WorkSplit wsplit = make_split((long long)G * prefix[p.B], P, pool_tail_tiles(prefix, p.B, G, scratch[32]),
+                                        p.dyn_cap);
     int kissued = 0, vissued = 0, qissued = 0;
 
     if (warp == 0) {
         // ================================================================ producer
-        if (lane == 0 && ntiles > 0) {
+        // Hands every work range to the other roles through the ring: the static
+        // range first, then one claimed chunk at a time, then an end marker.
+        if (lane == 0) {
             const uint64_t pol_kv = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
-            Cursor kc = cursor_at(u0, prefix, p.B, G);
-            Cursor vc = kc;
-            int piece = 0;
-            uint32_t idle = 0;
-            uint64_t idle_t0 = 0;
-            while (vissued < ntiles) {
+            RangeEntry next{0, 0, -1};
+            bool have_next = false;
+            if ((int)blockIdx.x < wsplit.Pw) {
+                next.ub = range_start(blockIdx.x, wsplit.Ws, wsplit.Pw);
+                next.len = (int)(range_start(blockIdx.x + 1, wsplit.Ws, wsplit.Pw) - next.ub);
+                have_next = next.len > 0;
+            }
+            int pushed = 0, piece = 0, v_r = 0;
+            bool k_done = false, v_done = false;
+            long long k_u = 0, k_end = 0, k_ub = 0, v_u = 0, v_end = 0;
+            Cursor kc{0, 0, 0, 1}, vc{0, 0, 0, 1};
+            IdlePoll poll;
+            while (!v_done) {
                 bool progress = false;
-                // ---- K of tile kissued (and Q when it starts a piece)
-                if (kissued < ntiles) {
+                // ---- the next range, once the K side has issued the current one
+                if (!k_done && k_u == k_end) {
+                    if (!have_next) {
+                        next.chunk = -2;
+                        next.len = 0;
+                        if (wsplit.nchunks > 0) {
+                            const unsigned j = atomicAdd(p.ticket, 1u);
+                            if (j < (unsigned)wsplit.nchunks) {
+                                next.ub = wsplit.Ws + (long long)j * kChunk;
+                                next.len = kChunk;
+                                next.chunk = (int)j;
+                            } else if (atomicAdd(p.fails, 1u) == (unsigned)P - 1) {
+                                // every CTA has failed once: nobody claims again in this launch
+                                atomicExch(p.ticket, 0u);
+                                atomicExch(p.fails, 0u);
+                            }
+                        }
+                        have_next = true;
+                    }
+                    const int slot = pushed % kRing;
+                    if (pushed < kRing ||
+                        (v_r > pushed - kRing && mbar_test_wait(&rempty[slot], ((pushed / kRing) - 1) & 1))) {
+                        ring[slot] = next;
+                        mbar_arrive(&rfull[slot]);   // release: the entry is visible to the waiters
+                        ++pushed;
+                        have_next = false;
+                        if (next.chunk == -2) {
+                            k_done = true;
+                        } else {
+                            k_ub = k_u = next.ub;
+                            k_end = next.ub + next.len;
+                            kc = cursor_at(k_u, prefix, p.B, G);
+                        }
+                        progress = true;
+                    }
+                }
+                // ---- K of the next tile (and Q when it starts a piece)
+                if (k_u < k_end) {
                     const int i = kissued;
-                    const bool first = (i == 0) || (kc.j == 0);
-                    const bool last = (i + 1 == ntiles) || (kc.j + 1 == kc.tiles);
-                    const int st = i % S, qb = piece % QB;
-                    if ((!first || piece < QB || mbar_test_wait(&qempty[qb], ((piece / QB) - 1) & 1)) &&
-                        (i < S || mbar_test_wait(&kempty[st], ((i / S) - 1) & 1))) {
+                    const bool first = (k_u == k_ub) || (kc.j == 0);
+                    const bool last = (k_u + 1 == k_end) || (kc.j + 1 == kc.tiles);
+                    const int st = i % SK, qb = piece % QB;
+                    // K runs at most one tile ahead of V: a tile's V then lands about when its
+                    // probabilities are ready, and a piece's last value GEMM does not wait long
+                    if (vissued >= i &&
+                        (!first || piece < QB || mbar_test_wait(&qempty[qb], ((piece / QB) - 1) & 1)) &&
+                        (i < SK || mbar_test_wait(&kempty[st], ((i / SK) - 1) & 1))) {
                         if (first) {
                             mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
                             uint8_t *qdst = smem + C::kOffQ + qb * C::kQBytes;
                             const int y = kc.b * p.H + kc.g * n;
 #pragma unroll
-                            for (int c = 0; c < C::kBoxes; ++c)
+                            for (int c = 0; c < C::kQBoxes; ++c)
                                 tma_load_2d(qdst + c * N * 128, &tm_q, c * kBoxCols, y, &qfull[qb], pol_q);
                             ++qissued;
                             if (i == 0) GQA_TRACE_AT(kTrFirstQ, clock64());
@@ -354,75 +445,118 @@ __global__ void __launch_bounds__(192, 1)
                         const int z = kc.b * G + kc.g, y = kc.j * kTile;
                         mbar_arrive_expect_tx(&kfull[st], C::kTileBytes);
 #pragma unroll
-                        for (int c = 0; c < C::kBoxes; ++c)
+                        for (int c = 0; c < C::kColBoxes; ++c)
                             tma_load_3d(kdst + c * kBoxBytes, &tm_k, c * kBoxCols, y, z, &kfull[st], pol_kv);
                         if (i == 0) GQA_TRACE_AT(kTrFirstK, clock64());
                         if (i < 128) GQA_TRACE_AT(kTrKIssue + i, clock64());
                         ++kissued;
+                        ++k_u;
                         if (last) ++piece;
                         cursor_next(kc, prefix, p.B, G);
                         progress = true;
                     }
                 }
-                // ---- V of tile vissued (never ahead of its K)
-                if (vissued < kissued) {
-                    const int i = vissued, st = i % S;
-                    if (i < S || mbar_test_wait(&vempty[st], ((i / S) - 1) & 1)) {
+                // ---- V of the next tile (walks the same ranges, never ahead of K)
+                if (v_u == v_end && v_r < pushed) {
+                    const RangeEntry e = ring[v_r % kRing];   // written by this thread
+                    ++v_r;
+                    if (e.chunk == -2) {
+                        v_done = true;
+                    } else {
+                        v_u = e.ub;
+                        v_end = e.ub + e.len;
+                        vc = cursor_at(v_u, prefix, p.B, G);
+                    }
+                    progress = true;
+                }
+                if (v_u < v_end && vissued < kissued) {
+                    const int i = vissued, st = i % SV;
+                    if (i < SV || mbar_test_wait(&vempty[st], ((i / SV) - 1) & 1)) {
                         uint8_t *vdst = smem + C::kOffV + st * C::kTileBytes;
                         const int z = vc.b * G + vc.g, y = vc.j * kTile;
                         mbar_arrive_expect_tx(&vfull[st], C::kTileBytes);
 #pragma unroll
-                        for (int c = 0; c < C::kBoxes; ++c)
+                        for (int c = 0; c < C::kColBoxes; ++c)
                             tma_load_3d(vdst + c * kBoxBytes, &tm_v, c * kBoxCols, y, z, &vfull[st], pol_kv);
                         ++vissued;
+                        ++v_u;
                         cursor_next(vc, prefix, p.B, G);
                         progress = true;
                     }
                 }
                 if (progress) {
-                    idle = 0;
-                } else {
-                    if (idle == 0) idle_t0 = globaltimer_ns();
-                    if ((++idle & 63u) == 0) {
-                        if (*s_abort) break;
-                        if (globaltimer_ns() - idle_t0 > kWaitLimitNs) {
-                            *s_abort = 1;
-                            atomicOr(p.flags, 0x2u /* GQA_FLAG_WAIT_TIMEOUT */);
-                            break;
-                        }
-                    }
+                    poll.progressed();
+                } else if (!poll.step(ab)) {
+                    break;
                 }
             }
         }
-    } else if (warp == 1) {
-        // ================================================================ MMA issuer
-        if (lane == 0 && ntiles > 0) {
+    } else if (warp == 1 || warp == 6) {
+        // ================================================================ MMA issuers
+        // Warp 1 issues the score GEMMs, warp 6 the value GEMMs: a tcgen05.mma takes
+        // tens of nanoseconds to issue, and two issuing threads halve the serial time
+        // per tile.  Each writes its own accumulators and commits its own barriers.
+        const bool do_s = warp == 1, do_pv = warp == 6;
+        if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(128, N, false, false);
-            constexpr uint32_t idPV = idesc_bf16_f32(C::kPvM, N, true, false);
+            constexpr uint32_t idPV = idesc_bf16_f32(C::kPvM, C::kNPV, true, false);
             const uint32_t sbase = smem_addr(smem);
-            Cursor cur = cursor_at(u0, prefix, p.B, G);
-            int s_i = 0, pv_i = 0, piece = 0;
-            uint32_t idle = 0;
-            uint64_t idle_t0 = 0;
-            while (pv_i < ntiles) {
+            Cursor cur{0, 0, 0, 1};
+            long long s_u = 0, s_end = 0, s_ub = 0;
+            int s_i = 0, pv_i = 0, piece = 0, r_read = 0, pv_avail = 0;
+            bool ranges_done = false;   // the end marker has been read
+#ifdef GQA_TRACE
+            int k_seen = -1, v_seen = -1;
+#endif
+            IdlePoll poll;
+            while (!(ranges_done && (do_s ? s_u == s_end : pv_i == pv_avail))) {
                 bool progress = false;
+                // ---- the next range, once this role has used up the current one
+                if (!ranges_done && (do_s ? s_u == s_end : pv_i == pv_avail)) {
+                    const int slot = r_read % kRing;
+                    if (mbar_test_wait(&rfull[slot], (r_read / kRing) & 1)) {
+                        const RangeEntry e = ring[slot];
+                        mbar_arrive(&rempty[slot]);
+                        ++r_read;
+                        if (e.chunk == -2) {
+                            ranges_done = true;
+                        } else if (do_s) {
+                            s_ub = s_u = e.ub;
+                            s_end = e.ub + e.len;
+                            cur = cursor_at(s_u, prefix, p.B, G);
+                        } else {
+                            pv_avail += e.len;
+                        }
+                        progress = true;
+                    }
+                }
                 // ---- scores of tile s_i: needs its K, its piece's Q and a free S buffer
-                if (s_i < ntiles) {
-                    const bool first = (s_i == 0) || (cur.j == 0);
-                    const bool last = (s_i + 1 == ntiles) || (cur.j + 1 == cur.tiles);
-                    const int st = s_i % S, bi = s_i & 1, qb = piece % QB;
-                    if ((!first || mbar_test_wait(&qfull[qb], (piece / QB) & 1)) &&
-                        mbar_test_wait(&kfull[st], (s_i / S) & 1) &&
+                if (do_s && s_u < s_end) {
+                    const bool first = (s_u == s_ub) || (cur.j == 0);
+                    const bool last = (s_u + 1 == s_end) || (cur.j + 1 == cur.tiles);
+                    const int st = s_i % SK, bi = s_i & 1, qb = piece % QB;
+                    const bool kready = mbar_test_wait(&kfull[st], (s_i / SK) & 1);
+#ifdef GQA_TRACE
+                    if (kready && s_i > k_seen) {
+                        if (s_i < 128) GQA_TRACE_AT(kTrKReady + s_i, clock64());
+                        k_seen = s_i;
+                    }
+#endif
+                    if ((!first || mbar_test_wait(&qfull[qb], (piece / QB) & 1)) && kready &&
                         (s_i < 2 || mbar_test_wait(&sfree[bi], ((s_i >> 1) - 1) & 1))) {
                         tc_fence_after_sync();
                         const uint32_t kb = sbase + C::kOffK + st * C::kTileBytes;
                         const uint32_t qbase = sbase + C::kOffQ + qb * C::kQBytes;
+                        // part c (paired layout: the box of even / odd positions) -> S columns [bi][c];
+                        // base descriptors once, then constant offsets (K step = 32 bytes in a box)
+                        const uint64_t kd0 = sdesc_sw128(kb, 16, 1024), qd0 = sdesc_sw128(qbase, 16, 1024);
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            umma_bf16(tmem + bi * N,
-                                      sdesc_sw128(kb + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024),
-                                      sdesc_sw128(qbase + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024), idS,
-                                      kk != 0);
+                        for (int c = 0; c < NP; ++c)
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk)
+                                umma_bf16(tmem + (bi * NP + c) * N,
+                                          sdesc_add(kd0, (kPair ? c : (kk >> 2)) * kBoxBytes + (kk & 3) * 32),
+                                          sdesc_add(qd0, (kk >> 2) * (N * 128) + (kk & 3) * 32), idS, kk != 0);
                         umma_commit(&sfull[bi]);
                         umma_commit(&kempty[st]);
                         if (last) {
@@ -431,28 +565,39 @@ __global__ void __launch_bounds__(192, 1)
                         }
                         if (s_i < 128) GQA_TRACE_AT(kTrSIssue + s_i, clock64());
                         cursor_next(cur, prefix, p.B, G);
+                        ++s_u;
                         ++s_i;
                         progress = true;
                     }
                 }
-                // ---- values of tile pv_i: needs its V, its P and a free O buffer
-                if (pv_i < s_i) {
-                    const int st = pv_i % S, bi = pv_i & 1;
-                    if (mbar_test_wait(&vfull[st], (pv_i / S) & 1) && mbar_test_wait(&pfull[bi], (pv_i >> 1) & 1) &&
-                        (pv_i < 2 || mbar_test_wait(&ofree[bi], ((pv_i >> 1) - 1) & 1))) {
+                // ---- values of tile pv_i: needs its V, its P (so its scores are done) and a free O buffer
+                if (do_pv && pv_i < pv_avail) {
+                    const int st = pv_i % SV, pbi = pv_i % PB, ob = pv_i % 3;
+                    const bool vready = mbar_test_wait(&vfull[st], (pv_i / SV) & 1);
+#ifdef GQA_TRACE
+                    if (vready && pv_i > v_seen) {
+                        if (pv_i < 128) GQA_TRACE_AT(kTrVReady + pv_i, clock64());
+                        v_seen = pv_i;
+                    }
+#endif
+                    if (vready && mbar_test_wait(&pfull[pbi], (pv_i / PB) & 1) &&
+                        (pv_i < 3 || mbar_test_wait(&ofree[ob], ((pv_i / 3) - 1) & 1))) {
                         tc_fence_after_sync();
                         const uint32_t vb = sbase + C::kOffV + st * C::kTileBytes;
-                        const uint32_t d_o = tmem + 2 * N + bi * N;
+                        const uint32_t d_o = tmem + C::kOCol + ob * C::kNPV;
+                        const uint64_t vd0 = sdesc_sw128(vb, kBoxBytes, 1024);
+                        const uint64_t pd0 = sdesc_sw128(sbase + C::kOffP + pbi * C::kPBufBytes, 16, 1024);
 #pragma unroll
-                        for (int part = 0; part < 2; ++part) {
-                            const uint32_t pb = sbase + C::kOffP + (bi * 2 + part) * C::kPBytes;
+                        for (int c = 0; c < NP; ++c)
 #pragma unroll
-                            for (int kk = 0; kk < kTile / 16; ++kk)
-                                umma_bf16(d_o, sdesc_sw128(vb + kk * 2048, kBoxBytes, 1024),
-                                          sdesc_sw128(pb + (kk >> 2) * (N * 128) + (kk & 3) * 32, 16, 1024), idPV,
-                                          (part | kk) != 0);
-                        }
-                        umma_commit(&ofull[bi]);
+                            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                                for (int kk = 0; kk < kTile / 16; ++kk)
+                                    umma_bf16(d_o, sdesc_add(vd0, c * kBoxBytes + kk * 2048),
+                                              sdesc_add(pd0, (c * 2 + part) * C::kPBytes + (kk >> 2) * (C::kNPV * 128) +
+                                                                 (kk & 3) * 32),
+                                              idPV, (c | part | kk) != 0);
+                        umma_commit(&ofull[ob]);
                         umma_commit(&vempty[st]);
                         if (pv_i < 128) GQA_TRACE_AT(kTrPvIssue + pv_i, clock64());
                         ++pv_i;
@@ -460,23 +605,15 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
                 if (progress) {
-                    idle = 0;
-                } else {
-                    if (idle == 0) idle_t0 = globaltimer_ns();
-                    if ((++idle & 63u) == 0) {
-                        if (*s_abort) break;
-                        if (globaltimer_ns() - idle_t0 > kWaitLimitNs) {
-                            *s_abort = 1;
-                            atomicOr(p.flags, 0x2u /* GQA_FLAG_WAIT_TIMEOUT */);
-                            break;
-                        }
-                    }
+                    poll.progressed();
+                } else if (!poll.step(ab)) {
+                    break;
                 }
             }
             umma_commit(done);
             mbar_wait_teardown(done, 0);
         }
-    } else {
+    } else if (warp < 6) {
         // ================================================================ softmax + epilogue
         const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
         const int r = q4 * 32 + lane;            // tile position (S) / head dim (O, d = 128)
@@ -488,34 +625,42 @@ __global__ void __launch_bounds__(192, 1)
         zero_empty_sequences<D>(p, prefix, P, tg, 128);
         GroupSync gsync{grp, 0};
         float l_part[NH], acc[NH];
-        Cursor cur = (ntiles > 0) ? cursor_at(u0, prefix, p.B, G) : Cursor{0, 0, 0, 1};
-        int seq_b = 0;
-        long long piece_u0 = u0;
-        int piece_i0 = 0, npe = 0;
+        int seq_b = 0, piece_i0 = 0, npe = 0, i = 0, rr = 0;
+        long long piece_u0 = 0;
         bool ok = true;
 
-        // fold O of tile i into acc with that tile's rescale factor
-        auto fold_o = [&](int i) -> bool {
-            const int bi = i & 1;
-            if (!mbar_wait(&ofull[bi], (i >> 1) & 1, ab)) return false;
+        // fold O of tile t into acc with that tile's rescale factor
+        auto fold_o = [&](int t) -> bool {
+            const int ob = t % 3;
+            if (!mbar_wait(&ofull[ob], (t / 3) & 1, ab)) return false;
             tc_fence_after_sync();
             uint32_t o[NH];
-            tmem_ld_32x32b<NH>(tmem + lane_off + 2 * N + bi * N, o);
+            tmem_ld_32x32b<NH>(tmem + lane_off + C::kOCol + ob * C::kNPV, o);
             tmem_wait_ld();
             tc_fence_before_sync();
-            mbar_arrive(&ofree[bi]);
+            mbar_arrive(&ofree[ob]);
             float al[NH];
-            load_vec<NH>(alpha_s + (i % 3) * NH, al);
+            load_vec<NH>(alpha_s + (t % 4) * NH, al);
 #pragma unroll
             for (int h = 0; h < NH; ++h) acc[h] = fmaf(acc[h], al[h], __uint_as_float(o[h]));
             return true;
         };
 
-        for (int i = 0; i < ntiles && ok; ++i) {
-            const long long u = u0 + i;
-            const bool first = (i == 0) || (cur.j == 0);
-            const bool last = (i + 1 == ntiles) || (cur.j + 1 == cur.tiles);
-            const int st = i % S, bi = i & 1;
+        while (ok) {
+          // ---- the next work range from the producer
+          const int rslot = rr % kRing;
+          if (!mbar_wait(&rfull[rslot], (rr / kRing) & 1, ab)) { ok = false; break; }
+          const RangeEntry range = ring[rslot];
+          mbar_arrive(&rempty[rslot]);
+          ++rr;
+          if (range.chunk == -2) break;
+          Cursor cur = cursor_at(range.ub, prefix, p.B, G);
+          int range_piece = 0;   // pieces of this range finished so far (a chunk's slot index)
+          for (int k = 0; k < range.len && ok; ++k, ++i) {
+            const long long u = range.ub + k;
+            const bool first = (k == 0) || (cur.j == 0);
+            const bool last = (k + 1 == range.len) || (cur.j + 1 == cur.tiles);
+            const int bi = i & 1;
             if (first) {
                 piece_u0 = u;
                 piece_i0 = i;
@@ -526,29 +671,36 @@ __global__ void __launch_bounds__(192, 1)
                     acc[h] = 0.f;
                 }
             }
-            // ---- scores of this tile: S^T row r (heads 0..NH-1)
+            // ---- scores of this tile: S^T row r of every part (heads 0..NH-1); part c of row r
+            // is position r, or 2r + c in the paired layout
             if (!mbar_wait(&sfull[bi], (i >> 1) & 1, ab)) { ok = false; break; }
             if (tg == 0 && i < 128) GQA_TRACE_AT(kTrSFull + i, clock64());
             tc_fence_after_sync();
-            uint32_t sraw[NH];
-            tmem_ld_32x32b<NH>(tmem + lane_off + bi * N, sraw);
+            uint32_t sraw[NP][NH];
+#pragma unroll
+            for (int c = 0; c < NP; ++c) tmem_ld_32x32b<NH>(tmem + lane_off + (bi * NP + c) * N, sraw[c]);
             tmem_wait_ld();
             tc_fence_before_sync();
             mbar_arrive(&sfree[bi]);
-            const int valid_cnt = seq_b - cur.j * kTile;          // >= 1
-            const bool valid = r < valid_cnt;
-            float x[NH], red_v[NH];
+            const int valid_cnt = seq_b - (cur.j << C::kTileShift);   // >= 1
+            bool valid[NP];
+            float x[NP][NH], red_v[NH];
 #pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                x[h] = valid ? __uint_as_float(sraw[h]) * p.scale_log2 : -INFINITY;
-                red_v[h] = x[h];
+            for (int h = 0; h < NH; ++h) red_v[h] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < NP; ++c) {
+                valid[c] = (kPair ? 2 * r + c : r) < valid_cnt;
+#pragma unroll
+                for (int h = 0; h < NH; ++h) {
+                    x[c][h] = valid[c] ? __uint_as_float(sraw[c][h]) * p.scale_log2 : -INFINITY;
+                    red_v[h] = fmaxf(red_v[h], x[c][h]);
+                }
             }
             butterfly_reduce<NH, true>(red_v, lane);
             butterfly_store<NH, C::kHalve>(red_v, lane, red + (bi * 4 + q4) * NH);
             __syncwarp();
             if (lane == 0) mbar_arrive(&redbar[bi]);
             if (!mbar_wait(&redbar[bi], (i >> 1) & 1, ab)) { ok = false; break; }
-            if (tg == 0 && i < 128) GQA_TRACE_AT(kTrMax + i, clock64());
             float m_new[NH], alpha[NH];
             reduce4<NH, true>(red + bi * 4 * NH, m_new);        // tile maximum per head
             if (i == piece_i0) {
@@ -565,48 +717,59 @@ __global__ void __launch_bounds__(192, 1)
             }
 #pragma unroll
             for (int h = 0; h < NH; ++h) {
-                x[h] = ex2(x[h] - m_new[h]);                     // 0 at invalid positions
-                l_part[h] = fmaf(l_part[h], alpha[h], x[h]);
+                float sx = 0.f;
+#pragma unroll
+                for (int c = 0; c < NP; ++c) {
+                    x[c][h] = ex2(x[c][h] - m_new[h]);           // 0 at invalid positions
+                    sx += x[c][h];
+                }
+                l_part[h] = fmaf(l_part[h], alpha[h], sx);
             }
             if (tg == 0) {
                 store_vec<NH>(mrun_s + (i % 3) * NH, m_new);
-                store_vec<NH>(alpha_s + (i % 3) * NH, alpha);
+                store_vec<NH>(alpha_s + (i % 4) * NH, alpha);
             }
             // ---- the last tile of a sequence: clear V rows past the end (they may hold NaN)
-            if (valid_cnt < kTile) {
-                if (!mbar_wait(&vfull[st], (i / S) & 1, ab)) { ok = false; break; }
-                if (!valid) {
-                    uint8_t *vrow = smem + C::kOffV + st * C::kTileBytes + r * 128;
+            if (valid_cnt < C::kTilePos) {
+                const int sv = i % SV;
+                if (!mbar_wait(&vfull[sv], (i / SV) & 1, ab)) { ok = false; break; }
+                uint8_t *vrow = smem + C::kOffV + sv * C::kTileBytes + r * 128;
 #pragma unroll
-                    for (int c = 0; c < C::kBoxes; ++c) {
+                for (int c = 0; c < C::kColBoxes; ++c) {
+                    // paired layout: box c holds the positions of part c; otherwise a row's
+                    // boxes hold the dims of one position (part 0)
+                    if (!valid[kPair ? c : 0]) {
                         uint4 *w = reinterpret_cast<uint4 *>(vrow + c * kBoxBytes);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) w[k] = make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
             }
-            // ---- probabilities to shared memory as bf16 hi + lo (K-major, 128-byte swizzle)
-            {
-                uint8_t *phi = smem + C::kOffP + (bi * 2 + 0) * C::kPBytes + (r >> 6) * (N * 128);
+            // ---- probabilities to shared memory as bf16 hi + lo (K-major, 128-byte swizzle);
+            // P buffer i % PB last held P(i - PB): its value GEMM must be done with it
+            const int pbi = i % PB;
+            if (i >= PB && !mbar_wait(&ofull[(i - PB) % 3], ((i - PB) / 3) & 1, ab)) { ok = false; break; }
+#pragma unroll
+            for (int c = 0; c < NP; ++c) {
+                uint8_t *phi = smem + C::kOffP + pbi * C::kPBufBytes + (c * 2) * C::kPBytes + (r >> 6) * (C::kNPV * 128);
                 uint8_t *plo = phi + C::kPBytes;
-                const int c = r & 63;
+                const int col = r & 63;
 #pragma unroll
                 for (int h = 0; h < NH; ++h) {
                     if (h < n) {
-                        const int off = h * 128 + ((((c >> 3) ^ (h & 7))) << 4) + (c & 7) * 2;
-                        const __nv_bfloat16 hi = __float2bfloat16_rn(x[h]);
-                        const __nv_bfloat16 lo = __float2bfloat16_rn(x[h] - __bfloat162float(hi));
+                        const int off = h * 128 + ((((col >> 3) ^ (h & 7))) << 4) + (col & 7) * 2;
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(x[c][h]);
+                        const __nv_bfloat16 lo = __float2bfloat16_rn(x[c][h] - __bfloat162float(hi));
                         *reinterpret_cast<__nv_bfloat16 *>(phi + off) = hi;
                         *reinterpret_cast<__nv_bfloat16 *>(plo + off) = lo;
                     }
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(&pfull[bi]);
+            mbar_arrive(&pfull[pbi]);
             if (tg == 0 && i < 128) GQA_TRACE_AT(kTrPFull + i, clock64());
-            // ---- fold the previous tile's O (its GEMM ran while this tile's softmax did)
-            if (i > piece_i0 && !fold_o(i - 1)) { ok = false; break; }
-            if (tg == 0 && i < 128) GQA_TRACE_AT(kTrFold + i, clock64());
+            // ---- fold O of the tile before the previous one (its GEMM ran during two softmax steps)
+            if (i - 2 >= piece_i0 && !fold_o(i - 2)) { ok = false; break; }
 
             if (last) {
                 if (tg == 0) GQA_TRACE_AT(kTrPieceEnd + 2 * npe, clock64());
@@ -614,6 +777,7 @@ __global__ void __launch_bounds__(192, 1)
                 butterfly_reduce<NH, false>(l_part, lane);
                 butterfly_store<NH, C::kHalve>(l_part, lane, lred + q4 * NH);
                 if (!gsync(ab)) { ok = false; break; }        // also publishes tile i's alpha
+                if (i - 1 >= piece_i0 && !fold_o(i - 1)) { ok = false; break; }
                 if (!fold_o(i)) { ok = false; break; }
                 float L[NH];
                 reduce4<NH, false>(lred, L);
@@ -626,7 +790,8 @@ __global__ void __launch_bounds__(192, 1)
                     for (int h = 0; h < NH; ++h)
                         if (h < n && has_dim) orow[h * D + odim] = acc[h] / L[h];
                 } else {
-                    float *sp = slot_ptr(p, blockIdx.x + seg, D);
+                    const int slot = range.chunk < 0 ? (int)blockIdx.x + seg : chunk_slot(p, range.chunk, range_piece);
+                    float *sp = slot_ptr(p, slot, D);
                     const int aoff = slot_acc_offset(n);
 #pragma unroll
                     for (int h = 0; h < NH; ++h)
@@ -647,9 +812,12 @@ __global__ void __launch_bounds__(192, 1)
                 // thread reaches only after its reads here.
                 if (tg == 0) GQA_TRACE_AT(kTrPieceEnd + 2 * npe + 1, clock64());
                 ++npe;
+                ++range_piece;
             }
             cursor_next(cur, prefix, p.B, G);
+          }
         }
+        if (tg == 0) GQA_TRACE_AT(kTrTiles, i);
     }
 
     tc_fence_before_sync();
@@ -660,10 +828,10 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (warp == 0 && lane == 0 && *s_abort) {
         // let copies in flight land before the CTA's shared memory is released
-        for (int k = kissued > S ? kissued - S : 0; k < kissued; ++k)
-            mbar_wait_teardown(&kfull[k % S], (k / S) & 1);
-        for (int k = vissued > S ? vissued - S : 0; k < vissued; ++k)
-            mbar_wait_teardown(&vfull[k % S], (k / S) & 1);
+        for (int k = kissued > SK ? kissued - SK : 0; k < kissued; ++k)
+            mbar_wait_teardown(&kfull[k % SK], (k / SK) & 1);
+        for (int k = vissued > SV ? vissued - SV : 0; k < vissued; ++k)
+            mbar_wait_teardown(&vfull[k % SV], (k / SV) & 1);
         for (int k = qissued > QB ? qissued - QB : 0; k < qissued; ++k)
             mbar_wait_teardown(&qfull[k % QB], (k / QB) & 1);
     }
@@ -674,11 +842,11 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-template <int D, int N, int NH>
+template <int D, bool kPair, int N, int NH>
 cudaError_t launch_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const DecodeParams &p,
                         int ctas, cudaStream_t stream) {
-    using C = TcCfg<D, N, NH>;
-    auto kern = gqa_decode_tc_kernel<D, N, NH>;
+    using C = TcCfg<D, kPair, N, NH>;
+    auto kern = gqa_decode_tc_kernel<D, kPair, N, NH>;
     static unsigned long long attr_set = 0;   // one bit per device; setting twice is harmless
     int dev = 0;
     cudaGetDevice(&dev);
@@ -691,17 +859,20 @@ cudaError_t launch_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUte
     return launch_pdl(kern, ctas, C::kThreads, C::kSmemBytes, stream, tk, tv, tq, p);
 }
 
-template <int D>
+template <int D, bool kPair>
 cudaError_t launch_tc_d(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const DecodeParams &p,
                         int ctas, cudaStream_t stream) {
     const int n = p.n;
-    if (n <= 1) return launch_tc_t<D, 16, 1>(tk, tv, tq, p, ctas, stream);
-    if (n <= 2) return launch_tc_t<D, 16, 2>(tk, tv, tq, p, ctas, stream);
-    if (n <= 4) return launch_tc_t<D, 16, 4>(tk, tv, tq, p, ctas, stream);
-    if (n <= 8) return launch_tc_t<D, 16, 8>(tk, tv, tq, p, ctas, stream);
-    if (n <= 16) return launch_tc_t<D, 16, 16>(tk, tv, tq, p, ctas, stream);
-    if (n <= 32) return launch_tc_t<D, 32, 32>(tk, tv, tq, p, ctas, stream);
-    return launch_tc_t<D, 64, 64>(tk, tv, tq, p, ctas, stream);
+    if (n <= 1) return launch_tc_t<D, kPair, 16, 1>(tk, tv, tq, p, ctas, stream);
+    if (n <= 2) return launch_tc_t<D, kPair, 16, 2>(tk, tv, tq, p, ctas, stream);
+    if (n <= 4) return launch_tc_t<D, kPair, 16, 4>(tk, tv, tq, p, ctas, stream);
+    if (n <= 8) return launch_tc_t<D, kPair, 16, 8>(tk, tv, tq, p, ctas, stream);
+    if (n <= 16) return launch_tc_t<D, kPair, 16, 16>(tk, tv, tq, p, ctas, stream);
+    if constexpr (!kPair) {
+        if (n <= 32) return launch_tc_t<D, kPair, 32, 32>(tk, tv, tq, p, ctas, stream);
+        return launch_tc_t<D, kPair, 64, 64>(tk, tv, tq, p, ctas, stream);
+    }
+    return cudaErrorNotSupported;
 }
 
 }  // namespace
@@ -710,10 +881,13 @@ int tc_max_heads() { return 64; }
 
 int tc_rows_for(int n) { return n <= 16 ? 16 : (n <= 32 ? 32 : 64); }
 
+bool tc_paired(int D, int Lmax, int n) { return D == 64 && Lmax % 2 == 0 && n <= 16; }
+
 cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
-                             const DecodeParams &p, int D, int ctas, cudaStream_t stream) {
-    if (D == 128) return launch_tc_d<128>(tk, tv, tq, p, ctas, stream);
-    return launch_tc_d<64>(tk, tv, tq, p, ctas, stream);
+                             const DecodeParams &p, int D, bool paired, int ctas, cudaStream_t stream) {
+    if (D == 128) return launch_tc_d<128, false>(tk, tv, tq, p, ctas, stream);
+    if (paired) return launch_tc_d<64, true>(tk, tv, tq, p, ctas, stream);
+    return launch_tc_d<64, false>(tk, tv, tq, p, ctas, stream);
 }
 
 }  // namespace gqa

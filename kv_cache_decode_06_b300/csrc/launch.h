@@ -35,8 +35,11 @@ cudaError_t launch_decode_simt(const CUtensorMap &tk, const CUtensorMap &tv, con
 
 int tc_max_heads();
 int tc_rows_for(int n);   // rows of the q tensor-map box (n rounded up to 16, 32 or 64)
+// Whether the tensor-core kernel reads this shape's cache in the paired layout
+// (D = 64: rows of two positions, 256-position tiles, tile_shift 8).
+bool tc_paired(int D, int Lmax, int n);
 cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
-                             const DecodeParams &p, int D, int ctas, cudaStream_t stream);
+                             const DecodeParams &p, int D, bool paired, int ctas, cudaStream_t stream);
 
 // Leading bytes of a decode workspace that must be zero before its first call:
 // the flag word.

@@ -92,6 +92,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     }
 }
 
+// Idle bookkeeping of an event loop that polls several barriers without
+// blocking.  After a few empty polls it sleeps briefly, so the polling warp
+// leaves its sub-partition's issue slots to the compute warps sharing it.
+// step() returns false when the loop must stop: the CTA is aborting, or nothing
+// progressed for kWaitLimitNs (which starts the abort).
+struct IdlePoll {
+    uint32_t idle = 0;
+    uint64_t t0 = 0;
+    __device__ __forceinline__ void progressed() { idle = 0; }
+    __device__ __forceinline__ bool step(const AbortState &ab) {
+        if (idle == 0) t0 = globaltimer_ns();
+        ++idle;
+        if (idle > 4) __nanosleep(64);
+        if ((idle & 63u) == 0) {
+            if (*ab.cta_abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *ab.cta_abort = 1;
+                atomicOr(ab.flags, 0x2u /* GQA_FLAG_WAIT_TIMEOUT */);
+                return false;
+            }
+        }
+        return true;
+    }
+};
+
 // Teardown wait: bounded by time only (used while aborting, to let copies
 // already in flight land before the CTA's shared memory is released).
 __device__ __forceinline__ bool mbar_wait_teardown(uint64_t *bar, uint32_t parity) {

@@ -49,6 +49,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// The descriptor of the same matrix `byte_off` bytes further on (byte_off a
+// multiple of 16): only the start-address field (address >> 4, low 14 bits)
+// changes, and shared-memory addresses stay below 256 KB, so it cannot carry.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_off) { return desc + (byte_off >> 4); }
+
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator.
 //   bits 4-5 D format (1 = f32), bits 7-9 A format (1 = bf16), bits 10-12 B format,
 //   bit 15 A MN-major, bit 16 B MN-major, bits 17-22 N >> 3, bits 24-28 M >> 4.

@@ -70,6 +70,8 @@ SMALL = [
     (2, 8, 1, 128, 384, [384, 200]),
     (3, 6, 2, 128, 131, [130, 131, 2]),
     (2, 64, 8, 128, 1024, [1024, 777]),
+    (2, 8, 2, 64, 257, [257, 100]),        # d = 64, odd Lmax: unpaired layout
+    (3, 32, 4, 64, 1030, [1030, 513, 2]),  # d = 64, even Lmax: paired layout, odd lengths
 ]
 
 
@@ -100,6 +102,23 @@ def test_split_invariance(path):
         outs.append(got)
     spread = max(np.abs(o - outs[0]).max() for o in outs)
     assert spread <= 1e-5
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_dynamic_pool_with_empty_and_short_sequences(d):
+    """Small grids (>= 64 tiles per CTA) put a quarter of the tiles in the claimed pool:
+    chunks that cut short, empty-neighboured and whole segments must still merge to the
+    oracle's answer.  An odd Lmax keeps d=64 off the paired form, which splits statically."""
+    Lmax = 9000 if d == 128 else 9001
+    cfg = DecodeConfig("pool", 57, B=8, H=8, G=2, d=d, Lmax=Lmax)
+    inp = make_decode_inputs(cfg, seq_lens=[0, Lmax, 5, 0, 8192, 129, 3000, 0])
+    ref = oracle_out(inp)
+    outs = []
+    for ctas in (1, 2, 3, 5):
+        got = run(inp, path=gqa.PATH_TCGEN05, num_ctas=ctas)
+        check_close(got, ref, what=f"pool d={d} ctas={ctas}")
+        outs.append(got)
+    assert max(np.abs(o - outs[0]).max() for o in outs) <= 1e-5
 
 
 def test_repeated_calls_reuse_workspace():
