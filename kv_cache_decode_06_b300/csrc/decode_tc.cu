@@ -103,9 +103,20 @@ struct RangeEntry {
 // D = head dim, N = MMA N (>= 16), NH = heads held per thread (power of two >= n).
 // kPair (D = 64 only): the cache is read as rows of two positions (256 bytes), a
 // tile is 128 such rows = 256 positions in two column boxes (even positions,
-// odd positions), and scores and values run as two GEMMs per tile, one per box.
-// A tile then moves as many bytes as a D = 128 tile, so the per-tile work of
-// the softmax group is spread over twice the positions.
+// odd positions), and scores run as two GEMMs per tile, one per box.  A tile
+// then moves as many bytes as a D = 128 tile, so the per-tile work of the
+// softmax group is spread over twice the positions.
+//
+// The value GEMM is one M x kOW x 128 product per tile, whatever the layout.
+// Its B operand stacks the probability rows [part][hi, lo][kNPV heads]; its A
+// operand is V^T, with M = 128 rows (the two 64-dim boxes at D = 128; at
+// kPair, box 0 = dims of the even positions, box 1 = dims of the odd ones) or
+// M = 64 (D = 64, one box).  Row m of the result, column block (c, hi/lo),
+// is wanted where part c matches the box of row m (always, without kPair);
+// the other blocks are never read.  hi and lo land in separate columns and are
+// added when O is folded; at kPair, rows m and m + 64 (even and odd positions
+// of dim m) are added at the end of a piece.  One tcgen05.mma then covers
+// 16 positions of every head, part and hi/lo half: 8 instructions per tile.
 template <int D, bool kPair, int N, int NH>
 struct TcCfg {
     static_assert(!kPair || D == 64, "the paired layout is for D = 64");
@@ -116,11 +127,11 @@ struct TcCfg {
     static constexpr int kTilePos = 1 << kTileShift;
     static constexpr int kTileBytes = kColBoxes * kBoxBytes;         // one K or V tile
     static constexpr int kQBytes = kQBoxes * N * 128;                // one Q buffer (N rows x d)
-    // N of the value GEMM: with M = 64 (D = 64) N may be 8, which halves the P
-    // buffers when a group has at most 8 heads
-    static constexpr int kNPV = (D == 64 && NH <= 8) ? 8 : N;
-    static constexpr int kPBytes = 2 * kNPV * 128;                   // one P part: kNPV rows x 128 positions
-    static constexpr int kPBufBytes = 2 * kParts * kPBytes;          // one P buffer: [part][hi, lo]
+    // rows of one (part, hi/lo) block of the value GEMM's B operand: the heads,
+    // padded to 8 (the value GEMM's N = kOW stays a multiple of 16)
+    static constexpr int kNPV = NH <= 8 ? 8 : N;
+    static constexpr int kOW = 2 * kParts * kNPV;                    // value GEMM N: [part][hi, lo][kNPV]
+    static constexpr int kPBufBytes = 2 * kOW * 128;                 // one P buffer: [64-position half][kOW rows]
     // small shared state, in floats
     static constexpr int kRedF = 2 * 4 * NH;                     // [2][4 warps][NH] tile maxima
     static constexpr int kLredF = 4 * NH;                        // [4 warps][NH] l sums
@@ -168,11 +179,13 @@ struct TcCfg {
     static_assert(NH < 4 || (kOffRed % 16 == 0 && kOffLred % 16 == 0 && kOffM % 16 == 0 && kOffA % 16 == 0),
                   "float4 alignment");
     static constexpr int kThreads = 224;
-    // TMEM: S accumulators [2][part][N] then O accumulators [3][kNPV] (O is folded two tiles behind)
+    // TMEM: S accumulators [2][part][N] then O accumulators [3][kOW] (O is folded two tiles behind)
     static constexpr int kOCol = 2 * kParts * N;
-    static constexpr int kTmemCols = pow2_cols(kOCol + 3 * kNPV);
-    static_assert(kOCol + 3 * kNPV <= 512, "TMEM columns");
-    static constexpr int kPvM = D;
+    static constexpr int kTmemCols = pow2_cols(kOCol + 3 * kOW);
+    static_assert(kOCol + 3 * kOW <= 512, "TMEM columns");
+    static constexpr int kPvM = kPair ? 128 : D;
+    static_assert(kOW % 16 == 0 && kOW <= 256, "value GEMM N");
+    static_assert(!kPair || NH * 64 * 4 <= kPBufBytes, "piece-end exchange fits a P buffer");
     // butterfly: number of head-halving steps (the rest are plain reductions)
     static constexpr int kHalve = ilog2(NH) < 5 ? ilog2(NH) : 5;
 };
@@ -499,7 +512,7 @@ __global__ void __launch_bounds__(224, 1)
         const bool do_s = warp == 1, do_pv = warp == 6;
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(128, N, false, false);
-            constexpr uint32_t idPV = idesc_bf16_f32(C::kPvM, C::kNPV, true, false);
+            constexpr uint32_t idPV = idesc_bf16_f32(C::kPvM, C::kOW, true, false);
             const uint32_t sbase = smem_addr(smem);
             Cursor cur{0, 0, 0, 1};
             long long s_u = 0, s_end = 0, s_ub = 0;
@@ -584,19 +597,14 @@ __global__ void __launch_bounds__(224, 1)
                         (pv_i < 3 || mbar_test_wait(&ofree[ob], ((pv_i / 3) - 1) & 1))) {
                         tc_fence_after_sync();
                         const uint32_t vb = sbase + C::kOffV + st * C::kTileBytes;
-                        const uint32_t d_o = tmem + C::kOCol + ob * C::kNPV;
+                        const uint32_t d_o = tmem + C::kOCol + ob * C::kOW;
+                        // A = V^T, MN-major: the column boxes are the M atoms (LBO), 16 positions = 2 KB
                         const uint64_t vd0 = sdesc_sw128(vb, kBoxBytes, 1024);
                         const uint64_t pd0 = sdesc_sw128(sbase + C::kOffP + pbi * C::kPBufBytes, 16, 1024);
 #pragma unroll
-                        for (int c = 0; c < NP; ++c)
-#pragma unroll
-                            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                                for (int kk = 0; kk < kTile / 16; ++kk)
-                                    umma_bf16(d_o, sdesc_add(vd0, c * kBoxBytes + kk * 2048),
-                                              sdesc_add(pd0, (c * 2 + part) * C::kPBytes + (kk >> 2) * (C::kNPV * 128) +
-                                                                 (kk & 3) * 32),
-                                              idPV, (c | part | kk) != 0);
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            umma_bf16(d_o, sdesc_add(vd0, kk * 2048),
+                                      sdesc_add(pd0, (kk >> 2) * (C::kOW * 128) + (kk & 3) * 32), idPV, kk != 0);
                         umma_commit(&ofull[ob]);
                         umma_commit(&vempty[st]);
                         if (pv_i < 128) GQA_TRACE_AT(kTrPvIssue + pv_i, clock64());
@@ -619,9 +627,12 @@ __global__ void __launch_bounds__(224, 1)
         const int r = q4 * 32 + lane;            // tile position (S) / head dim (O, d = 128)
         const int tg = tid - 64;                 // 0..127 within the group
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        // dim held in the O accumulator by this thread (M = 64 puts 16 rows in each quadrant)
-        const int odim = (D == 128) ? r : q4 * 16 + lane;
-        const bool has_dim = (D == 128) || lane < 16;
+        // dim held in the O accumulator by this thread (M = 64 puts 16 rows in each
+        // quadrant; at kPair rows r and r + 64 hold the even and odd positions' share
+        // of dim r, and the threads r < 64 hold the sum after a piece ends)
+        const int odim = kPair ? (r & 63) : (D == 128) ? r : q4 * 16 + lane;
+        const bool has_dim = kPair ? (r < 64) : (D == 128) || lane < 16;
+        const uint32_t o_part = (kPair && r >= 64) ? 2 * C::kNPV : 0;   // this row's (part) column block
         zero_empty_sequences<D>(p, prefix, P, tg, 128);
         GroupSync gsync{grp, 0};
         float l_part[NH], acc[NH];
@@ -634,15 +645,23 @@ __global__ void __launch_bounds__(224, 1)
             const int ob = t % 3;
             if (!mbar_wait(&ofull[ob], (t / 3) & 1, ab)) return false;
             tc_fence_after_sync();
-            uint32_t o[NH];
-            tmem_ld_32x32b<NH>(tmem + lane_off + C::kOCol + ob * C::kNPV, o);
-            tmem_wait_ld();
-            tc_fence_before_sync();
-            mbar_arrive(&ofree[ob]);
             float al[NH];
             load_vec<NH>(alpha_s + (t % 4) * NH, al);
+            // hi and lo columns, at most 16 heads at a time (bounds the registers at NH = 64)
+            constexpr int CH = NH < 16 ? NH : 16;
+            const uint32_t oc = tmem + lane_off + C::kOCol + ob * C::kOW + o_part;
 #pragma unroll
-            for (int h = 0; h < NH; ++h) acc[h] = fmaf(acc[h], al[h], __uint_as_float(o[h]));
+            for (int h0 = 0; h0 < NH; h0 += CH) {
+                uint32_t ohi[CH], olo[CH];
+                tmem_ld_32x32b<CH>(oc + h0, ohi);
+                tmem_ld_32x32b<CH>(oc + C::kNPV + h0, olo);
+                tmem_wait_ld();
+#pragma unroll
+                for (int h = 0; h < CH; ++h)
+                    acc[h0 + h] = fmaf(acc[h0 + h], al[h0 + h], __uint_as_float(ohi[h]) + __uint_as_float(olo[h]));
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&ofree[ob]);
             return true;
         };
 
@@ -745,14 +764,16 @@ __global__ void __launch_bounds__(224, 1)
                     }
                 }
             }
-            // ---- probabilities to shared memory as bf16 hi + lo (K-major, 128-byte swizzle);
+            // ---- probabilities to shared memory as bf16 hi + lo (K-major, 128-byte swizzle):
+            // row (c * 2 + hi/lo) * kNPV + h of the value GEMM's B operand, position r;
             // P buffer i % PB last held P(i - PB): its value GEMM must be done with it
             const int pbi = i % PB;
             if (i >= PB && !mbar_wait(&ofull[(i - PB) % 3], ((i - PB) / 3) & 1, ab)) { ok = false; break; }
 #pragma unroll
             for (int c = 0; c < NP; ++c) {
-                uint8_t *phi = smem + C::kOffP + pbi * C::kPBufBytes + (c * 2) * C::kPBytes + (r >> 6) * (C::kNPV * 128);
-                uint8_t *plo = phi + C::kPBytes;
+                uint8_t *phi = smem + C::kOffP + pbi * C::kPBufBytes + (r >> 6) * (C::kOW * 128) +
+                               (c * 2) * (C::kNPV * 128);
+                uint8_t *plo = phi + C::kNPV * 128;
                 const int col = r & 63;
 #pragma unroll
                 for (int h = 0; h < NH; ++h) {
@@ -779,6 +800,21 @@ __global__ void __launch_bounds__(224, 1)
                 if (!gsync(ab)) { ok = false; break; }        // also publishes tile i's alpha
                 if (i - 1 >= piece_i0 && !fold_o(i - 1)) { ok = false; break; }
                 if (!fold_o(i)) { ok = false; break; }
+                if constexpr (kPair) {
+                    // odd positions' share (rows 64..127) to the even rows, through the P
+                    // buffer of tile i + 1: its last value GEMM is done (ofull of tile i was
+                    // waited for) and the next P write follows the next tile's max barrier
+                    float *xch = reinterpret_cast<float *>(smem + C::kOffP + ((i + 1) % PB) * C::kPBufBytes);
+                    if (r >= 64) {
+#pragma unroll
+                        for (int h = 0; h < NH; ++h) xch[h * 64 + (r - 64)] = acc[h];
+                    }
+                    if (!gsync(ab)) { ok = false; break; }
+                    if (r < 64) {
+#pragma unroll
+                        for (int h = 0; h < NH; ++h) acc[h] += xch[h * 64 + r];
+                    }
+                }
                 float L[NH];
                 reduce4<NH, false>(lred, L);
                 const int seg = cur.b * G + cur.g;
