@@ -113,7 +113,7 @@ gqa_status gqa_decode_workspace_size(int B, int H, int G, int d, int Lmax, size_
  * B         1 .. GQA_MAX_BATCH
  * H, G      H >= G >= 1, H % G == 0, H/G <= 64
  * d         head dimension: 64 or 128
- * Lmax      >= 1, cache capacity per sequence
+ * Lmax      >= 1, cache capacity per sequence, at most 2^24; B*G*ceil(Lmax/128) <= 2^30
  * scale     score scale, normally 1/sqrt(d), used as given (fp32)
  *
  * Arithmetic: exact bf16 products accumulated in fp32, softmax in fp32 with a

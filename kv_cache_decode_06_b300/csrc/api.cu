@@ -19,6 +19,7 @@ static_assert(gqa::kMaxCtas == GQA_MAX_CTAS, "CTA limit mismatch");
 constexpr int kMaxHeadsPerGroup = 64;
 constexpr int kMaxHeads = 4096;
 constexpr long long kMaxLmax = 1ll << 24;
+constexpr long long kMaxTiles = 1ll << 30;   // B * G * ceil(Lmax / 128), far above any cache that fits
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -99,6 +100,8 @@ gqa_status check_shape(int B, int H, int G, int d, int Lmax) {
     if (d != 64 && d != 128) return GQA_ERR_UNSUPPORTED;
     if (B > GQA_MAX_BATCH || H > kMaxHeads || H / G > kMaxHeadsPerGroup || Lmax > kMaxLmax)
         return GQA_ERR_UNSUPPORTED;
+    // the kernels index 128-position tiles of all K/V heads with 32-bit arithmetic
+    if ((long long)B * G * ((Lmax + gqa::kTile - 1) / gqa::kTile) > kMaxTiles) return GQA_ERR_UNSUPPORTED;
     return GQA_OK;
 }
 

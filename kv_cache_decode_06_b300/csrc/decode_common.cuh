@@ -65,13 +65,25 @@ __device__ __forceinline__ int tiles_of(int seq, int shift) { return (seq + (1 <
 
 __device__ __forceinline__ int clamp_seq(int s, int Lmax) { return s < 0 ? 0 : (s > Lmax ? Lmax : s); }
 
+// Tile counts stay below 2^31 (kMaxBatch * heads * tiles per sequence), so the
+// split arithmetic below avoids 64-bit divisions, which are long instruction
+// sequences on the start-up path of every CTA.
+
+// First tile of CTA c's static range: floor(c * W / P), 0 <= c <= P <= kMaxCtas.
 __device__ __forceinline__ long long range_start(int c, long long W, int P) {
-    return (long long)c * W / P;
+    const unsigned w = (unsigned)W, q = w / (unsigned)P, rem = w % (unsigned)P;
+    return (long long)c * q + ((unsigned)c * rem) / (unsigned)P;   // c * rem < 2^20
 }
 
-// The CTA whose range holds tile t (0 <= t < W).
+// The CTA whose range holds tile t (0 <= t < W): floor(((t + 1) * P - 1) / W),
+// from a single-precision estimate corrected with exact products.
 __device__ __forceinline__ int cta_of_tile(long long t, long long W, int P) {
-    return (int)(((t + 1) * P - 1) / W);
+    const long long num = (t + 1) * P - 1;
+    int c = (int)((float)num / (float)W);
+    c = c < 0 ? 0 : (c > P - 1 ? P - 1 : c);
+    while ((long long)(c + 1) * W <= num) ++c;
+    while ((long long)c * W > num) --c;
+    return c;
 }
 
 // The split of the W tiles between the static ranges and the dynamic pool.
@@ -117,9 +129,9 @@ __device__ __forceinline__ Cursor cursor_at(long long u, const int *prefix, int 
     Cursor c;
     c.b = lo;
     c.tiles = prefix[lo + 1] - prefix[lo];
-    const long long r = u - (long long)G * prefix[lo];
-    c.g = (int)(r / c.tiles);
-    c.j = (int)(r % c.tiles);
+    const int r = (int)(u - (long long)G * prefix[lo]);   // < G * tiles < 2^31
+    c.g = r / c.tiles;
+    c.j = r - c.g * c.tiles;
     return c;
 }
 

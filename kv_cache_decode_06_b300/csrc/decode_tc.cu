@@ -74,6 +74,10 @@ enum TraceSlot {
     kTrGlobalEnd = 5,     // %globaltimer at exit (ns)
     kTrFirstQ = 6,        // first Q copy issued
     kTrFirstK = 7,        // first K copy issued
+    kTrProdIn = 8,        // producer thread starts its loop
+    kTrRing0 = 9,         // first range handed on
+    kTrPreQ = 10,         // first Q copy about to be issued
+    kTrDepDone = 11,      // the grids this one depends on have completed
     kTrKIssue = 16,       // + i: K copy of tile i issued
     kTrSIssue = 144,      // + i: score GEMM of tile i issued
     kTrPvIssue = 272,     // + i: value GEMM of tile i issued
@@ -365,6 +369,7 @@ __global__ void __launch_bounds__(224, 1)
     // Everything above is on-chip; inputs and outputs are touched only once the
     // grids this one depends on have completed.
     griddep_wait();
+    if (tid == 64) GQA_TRACE_AT(kTrDepDone, clock64());
     griddep_launch_dependents();
     build_prefix(p.seq_lens, p.B, p.Lmax, C::kTileShift, prefix, scratch, p.flags);   // ends with __syncthreads
     tc_fence_after_sync();
@@ -381,6 +386,7 @@ __global__ void __launch_bounds__(224, 1)
         // Hands every work range to the other roles through the ring: the static
         // range first, then one claimed chunk at a time, then an end marker.
         if (lane == 0) {
+            GQA_TRACE_AT(kTrProdIn, clock64());
             const uint64_t pol_kv = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
             RangeEntry next{0, 0, -1};
@@ -421,6 +427,7 @@ __global__ void __launch_bounds__(224, 1)
                         (v_r > pushed - kRing && mbar_test_wait(&rempty[slot], ((pushed / kRing) - 1) & 1))) {
                         ring[slot] = next;
                         mbar_arrive(&rfull[slot]);   // release: the entry is visible to the waiters
+                        if (pushed == 0) GQA_TRACE_AT(kTrRing0, clock64());
                         ++pushed;
                         have_next = false;
                         if (next.chunk == -2) {
@@ -445,6 +452,7 @@ __global__ void __launch_bounds__(224, 1)
                         (!first || piece < QB || mbar_test_wait(&qempty[qb], ((piece / QB) - 1) & 1)) &&
                         (i < SK || mbar_test_wait(&kempty[st], ((i / SK) - 1) & 1))) {
                         if (first) {
+                            if (i == 0) GQA_TRACE_AT(kTrPreQ, clock64());
                             mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
                             uint8_t *qdst = smem + C::kOffQ + qb * C::kQBytes;
                             const int y = kc.b * p.H + kc.g * n;

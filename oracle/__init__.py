@@ -53,6 +53,14 @@ def _bind(lib):
     lib.oracle_gqa_decode_f64.restype = ctypes.c_int
     lib.oracle_gqa_decode_f64.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.c_int, ctypes.c_float, P, ctypes.c_int64]
+    lib.oracle_gqa_decode_window_f64.restype = ctypes.c_int
+    lib.oracle_gqa_decode_window_f64.argtypes = [P, P, P, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, P,
+                                                 ctypes.c_int64]
+    lib.oracle_gather_pages.restype = ctypes.c_int
+    lib.oracle_gather_pages.argtypes = [P, P, P, P] + [ctypes.c_int] * 7
+    lib.oracle_append_row.restype = ctypes.c_int
+    lib.oracle_append_row.argtypes = [P, P, P] + [ctypes.c_int] * 4
     lib.oracle_meanpool_f32.restype = ctypes.c_int
     lib.oracle_meanpool_f32.argtypes = [P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int64]
     lib.oracle_meanpool_f64.restype = ctypes.c_int
@@ -68,10 +76,12 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def gqa_decode_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, seq_lens: np.ndarray,
-                   scale, rows: Optional[np.ndarray] = None, lib=None) -> np.ndarray:
+def gqa_decode_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, seq_lens: Optional[np.ndarray],
+                   scale, rows: Optional[np.ndarray] = None, window: int = 0, lib=None) -> np.ndarray:
     """Float64 GQA decode.  q [B,H,d], k/v [B,G,Lmax,d] as uint16 bf16 bits.
 
+    ``seq_lens=None``: every one of the Lmax positions is valid (cross-attention).
+    ``window > 0``: only the last ``window`` valid positions are attended.
     Returns out [B, H, d] float64.  With ``rows`` (flat ids b*H+i), only those
     rows are computed; the others are NaN.
     """
@@ -79,20 +89,58 @@ def gqa_decode_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, seq_lens: np.nda
     q = np.ascontiguousarray(q, dtype=np.uint16)
     k = np.ascontiguousarray(k, dtype=np.uint16)
     v = np.ascontiguousarray(v, dtype=np.uint16)
-    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     B, H, d = q.shape
     Bk, G, L, dk = k.shape
-    assert Bk == B and dk == d and v.shape == k.shape and sl.shape == (B,)
+    assert Bk == B and dk == d and v.shape == k.shape
+    if seq_lens is not None:
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        assert sl.shape == (B,)
+        slp = _ptr(sl)
+    else:
+        slp = None
     out = np.full((B, H, d), np.nan, dtype=np.float64)
     if rows is None:
-        rc = lib.oracle_gqa_decode_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(sl), _ptr(out),
-                                       B, H, G, d, L, float(np.float32(scale)), None, 0)
+        rp, nr = None, 0
     else:
         r = np.ascontiguousarray(rows, dtype=np.int64)
-        rc = lib.oracle_gqa_decode_f64(_ptr(q), _ptr(k), _ptr(v), _ptr(sl), _ptr(out),
-                                       B, H, G, d, L, float(np.float32(scale)), _ptr(r), r.size)
+        rp, nr = _ptr(r), r.size
+    rc = lib.oracle_gqa_decode_window_f64(_ptr(q), _ptr(k), _ptr(v), slp, int(window), _ptr(out),
+                                          B, H, G, d, L, float(np.float32(scale)), rp, nr)
     if rc != 0:
-        raise ValueError("oracle_gqa_decode_f64 rejected its arguments")
+        raise ValueError("oracle_gqa_decode_window_f64 rejected its arguments")
+    return out
+
+
+def gather_pages(pages: np.ndarray, table: np.ndarray, seq_lens: Optional[np.ndarray], Lmax: int,
+                 fill: int = 0x7FC0, lib=None) -> np.ndarray:
+    """Paged cache [num_pages, G, page_size, d] + block table [B, max_pages] -> [B, G, Lmax, d].
+
+    Rows past each sequence's length hold ``fill`` (default: bf16 NaN bits).
+    """
+    lib = lib or load()
+    pages = np.ascontiguousarray(pages, dtype=np.uint16)
+    table = np.ascontiguousarray(table, dtype=np.int32)
+    num_pages, G, page_size, d = pages.shape
+    B, max_pages = table.shape
+    out = np.full((B, G, Lmax, d), fill, dtype=np.uint16)
+    sl = None if seq_lens is None else np.ascontiguousarray(seq_lens, dtype=np.int32)
+    rc = lib.oracle_gather_pages(_ptr(pages), _ptr(table), None if sl is None else _ptr(sl), _ptr(out),
+                                 B, G, d, page_size, max_pages, num_pages, Lmax)
+    if rc != 0:
+        raise ValueError("oracle_gather_pages rejected its arguments")
+    return out
+
+
+def append_row(cache: np.ndarray, row: np.ndarray, seq_lens: np.ndarray, lib=None) -> np.ndarray:
+    """Copy of ``cache`` [B,G,Lmax,d] with ``row`` [B,G,d] written at position seq_lens[b] - 1."""
+    lib = lib or load()
+    out = np.array(cache, dtype=np.uint16, order="C", copy=True)
+    row = np.ascontiguousarray(row, dtype=np.uint16)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, G, L, d = out.shape
+    assert row.shape == (B, G, d) and sl.shape == (B,)
+    if lib.oracle_append_row(_ptr(out), _ptr(row), _ptr(sl), B, G, d, L) != 0:
+        raise ValueError("oracle_append_row rejected its arguments")
     return out
 
 

@@ -17,6 +17,11 @@ Sources of truth used here, none of them the oracle's own code:
     (shifting every key by the same vector, permuting cache positions);
   * brute force on tiny integer inputs with 50-digit arithmetic and no
     maximum subtraction;
+  * for the variants (cross-attention over all positions, sliding window,
+    paged cache, fused append): the library's attention with an explicit
+    position mask, a numpy scatter of the cache into pages that the gather
+    must invert, the newest-position closed form (window 1) and a numpy
+    assignment of the appended row;
   * for the mean-pool conversion (same page, "Converted and uptrained
     checkpoints" and the conversion pseudocode; arxiv:2305.13245 §2.1):
     identical heads, the identity at G = H, the column mean at G = 1, exact
@@ -264,6 +269,142 @@ def check_empty_sequence_gives_zero(lib):
     assert np.isfinite(got[1]).all() and np.abs(got[1]).max() > 0
 
 
+# ------------------------------------------------ variants of the decode step
+
+def _sdpa_masked(inp, allowed) -> np.ndarray:
+    """torch CPU attention (float64) with an explicit boolean mask allowed[b][t] over the Lmax positions."""
+    cfg = inp.cfg
+    q = torch.from_numpy(_f64(inp.q))
+    k = torch.from_numpy(np.nan_to_num(_f64(inp.k)))
+    v = torch.from_numpy(np.nan_to_num(_f64(inp.v)))
+    out = np.zeros((cfg.B, cfg.H, cfg.d))
+    for b in range(cfg.B):
+        m = torch.from_numpy(np.asarray(allowed[b], dtype=bool))
+        if not m.any():
+            continue
+        o = F.scaled_dot_product_attention(q[b][None, :, None, :], k[b][None], v[b][None],
+                                           attn_mask=m[None, None, None, :], scale=float(inp.scale),
+                                           enable_gqa=True)
+        out[b] = o[0, :, 0, :].numpy()
+    return out
+
+
+def check_cross_attention_matches_library(lib):
+    """seq_lens = NULL: every one of the Lmax positions is attended (an encoder cache of fixed length)."""
+    cfg = _small_cfg(G=2, L=29, seq=(29, 29))
+    inp = make_decode_inputs(cfg)
+    got = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, None, inp.scale, lib=lib)
+    ref = _sdpa_masked(inp, np.ones((cfg.B, cfg.Lmax), dtype=bool))
+    assert np.max(np.abs(got - ref)) <= 1e-12
+
+
+def check_window_matches_library_mask(lib):
+    """A window W attends to positions max(0, T - W) <= t < T: the library with that mask agrees."""
+    cfg = _small_cfg(G=4, L=41, B=4, seq=(1, 41))
+    inp = make_decode_inputs(cfg, seq_lens=[41, 17, 1, 30], poison_tail=True)
+    for W in (1, 2, 7, 16, 30, 41, 100):
+        got = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale, window=W, lib=lib)
+        allowed = np.zeros((cfg.B, cfg.Lmax), dtype=bool)
+        for b, T in enumerate(inp.seq_lens):
+            allowed[b, max(0, int(T) - W):int(T)] = True
+        ref = _sdpa_masked(inp, allowed)
+        assert np.max(np.abs(got - ref)) <= 1e-12, W
+    # positions before the window may hold anything: they are never read
+    k, v = inp.k.copy(), inp.v.copy()
+    for b, T in enumerate(inp.seq_lens):
+        k[b, :, :max(0, int(T) - 7)] = 0x7FC0   # bf16 NaN
+        v[b, :, :max(0, int(T) - 7)] = 0x7FC0
+    got = oracle.gqa_decode_f64(inp.q, k, v, inp.seq_lens, inp.scale, window=7, lib=lib)
+    ref = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale, window=7, lib=lib)
+    assert np.array_equal(got, ref)
+
+
+def check_window_of_one_returns_last_value(lib):
+    """W = 1: the only attended position is the newest, so out = v[T-1] bit for bit."""
+    cfg = _small_cfg(G=2)
+    inp = make_decode_inputs(cfg)
+    got = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale, window=1, lib=lib)
+    v = _f64(inp.v)
+    for b, T in enumerate(inp.seq_lens):
+        for i in range(cfg.H):
+            assert np.array_equal(got[b, i], v[b, i // cfg.n, int(T) - 1])
+
+
+def scatter_to_pages(caches, seq_lens, page_size, rng, extra_pages=3):
+    """Numpy: contiguous caches [B,G,L,d] (K and V) cut into pages at random places of a pool.
+
+    Returns one page pool per cache and the shared block table.  Unused pool
+    pages and table entries past a sequence's pages are garbage (NaN bits and
+    -1), which nothing may read.
+    """
+    B, G, L, d = caches[0].shape
+    max_pages = -(-L // page_size)
+    need = [-(-int(T) // page_size) for T in seq_lens]
+    num_pages = sum(need) + extra_pages
+    order = rng.permutation(num_pages)
+    pools = [np.full((num_pages, G, page_size, d), 0x7FC0, dtype=np.uint16) for _ in caches]
+    table = np.full((B, max_pages), -1, dtype=np.int32)
+    nxt = 0
+    for b in range(B):
+        for p in range(need[b]):
+            page = int(order[nxt])
+            nxt += 1
+            table[b, p] = page
+            for pool, cache in zip(pools, caches):
+                rows = cache[b, :, p * page_size:(p + 1) * page_size]
+                pool[page, :, :rows.shape[1]] = rows
+    return pools, table
+
+
+def check_gather_inverts_scatter(lib):
+    """Pages gathered through the block table give back the contiguous cache on every valid
+    position, whatever the page size and the order of the pages in the pool; the paged
+    decode (decode of the gathered cache) matches the library on the contiguous cache."""
+    rng = np.random.default_rng(21)
+    for page_size in (1, 4, 16, 64):
+        cfg = _small_cfg(G=2, L=70, B=3, seq=(1, 70))
+        inp = make_decode_inputs(cfg, seq_lens=[70, 33, 0], poison_tail=True)
+        (kp, vp), table = scatter_to_pages([inp.k, inp.v], inp.seq_lens, page_size, rng)
+        kg = oracle.gather_pages(kp, table, inp.seq_lens, cfg.Lmax, lib=lib)
+        vg = oracle.gather_pages(vp, table, inp.seq_lens, cfg.Lmax, lib=lib)
+        for b, T in enumerate(inp.seq_lens):
+            assert np.array_equal(kg[b, :, :T], inp.k[b, :, :T]), (page_size, b)
+            assert np.array_equal(vg[b, :, :T], inp.v[b, :, :T]), (page_size, b)
+        a = oracle.gqa_decode_f64(inp.q, kg, vg, inp.seq_lens, inp.scale, lib=lib)
+        ref = sdpa_reference(inp)
+        assert np.max(np.abs(a - ref)) <= 1e-12
+    bad = table.copy()
+    bad[0, 0] = kp.shape[0]
+    try:
+        oracle.gather_pages(kp, bad, inp.seq_lens, cfg.Lmax, lib=lib)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a table entry outside the pool was accepted")
+
+
+def check_append_writes_one_row(lib):
+    """The appended row lands at position T-1 of every K/V head of its sequence and nowhere
+    else; the decode that follows attends to it as the newest position."""
+    cfg = _small_cfg(G=2, L=23, B=4, seq=(1, 23))
+    inp = make_decode_inputs(cfg, seq_lens=[23, 1, 0, 9], poison_tail=False)
+    rng = np.random.default_rng(8)
+    new = f32_to_bf16_bits(rng.standard_normal((cfg.B, cfg.G, cfg.d)).astype(np.float32))
+    got = oracle.append_row(inp.k, new, inp.seq_lens, lib=lib)
+    expect = inp.k.copy()
+    for b, T in enumerate(inp.seq_lens):
+        if T > 0:
+            expect[b, :, T - 1] = new[b]
+    assert np.array_equal(got, expect)
+    # W = 1 after the append returns the appended value row exactly
+    vnew = oracle.append_row(inp.v, new, inp.seq_lens, lib=lib)
+    out = oracle.gqa_decode_f64(inp.q, got, vnew, inp.seq_lens, inp.scale, window=1, lib=lib)
+    for b, T in enumerate(inp.seq_lens):
+        for i in range(cfg.H):
+            ref = _f64(new[b, i // cfg.n]) if T > 0 else np.zeros(cfg.d)
+            assert np.array_equal(out[b, i], ref)
+
+
 # ---------------------------------------------------------------- mean-pool
 
 def check_meanpool_identical_heads(lib):
@@ -326,6 +467,10 @@ DECODE_CHECKS = [
     check_single_token_returns_v0, check_two_token_closed_form, check_key_shift_invariance,
     check_permutation_invariance, check_bruteforce_high_precision, check_tail_is_never_read,
     check_empty_sequence_gives_zero,
+]
+VARIANT_CHECKS = [
+    check_cross_attention_matches_library, check_window_matches_library_mask,
+    check_window_of_one_returns_last_value, check_gather_inverts_scatter, check_append_writes_one_row,
 ]
 MEANPOOL_CHECKS = [
     check_meanpool_identical_heads, check_meanpool_identity_and_mean,

@@ -68,6 +68,8 @@ def test_workspace_size_for_every_workload(gqa_lib):
     ((0, 8, 2, 64, 128), 1), ((1, 8, 3, 64, 128), 1), ((1, 8, 16, 64, 128), 1), ((1, 8, 2, 96, 128), 2),
     ((1, 8, 2, 64, 0), 1), ((2048, 8, 2, 64, 128), 2), ((1, 128, 1, 64, 128), 2), ((1, 8, 2, -64, 128), 1),
     ((1, 8, 2, 64, 1 << 25), 2),
+    # 1024 * 4096 K/V heads * 2^17 tiles: more 128-position tiles than the kernels index (2^30)
+    ((1024, 4096, 4096, 64, 1 << 24), 2), ((1024, 64, 64, 64, 1 << 24), 2),
 ])
 def test_workspace_size_rejects(shape, status, gqa_lib):
     assert _ws(*shape)[0] == status

@@ -12,7 +12,8 @@ from kv_cache_decode_06_b300.inputs import (
 )
 
 
-@pytest.mark.parametrize("check", pins.DECODE_CHECKS + pins.MEANPOOL_CHECKS, ids=lambda c: c.__name__)
+@pytest.mark.parametrize("check", pins.DECODE_CHECKS + pins.VARIANT_CHECKS + pins.MEANPOOL_CHECKS,
+                         ids=lambda c: c.__name__)
 def test_oracle_pin(check, oracle_lib):
     check(oracle_lib)
 
@@ -40,8 +41,16 @@ MUTANTS = {
     "scale_dropped": ("s[t] = sc * dot;", "s[t] = dot;"),
     "k_and_v_swapped": ("acc += s[t] * bf16_value(vg[(int64_t)t * d + j]);",
                         "acc += s[t] * bf16_value(kg[(int64_t)t * d + j]);"),
-    "one_past_the_end": ("const int T = seq_lens[b];",
-                         "const int T = seq_lens[b] < Lmax ? seq_lens[b] + 1 : seq_lens[b];"),
+    "one_past_the_end": ("*T = seq_lens ? seq_lens[b] : Lmax;",
+                         "*T = seq_lens ? (seq_lens[b] < Lmax ? seq_lens[b] + 1 : seq_lens[b]) : Lmax;"),
+    "cross_attention_drops_last": ("*T = seq_lens ? seq_lens[b] : Lmax;", "*T = seq_lens ? seq_lens[b] : Lmax - 1;"),
+    "window_one_too_wide": ("*t0 = (window > 0 && *T > window) ? *T - window : 0;",
+                            "*t0 = (window > 0 && *T > window + 1) ? *T - window - 1 : 0;"),
+    "window_ignored": ("*t0 = (window > 0 && *T > window) ? *T - window : 0;", "*t0 = 0;"),
+    "gather_page_offset_swapped": ("+ t % page_size) * d;", "+ (t / page_size) % page_size) * d;"),
+    "gather_wrong_table_row": ("table[(int64_t)b * max_pages + t / page_size]",
+                               "table[(int64_t)(B - 1 - b) * max_pages + t / page_size]"),
+    "append_one_row_early": ("* Lmax + (T - 1)) * d", "* Lmax + (T > 1 ? T - 2 : 0)) * d"),
     "normaliser_missing": ("o[j] = acc / l;", "o[j] = acc;"),
     "exp_of_unshifted_sum": ("l += s[t];", "l += s[t] * s[t];"),
     "meanpool_divides_by_H": ("out[(o * G + g) * inner + x] = acc / (float)n;",
@@ -66,7 +75,7 @@ def test_pins_catch_planted_mistake(name, mutant_dir):
     so = mutant_dir / f"lib{name}.so"
     subprocess.run(["gcc", *oracle.CFLAGS, "-o", str(so), str(mpath), "-lm"], check=True)
     lib = oracle.load(str(so))
-    checks = pins.MEANPOOL_CHECKS if name.startswith("meanpool") else pins.DECODE_CHECKS
+    checks = pins.MEANPOOL_CHECKS if name.startswith("meanpool") else pins.DECODE_CHECKS + pins.VARIANT_CHECKS
     failed = []
     for check in checks:
         try:
