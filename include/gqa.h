@@ -52,6 +52,8 @@ typedef enum gqa_status {
 /* Bits the decode kernel ORs into the workspace's flag word (see gqa_decode_read_flags). */
 #define GQA_FLAG_SEQ_LEN_CLAMPED 0x1u  /* some seq_lens[b] was < 0 or > Lmax; it was clamped */
 #define GQA_FLAG_WAIT_TIMEOUT    0x2u  /* a pipeline wait ran out; that call's output is invalid */
+#define GQA_FLAG_BAD_PAGE        0x4u  /* a block-table entry needed by gqa_decode_paged was not a page
+                                          of the pool; its rows were read as zeros */
 
 /* Kernel variants of gqa_decode_ex. */
 #define GQA_PATH_AUTO    0   /* pick per shape (the default of gqa_decode) */
@@ -107,6 +109,10 @@ gqa_status gqa_decode_workspace_size(int B, int H, int G, int d, int Lmax, size_
  * seq_lens  device, int32 [B]; expected 0 <= seq_lens[b] <= Lmax.  Values outside
  *           are clamped into that range on the device and GQA_FLAG_SEQ_LEN_CLAMPED
  *           is set in the workspace flag word.
+ *           NULL: every sequence has all Lmax positions valid.  This is decoder
+ *           cross-attention over a fixed-length encoder cache, where GQA applies
+ *           as it does to self-attention ["Grouped-query attention (GQA)"
+ *           concept page, "When to use which", last row; arxiv:2305.13245 §3.1].
  * out       device, float32 [B, H, d], contiguous.  Must not overlap any input.
  * workspace device, zero-filled before first use, >= gqa_decode_workspace_size bytes,
  *           256-byte aligned.  Used by one call at a time.
@@ -136,7 +142,14 @@ gqa_status gqa_decode(const void *q, const void *k_cache, const void *v_cache,
 typedef struct gqa_decode_options {
     int path;          /* GQA_PATH_*; 0 = automatic */
     int num_ctas;      /* CTAs of the split kernel; 0 = automatic (1..GQA_MAX_CTAS) */
-    int reserved[6];   /* must be zero */
+    int window;        /* sliding window: > 0 attends to the last `window` valid
+                          positions of each sequence only, max(0, T - window) <= t < T;
+                          0 = every valid position.  Mistral 7B pairs GQA with a
+                          sliding window ["Grouped-query attention (GQA)" concept
+                          page, "Variants", "Decoder-only models with GQA"]; the
+                          pages give no size, so it is the caller's.  Tensor-core
+                          path only. */
+    int reserved[5];   /* must be zero */
 } gqa_decode_options;
 
 /* gqa_decode with explicit options (opts may be NULL = defaults).  A path that
@@ -146,6 +159,60 @@ gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache
                          void *workspace, size_t workspace_bytes,
                          int B, int H, int G, int d, int Lmax, float scale, void *stream,
                          const gqa_decode_options *opts);
+
+/*
+ * Decode step with the cache append fused in.
+ * ["Grouped-query attention (GQA)" concept page, "Implementation sketch": the
+ *  decode step appends the new token's key and value to the cache, then attends]
+ *
+ * For every sequence b with T = seq_lens[b] >= 1 and K/V head g, the new rows
+ * k_new[b, g, :] and v_new[b, g, :] are written to k_cache[b, g, T-1, :] and
+ * v_cache[b, g, T-1, :], and the decode of gqa_decode_ex runs over the T
+ * positions with those rows in place (the written rows are the ones attended
+ * to; the caches' old contents at T-1 are never used).  Sequences with T = 0 are
+ * not written and give out = 0.  One launch pair, as gqa_decode.
+ *
+ * k_new, v_new  device, bf16 [B, G, d], contiguous, 16-byte aligned
+ * k_cache, v_cache  as gqa_decode, but written (row T-1 of each sequence)
+ * seq_lens  device, int32 [B], required (counts the new token)
+ * Other arguments as gqa_decode_ex.  Tensor-core path only.
+ */
+gqa_status gqa_decode_append(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                             const int32_t *seq_lens, float *out, void *workspace, size_t workspace_bytes,
+                             int B, int H, int G, int d, int Lmax, float scale, void *stream,
+                             const gqa_decode_options *opts);
+
+/*
+ * Decode step over a paged KV cache.
+ * [paged attention is named on the GQA paper's page, "How researchers see this
+ *  paper", where a citing serving paper lists it beside GQA; the layout is this
+ *  library's choice]
+ *
+ * The cache is a pool of num_pages pages; page p holds page_size consecutive
+ * positions of all G K/V heads:
+ *   k_pages, v_pages  device, bf16 [num_pages, G, page_size, d], 16-byte aligned
+ *   block_table       device, int32 [B, max_pages]: position t of sequence b is
+ *                     row t % page_size of page block_table[b, t / page_size]
+ * Only the entries of attended positions are read (t < seq_lens[b], and inside
+ * the window if one is set).  An entry outside [0, num_pages) reads zeros and
+ * sets GQA_FLAG_BAD_PAGE.
+ * page_size   a power of two, 16 .. 2^20
+ * max_pages   >= 1; the cache capacity per sequence is Lmax = max_pages * page_size
+ *             (workspace: gqa_decode_workspace_size(B, H, G, d, Lmax))
+ * num_pages   >= 1, num_pages * G < 2^31
+ * k_new, v_new  optional (both or neither): fused append as gqa_decode_append,
+ *             written into the page that holds position seq_lens[b] - 1
+ * seq_lens    as gqa_decode (NULL: every sequence has Lmax positions; not with
+ *             k_new)
+ * Computes exactly what gqa_decode_ex computes on the contiguous cache
+ * [b, g, t, :] = pages[block_table[b, t / page_size], g, t % page_size, :].
+ * Tensor-core path only.
+ */
+gqa_status gqa_decode_paged(const void *q, void *k_pages, void *v_pages, const int32_t *block_table,
+                            const int32_t *seq_lens, const void *k_new, const void *v_new, float *out,
+                            void *workspace, size_t workspace_bytes, int B, int H, int G, int d, int page_size,
+                            int max_pages, int num_pages, float scale, void *stream,
+                            const gqa_decode_options *opts);
 
 /* The path gqa_decode would take for this shape (GQA_PATH_SIMT or
  * GQA_PATH_TCGEN05), or a negative gqa_status if the shape is rejected. */

@@ -148,6 +148,136 @@ int auto_path(int H, int G, int d) {
     return GQA_PATH_SIMT;
 }
 
+// Paged-cache limits: a page holds at least one 8-row swizzle atom of
+// position pairs, and the pool's K/V rows fit the tensor map's 32-bit extent.
+constexpr int kMinPage = 16;
+constexpr int kMaxPage = 1 << 20;
+constexpr long long kMaxPoolRows = 1ll << 31;
+
+// Page pool viewed as a 3-D tensor [num_pages*G][page_size][d] (paired:
+// [num_pages*G][page_size/2][2d]), boxes of 64 columns x min(rows per page,
+// 128) rows x 1, 128-byte swizzle.  A page smaller than a tile is one box.
+bool make_page_map(CUtensorMap *map, const void *base, int num_pages, int G, int d, int page_size, bool paired) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const int cols = paired ? 2 * d : d, rows = paired ? page_size / 2 : page_size;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)num_pages * G};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)page_size * d * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)gqa::kBoxCols, (cuuint32_t)(rows < gqa::kTile ? rows : gqa::kTile), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Every decode variant: contiguous or paged cache, with or without the fused
+// append, a window, or all positions valid (seq_lens null).
+struct DecodeRequest {
+    const void *q = nullptr, *k = nullptr, *v = nullptr;   // k, v: cache or page pool
+    const void *k_new = nullptr, *v_new = nullptr;         // fused append rows [B, G, d]
+    const int32_t *block_table = nullptr;
+    int page_size = 0, max_pages = 0, num_pages = 0;
+    const int32_t *seq_lens = nullptr;
+    float *out = nullptr;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    int B = 0, H = 0, G = 0, d = 0, Lmax = 0;
+    float scale = 0.f;
+    void *stream = nullptr;
+    const gqa_decode_options *opts = nullptr;
+};
+
+gqa_status decode_impl(const DecodeRequest &r) {
+    if (!r.q || !r.k || !r.v || !r.out) return GQA_ERR_INVALID_ARG;
+    const int B = r.B, H = r.H, G = r.G, d = r.d, Lmax = r.Lmax;
+    gqa_status s = check_shape(B, H, G, d, Lmax);
+    if (s != GQA_OK) return s;
+    if (!std::isfinite(r.scale)) return GQA_ERR_INVALID_ARG;
+    if (!aligned(r.k, 16) || !aligned(r.v, 16) || !aligned(r.q, 16) || !aligned(r.out, 16) ||
+        !aligned(r.seq_lens, 4) || !aligned(r.k_new, 16) || !aligned(r.v_new, 16) || !aligned(r.block_table, 4))
+        return GQA_ERR_INVALID_ARG;
+    gqa_decode_options o{};
+    if (r.opts) o = *r.opts;
+    for (int x : o.reserved)
+        if (x != 0) return GQA_ERR_INVALID_ARG;
+    if (o.num_ctas < 0 || o.num_ctas > GQA_MAX_CTAS) return GQA_ERR_INVALID_ARG;
+    if (o.path < 0 || o.path > GQA_PATH_TCGEN05 || o.window < 0) return GQA_ERR_INVALID_ARG;
+    if (!r.ws || !aligned(r.ws, 256) || r.ws_bytes < workspace_bytes_for(B, H, G, d, Lmax)) return GQA_ERR_WORKSPACE;
+
+    const int n = H / G;
+    const int path = o.path ? o.path : auto_path(H, G, d);
+    if (path == GQA_PATH_SIMT && n > gqa::simt_max_heads()) return GQA_ERR_UNSUPPORTED;
+    if (path == GQA_PATH_TCGEN05 && n > gqa::tc_max_heads()) return GQA_ERR_UNSUPPORTED;
+    // the CUDA-core path reads a contiguous cache, every valid position
+    if (path == GQA_PATH_SIMT && (r.block_table || r.k_new || o.window > 0)) return GQA_ERR_UNSUPPORTED;
+
+    DeviceInfo dev;
+    s = device_info(&dev);
+    if (s != GQA_OK) return s;
+
+    const bool paired = path == GQA_PATH_TCGEN05 && gqa::tc_paired(d, Lmax, n);
+    const int tile_pos = paired ? 2 * gqa::kTile : gqa::kTile;
+    // One CTA per SM, never more than there are tiles.
+    const long long tiles_max = (long long)B * G * ((Lmax + tile_pos - 1) / tile_pos);
+    long long ctas = o.num_ctas ? o.num_ctas : dev.sms;
+    if (ctas > GQA_MAX_CTAS) ctas = GQA_MAX_CTAS;
+    if (ctas > tiles_max) ctas = tiles_max;
+    if (ctas < 1) ctas = 1;
+
+    uint8_t *ws = static_cast<uint8_t *>(r.ws);
+    DecodeParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(r.q);
+    p.seq_lens = r.seq_lens;
+    p.window = o.window;
+    p.block_table = r.block_table;
+    p.page_shift = 0;
+    while (r.block_table && (1 << p.page_shift) < r.page_size) ++p.page_shift;
+    p.max_pages = r.max_pages;
+    p.num_pages = r.num_pages;
+    p.k_new = static_cast<const __nv_bfloat16 *>(r.k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(r.v_new);
+    p.k_dst = r.k_new ? static_cast<__nv_bfloat16 *>(const_cast<void *>(r.k)) : nullptr;
+    p.v_dst = r.v_new ? static_cast<__nv_bfloat16 *>(const_cast<void *>(r.v)) : nullptr;
+    p.out = r.out;
+    p.flags = reinterpret_cast<unsigned int *>(ws);
+    p.ticket = reinterpret_cast<unsigned int *>(ws + 4);
+    p.fails = reinterpret_cast<unsigned int *>(ws + 8);
+    // The CUDA-core path splits statically; so does the paired d=64 tcgen05 form, whose
+    // piece ends (two GEMM parts per tile) cost more than per-SM balancing wins back.
+    p.dyn_cap = (path == GQA_PATH_TCGEN05 && !paired) ? dyn_cap_for(B, G, Lmax) : 0;
+    p.tile_shift = paired ? 8 : 7;
+    p.partials = reinterpret_cast<float *>(ws + kHeaderBytes);
+    p.B = B;
+    p.H = H;
+    p.G = G;
+    p.n = n;
+    p.Lmax = Lmax;
+    p.scale_log2 = r.scale * 1.4426950408889634f;
+
+    CUtensorMap tk, tv;
+    const bool maps_ok = r.block_table
+                             ? make_page_map(&tk, r.k, r.num_pages, G, d, r.page_size, paired) &&
+                                   make_page_map(&tv, r.v, r.num_pages, G, d, r.page_size, paired)
+                             : make_cache_map(&tk, r.k, B, G, d, Lmax, paired) &&
+                                   make_cache_map(&tv, r.v, B, G, d, Lmax, paired);
+    if (!maps_ok) return GQA_ERR_LAUNCH;
+    cudaStream_t st = static_cast<cudaStream_t>(r.stream);
+    cudaError_t e;
+    if (path == GQA_PATH_SIMT) {
+        e = gqa::launch_decode_simt(tk, tv, p, d, (int)ctas, st);
+    } else {
+        const int rows = gqa::tc_rows_for(n);
+        CUtensorMap tq;
+        if (!make_q_map(&tq, r.q, B, H, d, rows)) return GQA_ERR_LAUNCH;
+        e = gqa::launch_decode_tc(tk, tv, tq, p, d, paired, (int)ctas, st);
+    }
+    if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return GQA_ERR_LAUNCH;
+    // merge the segments the work split cut across CTAs (a no-op grid when none is)
+    e = gqa::launch_split_combine(p, d, (int)ctas, st);
+    return e == cudaSuccess ? GQA_OK : GQA_ERR_LAUNCH;
+}
+
 }  // namespace
 
 namespace gqa {
@@ -191,78 +321,19 @@ int gqa_decode_select_path(int B, int H, int G, int d, int Lmax) {
 gqa_status gqa_decode_ex(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
                          float *out, void *workspace, size_t workspace_bytes, int B, int H, int G, int d, int Lmax,
                          float scale, void *stream, const gqa_decode_options *opts) {
-    if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
-    gqa_status s = check_shape(B, H, G, d, Lmax);
-    if (s != GQA_OK) return s;
-    if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
-    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16) ||
-        !aligned(seq_lens, 4))
-        return GQA_ERR_INVALID_ARG;
-    gqa_decode_options o{};
-    if (opts) o = *opts;
-    for (int r : o.reserved)
-        if (r != 0) return GQA_ERR_INVALID_ARG;
-    if (o.num_ctas < 0 || o.num_ctas > GQA_MAX_CTAS) return GQA_ERR_INVALID_ARG;
-    if (o.path < 0 || o.path > GQA_PATH_TCGEN05) return GQA_ERR_INVALID_ARG;
-    if (!workspace || !aligned(workspace, 256) || workspace_bytes < workspace_bytes_for(B, H, G, d, Lmax))
-        return GQA_ERR_WORKSPACE;
-
-    const int n = H / G;
-    int path = o.path ? o.path : auto_path(H, G, d);
-    if (path == GQA_PATH_SIMT && n > gqa::simt_max_heads()) return GQA_ERR_UNSUPPORTED;
-    if (path == GQA_PATH_TCGEN05 && n > gqa::tc_max_heads()) return GQA_ERR_UNSUPPORTED;
-
-    DeviceInfo dev;
-    s = device_info(&dev);
-    if (s != GQA_OK) return s;
-
-    const bool paired = path == GQA_PATH_TCGEN05 && gqa::tc_paired(d, Lmax, n);
-    const int tile_pos = paired ? 2 * gqa::kTile : gqa::kTile;
-    // One CTA per SM, never more than there are tiles.
-    const long long tiles_max = (long long)B * G * ((Lmax + tile_pos - 1) / tile_pos);
-    long long ctas = o.num_ctas ? o.num_ctas : dev.sms;
-    if (ctas > GQA_MAX_CTAS) ctas = GQA_MAX_CTAS;
-    if (ctas > tiles_max) ctas = tiles_max;
-    if (ctas < 1) ctas = 1;
-
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    DecodeParams p;
-    p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.seq_lens = seq_lens;
-    p.out = out;
-    p.flags = reinterpret_cast<unsigned int *>(ws);
-    p.ticket = reinterpret_cast<unsigned int *>(ws + 4);
-    p.fails = reinterpret_cast<unsigned int *>(ws + 8);
-    // The CUDA-core path splits statically; so does the paired d=64 tcgen05 form, whose
-    // piece ends (two GEMM parts per tile) cost more than per-SM balancing wins back.
-    p.dyn_cap = (path == GQA_PATH_TCGEN05 && !paired) ? dyn_cap_for(B, G, Lmax) : 0;
-    p.tile_shift = paired ? 8 : 7;
-    p.partials = reinterpret_cast<float *>(ws + kHeaderBytes);
-    p.B = B;
-    p.H = H;
-    p.G = G;
-    p.n = n;
-    p.Lmax = Lmax;
-    p.scale_log2 = scale * 1.4426950408889634f;
-
-    CUtensorMap tk, tv;
-    if (!make_cache_map(&tk, k_cache, B, G, d, Lmax, paired) || !make_cache_map(&tv, v_cache, B, G, d, Lmax, paired))
-        return GQA_ERR_LAUNCH;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (path == GQA_PATH_SIMT) {
-        e = gqa::launch_decode_simt(tk, tv, p, d, (int)ctas, st);
-    } else {
-        const int rows = gqa::tc_rows_for(n);
-        CUtensorMap tq;
-        if (!make_q_map(&tq, q, B, H, d, rows)) return GQA_ERR_LAUNCH;
-        e = gqa::launch_decode_tc(tk, tv, tq, p, d, paired, (int)ctas, st);
-    }
-    if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
-    if (e != cudaSuccess) return GQA_ERR_LAUNCH;
-    // merge the segments the work split cut across CTAs (a no-op grid when none is)
-    e = gqa::launch_split_combine(p, d, (int)ctas, st);
-    return e == cudaSuccess ? GQA_OK : GQA_ERR_LAUNCH;
+    DecodeRequest r;
+    r.q = q;
+    r.k = k_cache;
+    r.v = v_cache;
+    r.seq_lens = seq_lens;
+    r.out = out;
+    r.ws = workspace;
+    r.ws_bytes = workspace_bytes;
+    r.B = B, r.H = H, r.G = G, r.d = d, r.Lmax = Lmax;
+    r.scale = scale;
+    r.stream = stream;
+    r.opts = opts;
+    return decode_impl(r);
 }
 
 gqa_status gqa_decode(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens, float *out,
@@ -270,6 +341,60 @@ gqa_status gqa_decode(const void *q, const void *k_cache, const void *v_cache, c
                       void *stream) {
     return gqa_decode_ex(q, k_cache, v_cache, seq_lens, out, workspace, workspace_bytes, B, H, G, d, Lmax, scale,
                          stream, nullptr);
+}
+
+gqa_status gqa_decode_append(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                             const int32_t *seq_lens, float *out, void *workspace, size_t workspace_bytes, int B,
+                             int H, int G, int d, int Lmax, float scale, void *stream,
+                             const gqa_decode_options *opts) {
+    if (!k_new || !v_new || !seq_lens) return GQA_ERR_INVALID_ARG;
+    DecodeRequest r;
+    r.q = q;
+    r.k = k_cache;
+    r.v = v_cache;
+    r.k_new = k_new;
+    r.v_new = v_new;
+    r.seq_lens = seq_lens;
+    r.out = out;
+    r.ws = workspace;
+    r.ws_bytes = workspace_bytes;
+    r.B = B, r.H = H, r.G = G, r.d = d, r.Lmax = Lmax;
+    r.scale = scale;
+    r.stream = stream;
+    r.opts = opts;
+    return decode_impl(r);
+}
+
+gqa_status gqa_decode_paged(const void *q, void *k_pages, void *v_pages, const int32_t *block_table,
+                            const int32_t *seq_lens, const void *k_new, const void *v_new, float *out,
+                            void *workspace, size_t workspace_bytes, int B, int H, int G, int d, int page_size,
+                            int max_pages, int num_pages, float scale, void *stream,
+                            const gqa_decode_options *opts) {
+    if (!block_table || (!k_new) != (!v_new) || (k_new && !seq_lens)) return GQA_ERR_INVALID_ARG;
+    if (page_size < kMinPage || page_size > kMaxPage || (page_size & (page_size - 1)) != 0 || max_pages <= 0 ||
+        num_pages <= 0)
+        return GQA_ERR_INVALID_ARG;
+    if ((long long)max_pages * page_size > kMaxLmax || (long long)num_pages * G >= kMaxPoolRows)
+        return GQA_ERR_UNSUPPORTED;
+    DecodeRequest r;
+    r.q = q;
+    r.k = k_pages;
+    r.v = v_pages;
+    r.k_new = k_new;
+    r.v_new = v_new;
+    r.block_table = block_table;
+    r.page_size = page_size;
+    r.max_pages = max_pages;
+    r.num_pages = num_pages;
+    r.seq_lens = seq_lens;
+    r.out = out;
+    r.ws = workspace;
+    r.ws_bytes = workspace_bytes;
+    r.B = B, r.H = H, r.G = G, r.d = d, r.Lmax = max_pages * page_size;
+    r.scale = scale;
+    r.stream = stream;
+    r.opts = opts;
+    return decode_impl(r);
 }
 
 gqa_status gqa_decode_read_flags(void *workspace, uint32_t *flags, int clear, void *stream) {

@@ -36,7 +36,7 @@ template <int D>
 __global__ void __launch_bounds__(kCombThreads) gqa_split_combine_kernel(const DecodeParams p, int grid_main) {
     __shared__ int prefix[kMaxBatch + 1];
     __shared__ int scratch[33];
-    build_prefix(p.seq_lens, p.B, p.Lmax, p.tile_shift, prefix, scratch, nullptr);   // ends with __syncthreads
+    build_prefix(p, p.tile_shift, prefix, scratch, nullptr);   // ends with __syncthreads
     const int G = p.G, n = p.n;
     const WorkSplit split = make_split((long long)G * prefix[p.B], grid_main,
                                        pool_tail_tiles(prefix, p.B, G, scratch[32]), p.dyn_cap);

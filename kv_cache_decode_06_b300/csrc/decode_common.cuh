@@ -2,7 +2,10 @@
 //
 // Work unit: a tile of 128 (or, in the paired d = 64 layout, 256) consecutive
 // cache positions of one (sequence b, K/V head g) pair, a "segment".  Segment
-// s = b*G + g holds tiles_b = ceil(seq_lens[b] / tile) tiles.  All tiles of all
+// s = b*G + g holds the tiles that meet the attended positions [t0_b, T_b) of
+// sequence b: T_b = seq_lens[b] (Lmax when seq_lens is null), t0_b = T_b - window
+// with a sliding window shorter than T_b, else 0.  Tile j of the segment covers
+// positions [(j0_b + j) * tile, ...), j0_b = t0_b / tile.  All tiles of all
 // segments form one list in (b, g, j) order, W tiles long.
 //
 // Static part.  The first Ws tiles are split evenly: CTA c of Pw = min(grid, Ws)
@@ -49,7 +52,18 @@ constexpr int kPoolMinTilesPerCta = 64;   // tiles per CTA below which the split
 
 struct DecodeParams {
     const __nv_bfloat16 *q;   // [B, H, D]
-    const int32_t *seq_lens;  // [B]
+    const int32_t *seq_lens;  // [B]; null: every sequence holds Lmax positions
+    int window;               // > 0: attend to the last `window` positions only
+    // paged cache (block_table non-null): the K/V tensor maps view a pool of
+    // pages [num_pages, G, page_size, D]; row b of the table lists sequence b's pages
+    const int32_t *block_table;   // [B, max_pages]
+    int page_shift;               // log2(page_size)
+    int max_pages, num_pages;
+    // fused append (k_new non-null): the new token's K/V rows [B, G, D] replace
+    // position T_b - 1 in the tiles read and are written to the cache (k_dst, v_dst:
+    // the contiguous cache or the page pool)
+    const __nv_bfloat16 *k_new, *v_new;
+    __nv_bfloat16 *k_dst, *v_dst;
     float *out;               // [B, H, D]
     unsigned int *flags;      // workspace flag word
     unsigned int *ticket;     // dynamic-pool claims (zero between calls)
@@ -64,6 +78,21 @@ struct DecodeParams {
 __device__ __forceinline__ int tiles_of(int seq, int shift) { return (seq + (1 << shift) - 1) >> shift; }
 
 __device__ __forceinline__ int clamp_seq(int s, int Lmax) { return s < 0 ? 0 : (s > Lmax ? Lmax : s); }
+
+// T_b: valid positions of sequence b, clamped into [0, Lmax].
+__device__ __forceinline__ int seq_len_of(const DecodeParams &p, int b) {
+    return p.seq_lens ? clamp_seq(__ldg(p.seq_lens + b), p.Lmax) : p.Lmax;
+}
+
+// t0_b: first attended position (sliding window), 0 without a window.
+__device__ __forceinline__ int window_start(const DecodeParams &p, int T) {
+    return (p.window > 0 && T > p.window) ? T - p.window : 0;
+}
+
+// Tiles of sequence b's segments: those meeting [t0_b, T_b).
+__device__ __forceinline__ int segment_tiles(const DecodeParams &p, int T, int shift) {
+    return tiles_of(T, shift) - (window_start(p, T) >> shift);
+}
 
 // Tile counts stay below 2^31 (kMaxBatch * heads * tiles per sequence), so the
 // split arithmetic below avoids 64-bit divisions, which are long instruction
@@ -149,22 +178,25 @@ __device__ __forceinline__ long long segment_start(const Cursor &c, const int *p
     return (long long)G * prefix[c.b] + (long long)c.g * c.tiles;
 }
 
-// Block-wide: clamps seq_lens into [0, Lmax] and writes the tile prefix sums;
-// with a flag word, CTA 0 records a clamp in it.  `scratch` needs 33 ints;
-// scratch[32] receives the last sequence whose segments are too long for the
-// dynamic pool (-1 if none).  Ends with __syncthreads().
-__device__ inline void build_prefix(const int32_t *seq_lens, int B, int Lmax, int shift, int *prefix, int *scratch,
+// Block-wide: clamps seq_lens into [0, Lmax] and writes the prefix sums of
+// the segments' tile counts; with a flag word, CTA 0 records a clamp in it.
+// `scratch` needs 33 ints; scratch[32] receives the last sequence whose
+// segments are too long for the dynamic pool (-1 if none).  Ends with
+// __syncthreads().
+__device__ inline void build_prefix(const DecodeParams &p, int shift, int *prefix, int *scratch,
                                     unsigned int *flags) {
-    const int tid = threadIdx.x, nth = blockDim.x;
+    const int tid = threadIdx.x, nth = blockDim.x, B = p.B;
     if (tid == 0) scratch[32] = -1;
     const int per = (B + nth - 1) / nth;
     const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
     int local = 0;
     bool bad = false;
     for (int b = b0; b < b1; ++b) {
-        const int s = __ldg(seq_lens + b);
-        bad |= (s < 0 || s > Lmax);
-        local += tiles_of(clamp_seq(s, Lmax), shift);
+        if (p.seq_lens) {
+            const int s = __ldg(p.seq_lens + b);
+            bad |= (s < 0 || s > p.Lmax);
+        }
+        local += segment_tiles(p, seq_len_of(p, b), shift);
     }
     // exclusive scan of `local` over the block
     const int lane = tid & 31, warp = tid >> 5, nwarps = (nth + 31) >> 5;
@@ -185,7 +217,7 @@ __device__ inline void build_prefix(const int32_t *seq_lens, int B, int Lmax, in
     int run = before + incl - local, last_long = -1;
     for (int b = b0; b < b1; ++b) {
         prefix[b] = run;
-        const int tb = tiles_of(clamp_seq(__ldg(seq_lens + b), Lmax), shift);
+        const int tb = segment_tiles(p, seq_len_of(p, b), shift);
         run += tb;
         if (tb > kPoolSegChunks * kChunk) last_long = b;
     }

@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(SimtCfg<D, NMAX>::kThreads, 1)
     // have completed.
     griddep_wait();
     griddep_launch_dependents();
-    build_prefix(p.seq_lens, p.B, p.Lmax, 7, prefix, scratch, p.flags);  // ends with __syncthreads
+    build_prefix(p, 7, prefix, scratch, p.flags);  // ends with __syncthreads
 
     const int G = p.G, n = p.n;
     const long long W = (long long)G * prefix[p.B];
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(SimtCfg<D, NMAX>::kThreads, 1)
             const float *qp = q_s + (piece & 1) * NMAX * D;
             if (first) {
                 piece_u0 = u;
-                seq_b = clamp_seq(__ldg(p.seq_lens + cur.b), p.Lmax);
+                seq_b = seq_len_of(p, cur.b);
                 const __nv_bfloat16 *qg = p.q + ((size_t)cur.b * p.H + (size_t)cur.g * n) * D;
                 float *qw = q_s + (piece & 1) * NMAX * D;
                 for (int x = tid; x < n * D; x += C::kWarps * 32) qw[x] = __bfloat162float(qg[x]);

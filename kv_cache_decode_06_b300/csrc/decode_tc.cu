@@ -97,6 +97,16 @@ constexpr int pow2_cols(int c) { return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ?
 
 constexpr int kRing = 4;   // work ranges in flight from the producer to the other roles
 
+// Where a K or V slot's staged row (the appended token) goes: tile row `rel`
+// (position T - 1 minus the tile's first position) and, when dst is not null,
+// the cache row in global memory.
+struct PatchInfo {
+    __nv_bfloat16 *dst;
+    int rel;
+    int on;   // 0: nothing staged for this slot
+};
+static_assert(sizeof(PatchInfo) == 16, "PatchInfo layout");
+
 // One work range (the static range or a claimed chunk) as the producer hands it on.
 struct RangeEntry {
     long long ub;   // first tile
@@ -146,18 +156,22 @@ struct TcCfg {
     static constexpr int fixed_bytes(int QB) {
         return QB * kQBytes + 2 * kPBufBytes + kSmallBytes + bar_bytes(8, 8, QB) + 1024 /* alignment slack */;
     }
+    // Per K or V slot, beside the tile: the appended token's row as copied from
+    // global memory, and where it goes (fused append; unused otherwise).
+    static constexpr int kRowBytes = D * 2;
+    static constexpr int kSlotCost = kTileBytes + kRowBytes + (int)sizeof(PatchInfo);
     // K and V rings: as deep as shared memory allows (at most 8), V one deeper when
     // a single extra tile still fits (V slots are held until the value GEMM is done)
     static constexpr int avail(int QB) { return kSmemLimit - fixed_bytes(QB); }
-    static constexpr int pairs_for(int QB) { return cmin(8, avail(QB) / (2 * kTileBytes)); }
+    static constexpr int pairs_for(int QB) { return cmin(8, avail(QB) / (2 * kSlotCost)); }
     static constexpr int kQBuf = pairs_for(2) >= 3 || pairs_for(1) == pairs_for(2) ? 2 : 1;
     static constexpr int kSK = pairs_for(kQBuf);
-    static constexpr int kSV = (kSK < 8 && avail(kQBuf) - 2 * kSK * kTileBytes >= kTileBytes) ? kSK + 1 : kSK;
+    static constexpr int kSV = (kSK < 8 && avail(kQBuf) - 2 * kSK * kSlotCost >= kSlotCost) ? kSK + 1 : kSK;
     static_assert(kSK >= 2, "shared memory too small for two stages");
     // P buffers: three when they fit beside the rings (the softmax then waits for the
     // value GEMM three tiles back before reusing one), else two
     static constexpr int layout_bytes(int pbuf) {
-        return (kSK + kSV) * kTileBytes + kQBuf * kQBytes + pbuf * kPBufBytes + kSmallBytes + 8 +
+        return (kSK + kSV) * kSlotCost + kQBuf * kQBytes + pbuf * kPBufBytes + kSmallBytes + 8 +
                (2 * kSK + 2 * kSV + 2 * kQBuf + 12 + pbuf + 2 + 2 * kRing) * 8 + 16 + 1024;
     }
     static constexpr int kPBuf = layout_bytes(3) <= kSmemLimit ? 3 : 2;
@@ -173,7 +187,9 @@ struct TcCfg {
     static constexpr int kOffPrefix = kOffA + kAF * 4;                    // i32 [kMaxBatch + 1]
     static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 1) * 4;  // i32 [33]
     static constexpr int kOffRing = (kOffScratch + 33 * 4 + 15) / 16 * 16;  // RangeEntry [kRing]
-    static constexpr int kOffBar = kOffRing + kRing * 16;
+    static constexpr int kOffStage = kOffRing + kRing * 16;                 // [SK + SV] appended rows
+    static constexpr int kOffPatch = kOffStage + (kSK + kSV) * kRowBytes;   // PatchInfo [SK + SV]
+    static constexpr int kOffBar = kOffPatch + (kSK + kSV) * (int)sizeof(PatchInfo);
     // barriers: kfull[SK] kempty[SK] vfull[SV] vempty[SV] qfull[QB] qempty[QB] sfull[2] sfree[2]
     //           pfull[PB] ofull[3] ofree[3] red[2] grp done
     static constexpr int kNumBars = 2 * kSK + 2 * kSV + 2 * kQBuf + 12 + kPBuf + 2 + 2 * kRing;
@@ -294,6 +310,109 @@ __device__ __forceinline__ void store_vec(float *dst, const float (&v)[NH]) {
     }
 }
 
+// A page id read from the block table, or (flagged) one past the pool when it
+// is not a page of the pool: the tensor map then fills the rows with zeros.
+__device__ __forceinline__ int checked_page(const DecodeParams &p, int page) {
+    if (page >= 0 && page < p.num_pages) return page;
+    atomicOr(p.flags, 0x4u /* GQA_FLAG_BAD_PAGE */);
+    return p.num_pages;
+}
+
+// Producer: copies the K or V tile at cursor c into `dst` (kColBoxes boxes of
+// 128 tensor-map rows x 128 bytes, 128-byte swizzle), completing on `bar`.
+// Contiguous cache: one box per column box at row (j0 + j) * 128 of segment
+// b*G + g.  Paged cache: the tile's positions come from the pages its block-table
+// entries name; pages smaller than a tile are copied one box each, and pages
+// holding no attended position are skipped (their rows are masked).  With an
+// appended row for the tile (row_new), it is copied beside the tile and `info`
+// says where it goes; `info` is written before the arrival that publishes it.
+template <class C>
+__device__ __forceinline__ void issue_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst, uint64_t *bar,
+                                           const Cursor &c, uint64_t pol, const __nv_bfloat16 *row_new,
+                                           uint8_t *stage_row, PatchInfo *info, __nv_bfloat16 *row_dst) {
+    constexpr int kPairShift = C::kParts - 1;   // tensor-map rows hold 2 positions in the paired layout
+    constexpr int kMaxBoxes = C::kTilePos / 16;   // pages of 16 positions or more
+    const int T = seq_len_of(p, c.b), t0 = window_start(p, T);
+    const int pos0 = ((t0 >> C::kTileShift) + c.j) << C::kTileShift;   // first position of the tile
+    const int seg = c.b * p.G + c.g;
+    const bool app = row_new != nullptr && c.j + 1 == c.tiles;        // the tile holds position T - 1
+    uint32_t bytes = app ? C::kRowBytes : 0;
+    if (app) {
+        __nv_bfloat16 *d = nullptr;
+        if (!p.block_table) {
+            d = row_dst + ((size_t)seg * p.Lmax + (T - 1)) * C::kRowBytes / 2;
+        } else {
+            const int page = __ldg(p.block_table + (size_t)c.b * p.max_pages + ((T - 1) >> p.page_shift));
+            if (page >= 0 && page < p.num_pages)
+                d = row_dst + (((size_t)page * p.G + c.g) * ((size_t)1 << p.page_shift) +
+                               ((T - 1) & ((1 << p.page_shift) - 1))) * (C::kRowBytes / 2);
+        }
+        info->dst = d;
+        info->rel = T - 1 - pos0;
+    }
+    info->on = app ? 1 : 0;
+    if (!p.block_table) {
+        mbar_arrive_expect_tx(bar, bytes + C::kTileBytes);
+#pragma unroll
+        for (int cb = 0; cb < C::kColBoxes; ++cb)
+            tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, pos0 >> kPairShift, seg, bar, pol);
+    } else {
+        const int ps = 1 << p.page_shift, prow = ps >> kPairShift;   // tensor-map rows per page
+        const int32_t *trow = p.block_table + (size_t)c.b * p.max_pages;
+        if (prow >= kTile) {
+            const int page = checked_page(p, __ldg(trow + (pos0 >> p.page_shift)));
+            mbar_arrive_expect_tx(bar, bytes + C::kTileBytes);
+#pragma unroll
+            for (int cb = 0; cb < C::kColBoxes; ++cb)
+                tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, (pos0 & (ps - 1)) >> kPairShift,
+                            page * p.G + c.g, bar, pol);
+        } else {
+            const int nb = kTile / prow;   // pages per tile, <= kMaxBoxes
+            int page[kMaxBoxes];
+            int loads = 0;
+#pragma unroll
+            for (int k = 0; k < kMaxBoxes; ++k) {
+                const int pos = pos0 + k * ps;
+                page[k] = -1;
+                if (k < nb && pos < T && pos + ps > t0) {
+                    page[k] = __ldg(trow + (pos >> p.page_shift));
+                    ++loads;
+                }
+            }
+            mbar_arrive_expect_tx(bar, bytes + (uint32_t)(loads * prow * 128 * C::kColBoxes));
+#pragma unroll
+            for (int k = 0; k < kMaxBoxes; ++k) {
+                if (k < nb && page[k] != -1) {
+                    const int z = checked_page(p, page[k]) * p.G + c.g;
+#pragma unroll
+                    for (int cb = 0; cb < C::kColBoxes; ++cb)
+                        tma_load_3d(dst + cb * kBoxBytes + k * prow * 128, tm, cb * kBoxCols, 0, z, bar, pol);
+                }
+            }
+        }
+    }
+    if (app) bulk_load(stage_row, row_new + (size_t)seg * (C::kRowBytes / 2), C::kRowBytes, bar);
+}
+
+// MMA issuer: writes a slot's staged row (the appended token) into its tile,
+// row info.rel, in the 128-byte swizzled layout the TMA produced, and to the
+// cache in global memory; then makes the tile visible to the tensor cores.
+template <class C>
+__device__ __forceinline__ void patch_tile(uint8_t *tile, const uint8_t *stage_row, const PatchInfo &info) {
+    constexpr bool kPairL = C::kParts == 2;
+    const int rel = info.rel;
+    const int r = kPairL ? rel >> 1 : rel;   // tensor-map row of the position
+#pragma unroll
+    for (int q = 0; q < C::kRowBytes / 16; ++q) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(stage_row + q * 16);
+        const int cb = kPairL ? (rel & 1) : (q >> 3);   // column box: the position's half, or dims 64q'..
+        const int qq = q & 7;                           // 16-byte chunk inside the 128-byte row
+        *reinterpret_cast<uint4 *>(tile + cb * kBoxBytes + r * 128 + ((qq ^ (r & 7)) << 4)) = v;
+        if (info.dst) reinterpret_cast<uint4 *>(info.dst)[q] = v;
+    }
+    fence_proxy_async_smem();
+}
+
 template <int D, bool kPair, int N, int NH>
 __global__ void __launch_bounds__(224, 1)
     gqa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -314,6 +433,8 @@ __global__ void __launch_bounds__(224, 1)
     uint64_t *sfull = qempty + QB, *sfree = sfull + 2, *pfull = sfree + 2, *ofull = pfull + PB, *ofree = ofull + 3;
     uint64_t *redbar = ofree + 3, *grp = redbar + 2, *done = grp + 1, *rfull = done + 1, *rempty = rfull + kRing;
     RangeEntry *ring = reinterpret_cast<RangeEntry *>(smem + C::kOffRing);
+    uint8_t *kstage = smem + C::kOffStage, *vstage = kstage + SK * C::kRowBytes;
+    PatchInfo *kinfo = reinterpret_cast<PatchInfo *>(smem + C::kOffPatch), *vinfo = kinfo + SK;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::kOffFlags);
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::kOffFlags + 8);
 
@@ -371,7 +492,7 @@ __global__ void __launch_bounds__(224, 1)
     griddep_wait();
     if (tid == 64) GQA_TRACE_AT(kTrDepDone, clock64());
     griddep_launch_dependents();
-    build_prefix(p.seq_lens, p.B, p.Lmax, C::kTileShift, prefix, scratch, p.flags);   // ends with __syncthreads
+    build_prefix(p, C::kTileShift, prefix, scratch, p.flags);   // ends with __syncthreads
     tc_fence_after_sync();
     const uint32_t tmem = *s_tmem;
     if (tid == 64) GQA_TRACE_AT(kTrSetup, clock64());
@@ -462,12 +583,8 @@ __global__ void __launch_bounds__(224, 1)
                             ++qissued;
                             if (i == 0) GQA_TRACE_AT(kTrFirstQ, clock64());
                         }
-                        uint8_t *kdst = smem + C::kOffK + st * C::kTileBytes;
-                        const int z = kc.b * G + kc.g, y = kc.j * kTile;
-                        mbar_arrive_expect_tx(&kfull[st], C::kTileBytes);
-#pragma unroll
-                        for (int c = 0; c < C::kColBoxes; ++c)
-                            tma_load_3d(kdst + c * kBoxBytes, &tm_k, c * kBoxCols, y, z, &kfull[st], pol_kv);
+                        issue_tile<C>(p, &tm_k, smem + C::kOffK + st * C::kTileBytes, &kfull[st], kc, pol_kv,
+                                      p.k_new, kstage + st * C::kRowBytes, &kinfo[st], p.k_dst);
                         if (i == 0) GQA_TRACE_AT(kTrFirstK, clock64());
                         if (i < 128) GQA_TRACE_AT(kTrKIssue + i, clock64());
                         ++kissued;
@@ -493,12 +610,8 @@ __global__ void __launch_bounds__(224, 1)
                 if (v_u < v_end && vissued < kissued) {
                     const int i = vissued, st = i % SV;
                     if (i < SV || mbar_test_wait(&vempty[st], ((i / SV) - 1) & 1)) {
-                        uint8_t *vdst = smem + C::kOffV + st * C::kTileBytes;
-                        const int z = vc.b * G + vc.g, y = vc.j * kTile;
-                        mbar_arrive_expect_tx(&vfull[st], C::kTileBytes);
-#pragma unroll
-                        for (int c = 0; c < C::kColBoxes; ++c)
-                            tma_load_3d(vdst + c * kBoxBytes, &tm_v, c * kBoxCols, y, z, &vfull[st], pol_kv);
+                        issue_tile<C>(p, &tm_v, smem + C::kOffV + st * C::kTileBytes, &vfull[st], vc, pol_kv,
+                                      p.v_new, vstage + st * C::kRowBytes, &vinfo[st], p.v_dst);
                         ++vissued;
                         ++v_u;
                         cursor_next(vc, prefix, p.B, G);
@@ -566,6 +679,8 @@ __global__ void __launch_bounds__(224, 1)
                     if ((!first || mbar_test_wait(&qfull[qb], (piece / QB) & 1)) && kready &&
                         (s_i < 2 || mbar_test_wait(&sfree[bi], ((s_i >> 1) - 1) & 1))) {
                         tc_fence_after_sync();
+                        if (p.k_new && kinfo[st].on)   // the appended key replaces its row first
+                            patch_tile<C>(smem + C::kOffK + st * C::kTileBytes, kstage + st * C::kRowBytes, kinfo[st]);
                         const uint32_t kb = sbase + C::kOffK + st * C::kTileBytes;
                         const uint32_t qbase = sbase + C::kOffQ + qb * C::kQBytes;
                         // part c (paired layout: the box of even / odd positions) -> S columns [bi][c];
@@ -604,6 +719,8 @@ __global__ void __launch_bounds__(224, 1)
                     if (vready && mbar_test_wait(&pfull[pbi], (pv_i / PB) & 1) &&
                         (pv_i < 3 || mbar_test_wait(&ofree[ob], ((pv_i / 3) - 1) & 1))) {
                         tc_fence_after_sync();
+                        if (p.v_new && vinfo[st].on)   // the appended value replaces its row first
+                            patch_tile<C>(smem + C::kOffV + st * C::kTileBytes, vstage + st * C::kRowBytes, vinfo[st]);
                         const uint32_t vb = sbase + C::kOffV + st * C::kTileBytes;
                         const uint32_t d_o = tmem + C::kOCol + ob * C::kOW;
                         // A = V^T, MN-major: the column boxes are the M atoms (LBO), 16 positions = 2 KB
@@ -644,7 +761,7 @@ __global__ void __launch_bounds__(224, 1)
         zero_empty_sequences<D>(p, prefix, P, tg, 128);
         GroupSync gsync{grp, 0};
         float l_part[NH], acc[NH];
-        int seq_b = 0, piece_i0 = 0, npe = 0, i = 0, rr = 0;
+        int seq_b = 0, win_b = 0, piece_i0 = 0, npe = 0, i = 0, rr = 0;
         long long piece_u0 = 0;
         bool ok = true;
 
@@ -691,7 +808,8 @@ __global__ void __launch_bounds__(224, 1)
             if (first) {
                 piece_u0 = u;
                 piece_i0 = i;
-                seq_b = clamp_seq(__ldg(p.seq_lens + cur.b), p.Lmax);
+                seq_b = seq_len_of(p, cur.b);
+                win_b = window_start(p, seq_b);
 #pragma unroll
                 for (int h = 0; h < NH; ++h) {
                     l_part[h] = 0.f;
@@ -709,14 +827,18 @@ __global__ void __launch_bounds__(224, 1)
             tmem_wait_ld();
             tc_fence_before_sync();
             mbar_arrive(&sfree[bi]);
-            const int valid_cnt = seq_b - (cur.j << C::kTileShift);   // >= 1
+            // attended positions of this tile: [lo, hi) relative to its first position
+            const int tile_pos0 = ((win_b >> C::kTileShift) + cur.j) << C::kTileShift;
+            const int valid_cnt = seq_b - tile_pos0;   // hi, >= 1
+            const int lo = win_b - tile_pos0;          // <= 0 except in a window's first tile
             bool valid[NP];
             float x[NP][NH], red_v[NH];
 #pragma unroll
             for (int h = 0; h < NH; ++h) red_v[h] = -INFINITY;
 #pragma unroll
             for (int c = 0; c < NP; ++c) {
-                valid[c] = (kPair ? 2 * r + c : r) < valid_cnt;
+                const int pos = kPair ? 2 * r + c : r;
+                valid[c] = pos < valid_cnt && pos >= lo;
 #pragma unroll
                 for (int h = 0; h < NH; ++h) {
                     x[c][h] = valid[c] ? __uint_as_float(sraw[c][h]) * p.scale_log2 : -INFINITY;
@@ -756,8 +878,9 @@ __global__ void __launch_bounds__(224, 1)
                 store_vec<NH>(mrun_s + (i % 3) * NH, m_new);
                 store_vec<NH>(alpha_s + (i % 4) * NH, alpha);
             }
-            // ---- the last tile of a sequence: clear V rows past the end (they may hold NaN)
-            if (valid_cnt < C::kTilePos) {
+            // ---- clear V rows outside [lo, hi): past the end of a sequence, before a window's
+            // start, or in pages not copied; they may hold anything, NaN included
+            if (valid_cnt < C::kTilePos || lo > 0) {
                 const int sv = i % SV;
                 if (!mbar_wait(&vfull[sv], (i / SV) & 1, ab)) { ok = false; break; }
                 uint8_t *vrow = smem + C::kOffV + sv * C::kTileBytes + r * 128;

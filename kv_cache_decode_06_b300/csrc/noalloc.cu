@@ -59,7 +59,7 @@ gqa_status scratch_address(void **out) {
 extern "C" gqa_status gqa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
                                          const int32_t *seq_lens, float *out, int B, int H, int G, int d, int Lmax,
                                          float scale, void *stream) {
-    if (!q || !k_cache || !v_cache || !seq_lens || !out) return GQA_ERR_INVALID_ARG;
+    if (!q || !k_cache || !v_cache || !out) return GQA_ERR_INVALID_ARG;
     size_t need = 0;
     const gqa_status s = gqa_decode_workspace_size(B, H, G, d, Lmax, &need);
     if (s != GQA_OK) return s;

@@ -25,11 +25,12 @@ STATUS_NAMES = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_UNSUPPORTED",
 PATH_AUTO, PATH_SIMT, PATH_TCGEN05 = 0, 1, 2
 FLAG_SEQ_LEN_CLAMPED = 0x1
 FLAG_WAIT_TIMEOUT = 0x2
+FLAG_BAD_PAGE = 0x4
 
 # Every symbol include/gqa.h declares.
 EXPORTS = ("gqa_status_string", "gqa_abi_version", "gqa_decode_workspace_size", "gqa_decode", "gqa_decode_ex",
            "gqa_decode_select_path", "gqa_decode_read_flags", "gqa_meanpool_kv", "gqa_meanpool_kv_strided",
-           "gqa_decode_noalloc")
+           "gqa_decode_noalloc", "gqa_decode_append", "gqa_decode_paged")
 NOALLOC_WORKSPACE_BYTES = 8 << 20
 
 _lock = threading.Lock()
@@ -43,7 +44,8 @@ class GQAError(RuntimeError):
 
 
 class DecodeOptions(ctypes.Structure):
-    _fields_ = [("path", ctypes.c_int), ("num_ctas", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+    _fields_ = [("path", ctypes.c_int), ("num_ctas", ctypes.c_int), ("window", ctypes.c_int),
+                ("reserved", ctypes.c_int * 5)]
 
 
 def load(path: Optional[str] = None):
@@ -68,6 +70,12 @@ def load(path: Optional[str] = None):
         lib.gqa_decode.argtypes = [V, V, V, V, V, V, Z, I, I, I, I, I, F, V]
         lib.gqa_decode_ex.restype = I
         lib.gqa_decode_ex.argtypes = [V, V, V, V, V, V, Z, I, I, I, I, I, F, V, ctypes.POINTER(DecodeOptions)]
+        lib.gqa_decode_append.restype = I
+        lib.gqa_decode_append.argtypes = [V, V, V, V, V, V, V, V, Z, I, I, I, I, I, F, V,
+                                          ctypes.POINTER(DecodeOptions)]
+        lib.gqa_decode_paged.restype = I
+        lib.gqa_decode_paged.argtypes = [V, V, V, V, V, V, V, V, V, Z, I, I, I, I, I, I, I, F, V,
+                                         ctypes.POINTER(DecodeOptions)]
         lib.gqa_decode_select_path.restype = I
         lib.gqa_decode_select_path.argtypes = [I, I, I, I, I]
         lib.gqa_decode_read_flags.restype = I
@@ -120,25 +128,18 @@ def select_path(B: int, H: int, G: int, d: int, Lmax: int) -> int:
     return r
 
 
-def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens: torch.Tensor,
-           out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-           scale: Optional[float] = None, stream: Optional[torch.cuda.Stream] = None,
-           path: int = PATH_AUTO, num_ctas: int = 0) -> torch.Tensor:
-    """One GQA decode step: q [B,H,d] bf16, caches [B,G,Lmax,d] bf16, seq_lens [B] int32 -> out [B,H,d] fp32.
+def _ptr_or_null(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
 
-    Enqueued on ``stream`` (default: the current stream); returns ``out``.
-    ``workspace`` must come from :func:`alloc_workspace` (zero-filled) and may be
-    reused by later calls of any shape that fits it.
-    """
+
+def _prepare(q, seq_lens, out, workspace, scale, G, Lmax):
     dev = q.device
     B, H, d = q.shape
-    Bk, G, Lmax, dk = k_cache.shape
-    if Bk != B or dk != d or tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(seq_lens.shape) != (B,):
-        raise ValueError("shape mismatch between q, k_cache, v_cache and seq_lens")
     _require(q, "q", torch.bfloat16, dev)
-    _require(k_cache, "k_cache", torch.bfloat16, dev)
-    _require(v_cache, "v_cache", torch.bfloat16, dev)
-    _require(seq_lens, "seq_lens", torch.int32, dev)
+    if seq_lens is not None:
+        if tuple(seq_lens.shape) != (B,):
+            raise ValueError("seq_lens must be [B]")
+        _require(seq_lens, "seq_lens", torch.int32, dev)
     if out is None:
         out = torch.empty((B, H, d), dtype=torch.float32, device=dev)
     _require(out, "out", torch.float32, dev)
@@ -147,11 +148,94 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_le
     _require(workspace, "workspace", torch.uint8, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    opts = DecodeOptions(path, num_ctas)
-    _check(load().gqa_decode_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seq_lens.data_ptr(),
+    return out, workspace, float(scale)
+
+
+def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens: Optional[torch.Tensor],
+           out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+           scale: Optional[float] = None, stream: Optional[torch.cuda.Stream] = None,
+           path: int = PATH_AUTO, num_ctas: int = 0, window: int = 0) -> torch.Tensor:
+    """One GQA decode step: q [B,H,d] bf16, caches [B,G,Lmax,d] bf16, seq_lens [B] int32 -> out [B,H,d] fp32.
+
+    ``seq_lens=None`` attends to all Lmax positions (cross-attention); ``window > 0``
+    to the last ``window`` valid positions only.  Enqueued on ``stream`` (default:
+    the current stream); returns ``out``.  ``workspace`` must come from
+    :func:`alloc_workspace` (zero-filled) and may be reused by later calls of any
+    shape that fits it.
+    """
+    dev = q.device
+    B, H, d = q.shape
+    Bk, G, Lmax, dk = k_cache.shape
+    if Bk != B or dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch between q, k_cache and v_cache")
+    _require(k_cache, "k_cache", torch.bfloat16, dev)
+    _require(v_cache, "v_cache", torch.bfloat16, dev)
+    out, workspace, scale = _prepare(q, seq_lens, out, workspace, scale, G, Lmax)
+    opts = DecodeOptions(path, num_ctas, window)
+    _check(load().gqa_decode_ex(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), _ptr_or_null(seq_lens),
                                 out.data_ptr(), workspace.data_ptr(), workspace.numel(), B, H, G, d, Lmax,
-                                float(scale), _stream_handle(stream, dev), ctypes.byref(opts)),
+                                scale, _stream_handle(stream, dev), ctypes.byref(opts)),
            "gqa_decode")
+    return out
+
+
+def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                  v_cache: torch.Tensor, seq_lens: torch.Tensor, out: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+                  stream: Optional[torch.cuda.Stream] = None, num_ctas: int = 0, window: int = 0) -> torch.Tensor:
+    """Decode step with the cache append fused in: writes k_new/v_new [B,G,d] at position
+    seq_lens[b] - 1 of the caches (in place) and attends over seq_lens[b] positions."""
+    dev = q.device
+    B, H, d = q.shape
+    Bk, G, Lmax, dk = k_cache.shape
+    if Bk != B or dk != d or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("shape mismatch between q, k_cache and v_cache")
+    if tuple(k_new.shape) != (B, G, d) or tuple(v_new.shape) != (B, G, d):
+        raise ValueError("k_new and v_new must be [B, G, d]")
+    for t, name in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_new, "k_new"), (v_new, "v_new")):
+        _require(t, name, torch.bfloat16, dev)
+    out, workspace, scale = _prepare(q, seq_lens, out, workspace, scale, G, Lmax)
+    opts = DecodeOptions(0, num_ctas, window)
+    _check(load().gqa_decode_append(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(),
+                                    v_cache.data_ptr(), seq_lens.data_ptr(), out.data_ptr(),
+                                    workspace.data_ptr(), workspace.numel(), B, H, G, d, Lmax, scale,
+                                    _stream_handle(stream, dev), ctypes.byref(opts)),
+           "gqa_decode_append")
+    return out
+
+
+def decode_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
+                 seq_lens: Optional[torch.Tensor], k_new: Optional[torch.Tensor] = None,
+                 v_new: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None, scale: Optional[float] = None,
+                 stream: Optional[torch.cuda.Stream] = None, num_ctas: int = 0, window: int = 0) -> torch.Tensor:
+    """Decode step over a paged cache: pages [num_pages, G, page_size, d] bf16, block_table
+    [B, max_pages] int32 (position t of sequence b is row t % page_size of page
+    block_table[b, t // page_size]).  Optional fused append (k_new, v_new [B, G, d])."""
+    dev = q.device
+    B, H, d = q.shape
+    num_pages, G, page_size, dk = k_pages.shape
+    if dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("shape mismatch between q, k_pages and v_pages")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_pages]")
+    max_pages = block_table.shape[1]
+    _require(k_pages, "k_pages", torch.bfloat16, dev)
+    _require(v_pages, "v_pages", torch.bfloat16, dev)
+    _require(block_table, "block_table", torch.int32, dev)
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        if t is not None:
+            if tuple(t.shape) != (B, G, d):
+                raise ValueError(f"{name} must be [B, G, d]")
+            _require(t, name, torch.bfloat16, dev)
+    out, workspace, scale = _prepare(q, seq_lens, out, workspace, scale, G, max_pages * page_size)
+    opts = DecodeOptions(0, num_ctas, window)
+    _check(load().gqa_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), block_table.data_ptr(),
+                                   _ptr_or_null(seq_lens), _ptr_or_null(k_new), _ptr_or_null(v_new),
+                                   out.data_ptr(), workspace.data_ptr(), workspace.numel(), B, H, G, d,
+                                   page_size, max_pages, num_pages, scale, _stream_handle(stream, dev),
+                                   ctypes.byref(opts)),
+           "gqa_decode_paged")
     return out
 
 
@@ -169,12 +253,13 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     B, H, d = q.shape
     _, G, Lmax, _ = k_cache.shape
     for t, name, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
-                        (v_cache, "v_cache", torch.bfloat16), (seq_lens, "seq_lens", torch.int32),
-                        (out, "out", torch.float32)):
+                        (v_cache, "v_cache", torch.bfloat16), (out, "out", torch.float32)):
         _require(t, name, dt, dev)
+    if seq_lens is not None:
+        _require(seq_lens, "seq_lens", torch.int32, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    _check(load().gqa_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seq_lens.data_ptr(),
+    _check(load().gqa_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), _ptr_or_null(seq_lens),
                                      out.data_ptr(), B, H, G, d, Lmax, float(scale),
                                      _stream_handle(stream, dev)),
            f"gqa_decode_noalloc (scratch limit {NOALLOC_WORKSPACE_BYTES} bytes)")

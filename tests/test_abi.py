@@ -85,7 +85,7 @@ def _decode(lib, ptrs=None, shape=(1, 8, 2, 64, 128), scale=0.125, ws_bytes=None
 
 
 def test_decode_rejects_null_pointers(gqa_lib):
-    for i in range(5):
+    for i in (0, 1, 2, 4):   # q, k_cache, v_cache, out (seq_lens may be NULL: every position valid)
         ptrs = [FAKE] * 6
         ptrs[i] = None
         assert _decode(gqa_lib, ptrs) == 1
@@ -128,6 +128,46 @@ def test_decode_rejects_bad_options(gqa_lib):
     assert _decode(gqa_lib, opts=o) == 1
     o = gqa.DecodeOptions(gqa.PATH_SIMT, 0)                          # H/G = 16 > simt limit
     assert _decode(gqa_lib, shape=(1, 32, 2, 64, 128), opts=o) == 2
+    assert _decode(gqa_lib, opts=gqa.DecodeOptions(0, 0, -1)) == 1   # negative window
+    assert _decode(gqa_lib, opts=gqa.DecodeOptions(gqa.PATH_SIMT, 0, 16)) == 2   # window: tensor-core path only
+
+
+def _append(lib, k_new=FAKE, v_new=FAKE, seq_lens=FAKE, shape=(1, 8, 2, 64, 128)):
+    B, H, G, d, L = shape
+    ws_bytes = _ws(*shape)[1]
+    return lib.gqa_decode_append(FAKE, k_new, v_new, FAKE, FAKE, seq_lens, FAKE, FAKE, ws_bytes, B, H, G, d, L,
+                                 0.125, None, None)
+
+
+def test_append_rejects(gqa_lib):
+    assert _append(gqa_lib, k_new=None) == 1
+    assert _append(gqa_lib, v_new=None) == 1
+    assert _append(gqa_lib, seq_lens=None) == 1      # the append position needs the lengths
+    assert _append(gqa_lib, k_new=FAKE + 8) == 1     # rows are copied in 16-byte units
+    assert _append(gqa_lib, shape=(1, 8, 3, 64, 128)) == 1
+
+
+def _paged(lib, table=FAKE, seq_lens=FAKE, k_new=None, v_new=None, page_size=16, max_pages=8, num_pages=64,
+           G=2, d=64, opts=None):
+    B, H = 1, 8
+    ws_bytes = _ws(B, H, G, d, max(1, max_pages * page_size))[1] if max_pages * page_size <= (1 << 24) else 1 << 30
+    return lib.gqa_decode_paged(FAKE, FAKE, FAKE, table, seq_lens, k_new, v_new, FAKE, FAKE, ws_bytes, B, H, G, d,
+                                page_size, max_pages, num_pages, 0.125, None,
+                                ctypes.byref(opts) if opts is not None else None)
+
+
+def test_paged_rejects(gqa_lib):
+    assert _paged(gqa_lib, table=None) == 1
+    for ps in (0, 8, 24, 100, 1 << 21):              # powers of two from 16 to 2^20 only
+        assert _paged(gqa_lib, page_size=ps) == 1, ps
+    assert _paged(gqa_lib, max_pages=0) == 1
+    assert _paged(gqa_lib, num_pages=0) == 1
+    assert _paged(gqa_lib, k_new=FAKE) == 1          # k_new without v_new
+    assert _paged(gqa_lib, k_new=FAKE, v_new=FAKE, seq_lens=None) == 1
+    assert _paged(gqa_lib, table=FAKE + 2) == 1      # misaligned table
+    assert _paged(gqa_lib, page_size=1 << 20, max_pages=32) == 2         # capacity above 2^24 positions
+    assert _paged(gqa_lib, num_pages=1 << 30, G=2) == 2                  # pool rows above 2^31
+    assert _paged(gqa_lib, opts=gqa.DecodeOptions(gqa.PATH_SIMT, 0)) == 2   # tensor-core path only
 
 
 def test_select_path(gqa_lib):
