@@ -131,7 +131,9 @@ struct RangeEntry {
 // added when O is folded; at kPair, rows m and m + 64 (even and odd positions
 // of dim m) are added at the end of a piece.  One tcgen05.mma then covers
 // 16 positions of every head, part and hi/lo half: 8 instructions per tile.
-template <int D, bool kPair, int N, int NH>
+// kExt: the instance also serves the variants (paged cache, sliding window,
+// fused append); the plain instance carries none of their code or staging.
+template <int D, bool kPair, int N, int NH, bool kExt = false>
 struct TcCfg {
     static_assert(!kPair || D == 64, "the paired layout is for D = 64");
     static constexpr int kColBoxes = (D == 128 || kPair) ? 2 : 1;   // 64-column boxes per tile row
@@ -159,7 +161,9 @@ struct TcCfg {
     // Per K or V slot, beside the tile: the appended token's row as copied from
     // global memory, and where it goes (fused append; unused otherwise).
     static constexpr int kRowBytes = D * 2;
-    static constexpr int kSlotCost = kTileBytes + kRowBytes + (int)sizeof(PatchInfo);
+    static constexpr int kStageRow = kExt ? kRowBytes : 0;
+    static constexpr int kStageInfo = kExt ? (int)sizeof(PatchInfo) : 0;
+    static constexpr int kSlotCost = kTileBytes + kStageRow + kStageInfo;
     // K and V rings: as deep as shared memory allows (at most 8), V one deeper when
     // a single extra tile still fits (V slots are held until the value GEMM is done)
     static constexpr int avail(int QB) { return kSmemLimit - fixed_bytes(QB); }
@@ -188,8 +192,8 @@ struct TcCfg {
     static constexpr int kOffScratch = kOffPrefix + (kMaxBatch + 1) * 4;  // i32 [33]
     static constexpr int kOffRing = (kOffScratch + 33 * 4 + 15) / 16 * 16;  // RangeEntry [kRing]
     static constexpr int kOffStage = kOffRing + kRing * 16;                 // [SK + SV] appended rows
-    static constexpr int kOffPatch = kOffStage + (kSK + kSV) * kRowBytes;   // PatchInfo [SK + SV]
-    static constexpr int kOffBar = kOffPatch + (kSK + kSV) * (int)sizeof(PatchInfo);
+    static constexpr int kOffPatch = kOffStage + (kSK + kSV) * kStageRow;   // PatchInfo [SK + SV]
+    static constexpr int kOffBar = kOffPatch + (kSK + kSV) * kStageInfo;
     // barriers: kfull[SK] kempty[SK] vfull[SV] vempty[SV] qfull[QB] qempty[QB] sfull[2] sfree[2]
     //           pfull[PB] ofull[3] ofree[3] red[2] grp done
     static constexpr int kNumBars = 2 * kSK + 2 * kSV + 2 * kQBuf + 12 + kPBuf + 2 + 2 * kRing;
@@ -326,16 +330,32 @@ __device__ __forceinline__ int checked_page(const DecodeParams &p, int page) {
 // holding no attended position are skipped (their rows are masked).  With an
 // appended row for the tile (row_new), it is copied beside the tile and `info`
 // says where it goes; `info` is written before the arrival that publishes it.
+// The producer's copy of T_b for the sequence its cursor is in: one load per
+// sequence, and none at all for a contiguous cache without window or append.
+struct SeqLenCache {
+    int b = -1, T = 0;
+    __device__ __forceinline__ int get(const DecodeParams &p, int bb) {
+        if (bb != b) {
+            b = bb;
+            T = seq_len_of(p, bb);
+        }
+        return T;
+    }
+};
+
+// The general case (paged cache, window or appended row), kept out of line so
+// that the producer's loop stays small for the plain contiguous cache.
 template <class C>
-__device__ __forceinline__ void issue_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst, uint64_t *bar,
-                                           const Cursor &c, uint64_t pol, const __nv_bfloat16 *row_new,
-                                           uint8_t *stage_row, PatchInfo *info, __nv_bfloat16 *row_dst) {
+__device__ __noinline__ void issue_tile_general(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst,
+                                                uint64_t *bar, const Cursor c, uint64_t pol,
+                                                const __nv_bfloat16 *row_new, uint8_t *stage_row, PatchInfo *info,
+                                                __nv_bfloat16 *row_dst, SeqLenCache *lens_p) {
     constexpr int kPairShift = C::kParts - 1;   // tensor-map rows hold 2 positions in the paired layout
     constexpr int kMaxBoxes = C::kTilePos / 16;   // pages of 16 positions or more
-    const int T = seq_len_of(p, c.b), t0 = window_start(p, T);
-    const int pos0 = ((t0 >> C::kTileShift) + c.j) << C::kTileShift;   // first position of the tile
     const int seg = c.b * p.G + c.g;
     const bool app = row_new != nullptr && c.j + 1 == c.tiles;        // the tile holds position T - 1
+    const int T = lens_p->get(p, c.b), t0 = window_start(p, T);
+    const int pos0 = ((t0 >> C::kTileShift) + c.j) << C::kTileShift;   // first position of the tile
     uint32_t bytes = app ? C::kRowBytes : 0;
     if (app) {
         __nv_bfloat16 *d = nullptr;
@@ -394,11 +414,30 @@ __device__ __forceinline__ void issue_tile(const DecodeParams &p, const CUtensor
     if (app) bulk_load(stage_row, row_new + (size_t)seg * (C::kRowBytes / 2), C::kRowBytes, bar);
 }
 
+template <class C, bool kExt>
+__device__ __forceinline__ void issue_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst, uint64_t *bar,
+                                           const Cursor &c, uint64_t pol, const __nv_bfloat16 *row_new,
+                                           uint8_t *stage_row, PatchInfo *info, __nv_bfloat16 *row_dst,
+                                           SeqLenCache &lens) {
+    if constexpr (kExt) {
+        if (p.block_table || p.window != 0 || (row_new != nullptr && c.j + 1 == c.tiles)) {
+            issue_tile_general<C>(p, tm, dst, bar, c, pol, row_new, stage_row, info, row_dst, &lens);
+            return;
+        }
+        info->on = 0;
+    }
+    // plain contiguous cache: tile j of segment b*G + g is tensor-map rows j*128 ..
+    mbar_arrive_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+    for (int cb = 0; cb < C::kColBoxes; ++cb)
+        tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, c.j * kTile, c.b * p.G + c.g, bar, pol);
+}
+
 // MMA issuer: writes a slot's staged row (the appended token) into its tile,
 // row info.rel, in the 128-byte swizzled layout the TMA produced, and to the
 // cache in global memory; then makes the tile visible to the tensor cores.
 template <class C>
-__device__ __forceinline__ void patch_tile(uint8_t *tile, const uint8_t *stage_row, const PatchInfo &info) {
+__device__ __noinline__ void patch_tile(uint8_t *tile, const uint8_t *stage_row, const PatchInfo info) {
     constexpr bool kPairL = C::kParts == 2;
     const int rel = info.rel;
     const int r = kPairL ? rel >> 1 : rel;   // tensor-map row of the position
@@ -413,11 +452,11 @@ __device__ __forceinline__ void patch_tile(uint8_t *tile, const uint8_t *stage_r
     fence_proxy_async_smem();
 }
 
-template <int D, bool kPair, int N, int NH>
+template <int D, bool kPair, int N, int NH, bool kExt>
 __global__ void __launch_bounds__(224, 1)
     gqa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
-    using C = TcCfg<D, kPair, N, NH>;
+    using C = TcCfg<D, kPair, N, NH, kExt>;
     constexpr int SK = C::kSK, SV = C::kSV, QB = C::kQBuf, NP = C::kParts, PB = C::kPBuf;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -521,6 +560,7 @@ __global__ void __launch_bounds__(224, 1)
             bool k_done = false, v_done = false;
             long long k_u = 0, k_end = 0, k_ub = 0, v_u = 0, v_end = 0;
             Cursor kc{0, 0, 0, 1}, vc{0, 0, 0, 1};
+            SeqLenCache k_lens, v_lens;
             IdlePoll poll;
             while (!v_done) {
                 bool progress = false;
@@ -583,8 +623,8 @@ __global__ void __launch_bounds__(224, 1)
                             ++qissued;
                             if (i == 0) GQA_TRACE_AT(kTrFirstQ, clock64());
                         }
-                        issue_tile<C>(p, &tm_k, smem + C::kOffK + st * C::kTileBytes, &kfull[st], kc, pol_kv,
-                                      p.k_new, kstage + st * C::kRowBytes, &kinfo[st], p.k_dst);
+                        issue_tile<C, kExt>(p, &tm_k, smem + C::kOffK + st * C::kTileBytes, &kfull[st], kc, pol_kv,
+                                      p.k_new, kstage + st * C::kRowBytes, &kinfo[st], p.k_dst, k_lens);
                         if (i == 0) GQA_TRACE_AT(kTrFirstK, clock64());
                         if (i < 128) GQA_TRACE_AT(kTrKIssue + i, clock64());
                         ++kissued;
@@ -610,8 +650,8 @@ __global__ void __launch_bounds__(224, 1)
                 if (v_u < v_end && vissued < kissued) {
                     const int i = vissued, st = i % SV;
                     if (i < SV || mbar_test_wait(&vempty[st], ((i / SV) - 1) & 1)) {
-                        issue_tile<C>(p, &tm_v, smem + C::kOffV + st * C::kTileBytes, &vfull[st], vc, pol_kv,
-                                      p.v_new, vstage + st * C::kRowBytes, &vinfo[st], p.v_dst);
+                        issue_tile<C, kExt>(p, &tm_v, smem + C::kOffV + st * C::kTileBytes, &vfull[st], vc, pol_kv,
+                                      p.v_new, vstage + st * C::kRowBytes, &vinfo[st], p.v_dst, v_lens);
                         ++vissued;
                         ++v_u;
                         cursor_next(vc, prefix, p.B, G);
@@ -679,7 +719,7 @@ __global__ void __launch_bounds__(224, 1)
                     if ((!first || mbar_test_wait(&qfull[qb], (piece / QB) & 1)) && kready &&
                         (s_i < 2 || mbar_test_wait(&sfree[bi], ((s_i >> 1) - 1) & 1))) {
                         tc_fence_after_sync();
-                        if (p.k_new && kinfo[st].on)   // the appended key replaces its row first
+                        if (kExt && p.k_new && kinfo[st].on)   // the appended key replaces its row first
                             patch_tile<C>(smem + C::kOffK + st * C::kTileBytes, kstage + st * C::kRowBytes, kinfo[st]);
                         const uint32_t kb = sbase + C::kOffK + st * C::kTileBytes;
                         const uint32_t qbase = sbase + C::kOffQ + qb * C::kQBytes;
@@ -719,7 +759,7 @@ __global__ void __launch_bounds__(224, 1)
                     if (vready && mbar_test_wait(&pfull[pbi], (pv_i / PB) & 1) &&
                         (pv_i < 3 || mbar_test_wait(&ofree[ob], ((pv_i / 3) - 1) & 1))) {
                         tc_fence_after_sync();
-                        if (p.v_new && vinfo[st].on)   // the appended value replaces its row first
+                        if (kExt && p.v_new && vinfo[st].on)   // the appended value replaces its row first
                             patch_tile<C>(smem + C::kOffV + st * C::kTileBytes, vstage + st * C::kRowBytes, vinfo[st]);
                         const uint32_t vb = sbase + C::kOffV + st * C::kTileBytes;
                         const uint32_t d_o = tmem + C::kOCol + ob * C::kOW;
@@ -809,7 +849,7 @@ __global__ void __launch_bounds__(224, 1)
                 piece_u0 = u;
                 piece_i0 = i;
                 seq_b = seq_len_of(p, cur.b);
-                win_b = window_start(p, seq_b);
+                win_b = kExt ? window_start(p, seq_b) : 0;
 #pragma unroll
                 for (int h = 0; h < NH; ++h) {
                     l_part[h] = 0.f;
@@ -830,7 +870,7 @@ __global__ void __launch_bounds__(224, 1)
             // attended positions of this tile: [lo, hi) relative to its first position
             const int tile_pos0 = ((win_b >> C::kTileShift) + cur.j) << C::kTileShift;
             const int valid_cnt = seq_b - tile_pos0;   // hi, >= 1
-            const int lo = win_b - tile_pos0;          // <= 0 except in a window's first tile
+            const int lo = kExt ? win_b - tile_pos0 : 0;   // > 0 only in a window's first tile
             bool valid[NP];
             float x[NP][NH], red_v[NH];
 #pragma unroll
@@ -1009,11 +1049,11 @@ __global__ void __launch_bounds__(224, 1)
     }
 }
 
-template <int D, bool kPair, int N, int NH>
+template <int D, bool kPair, int N, int NH, bool kExt>
 cudaError_t launch_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const DecodeParams &p,
                         int ctas, cudaStream_t stream) {
-    using C = TcCfg<D, kPair, N, NH>;
-    auto kern = gqa_decode_tc_kernel<D, kPair, N, NH>;
+    using C = TcCfg<D, kPair, N, NH, kExt>;
+    auto kern = gqa_decode_tc_kernel<D, kPair, N, NH, kExt>;
     static unsigned long long attr_set = 0;   // one bit per device; setting twice is harmless
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1026,20 +1066,28 @@ cudaError_t launch_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUte
     return launch_pdl(kern, ctas, C::kThreads, C::kSmemBytes, stream, tk, tv, tq, p);
 }
 
-template <int D, bool kPair>
+template <int D, bool kPair, bool kExt>
 cudaError_t launch_tc_d(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const DecodeParams &p,
                         int ctas, cudaStream_t stream) {
     const int n = p.n;
-    if (n <= 1) return launch_tc_t<D, kPair, 16, 1>(tk, tv, tq, p, ctas, stream);
-    if (n <= 2) return launch_tc_t<D, kPair, 16, 2>(tk, tv, tq, p, ctas, stream);
-    if (n <= 4) return launch_tc_t<D, kPair, 16, 4>(tk, tv, tq, p, ctas, stream);
-    if (n <= 8) return launch_tc_t<D, kPair, 16, 8>(tk, tv, tq, p, ctas, stream);
-    if (n <= 16) return launch_tc_t<D, kPair, 16, 16>(tk, tv, tq, p, ctas, stream);
+    if (n <= 1) return launch_tc_t<D, kPair, 16, 1, kExt>(tk, tv, tq, p, ctas, stream);
+    if (n <= 2) return launch_tc_t<D, kPair, 16, 2, kExt>(tk, tv, tq, p, ctas, stream);
+    if (n <= 4) return launch_tc_t<D, kPair, 16, 4, kExt>(tk, tv, tq, p, ctas, stream);
+    if (n <= 8) return launch_tc_t<D, kPair, 16, 8, kExt>(tk, tv, tq, p, ctas, stream);
+    if (n <= 16) return launch_tc_t<D, kPair, 16, 16, kExt>(tk, tv, tq, p, ctas, stream);
     if constexpr (!kPair) {
-        if (n <= 32) return launch_tc_t<D, kPair, 32, 32>(tk, tv, tq, p, ctas, stream);
-        return launch_tc_t<D, kPair, 64, 64>(tk, tv, tq, p, ctas, stream);
+        if (n <= 32) return launch_tc_t<D, kPair, 32, 32, kExt>(tk, tv, tq, p, ctas, stream);
+        return launch_tc_t<D, kPair, 64, 64, kExt>(tk, tv, tq, p, ctas, stream);
     }
     return cudaErrorNotSupported;
+}
+
+template <bool kExt>
+cudaError_t launch_tc_layout(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
+                             const DecodeParams &p, int D, bool paired, int ctas, cudaStream_t stream) {
+    if (D == 128) return launch_tc_d<128, false, kExt>(tk, tv, tq, p, ctas, stream);
+    if (paired) return launch_tc_d<64, true, kExt>(tk, tv, tq, p, ctas, stream);
+    return launch_tc_d<64, false, kExt>(tk, tv, tq, p, ctas, stream);
 }
 
 }  // namespace
@@ -1052,9 +1100,9 @@ bool tc_paired(int D, int Lmax, int n) { return D == 64 && Lmax % 2 == 0 && n <=
 
 cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
                              const DecodeParams &p, int D, bool paired, int ctas, cudaStream_t stream) {
-    if (D == 128) return launch_tc_d<128, false>(tk, tv, tq, p, ctas, stream);
-    if (paired) return launch_tc_d<64, true>(tk, tv, tq, p, ctas, stream);
-    return launch_tc_d<64, false>(tk, tv, tq, p, ctas, stream);
+    // the variants (paged cache, window, fused append) run the instances built for them
+    if (p.block_table || p.window > 0 || p.k_new) return launch_tc_layout<true>(tk, tv, tq, p, D, paired, ctas, stream);
+    return launch_tc_layout<false>(tk, tv, tq, p, D, paired, ctas, stream);
 }
 
 }  // namespace gqa
