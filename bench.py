@@ -40,7 +40,9 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from kv_cache_decode_06_b300.inputs import CONFIGS, T5XXL_SWEEP_GS, make_decode_inputs  # noqa: E402
+from kv_cache_decode_06_b300.inputs import (  # noqa: E402
+    CONFIGS, T5XXL_SWEEP_GS, make_decode_inputs, make_new_rows, make_paged_layout,
+)
 
 METRIC = "GQA decode KV-cache HBM GB/s (% of B300 peak) and decode steps/s, 1 GPU"
 UNIT = "GB/s"
@@ -145,14 +147,15 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_step(inp, segments, threads=None):
+def cpu_oracle_step(inp, segments, window=0):
     """Time the float64 oracle on the rows of the given (b, g) segments; returns (seconds, kv bytes)."""
     import oracle
     cfg = inp.cfg
     rows = np.array([b * cfg.H + g * cfg.n + h for (b, g) in segments for h in range(cfg.n)], dtype=np.int64)
-    kv = sum(int(inp.seq_lens[b]) for (b, _) in segments) * cfg.d * 2 * 2
+    att = [min(int(inp.seq_lens[b]), window) if window else int(inp.seq_lens[b]) for (b, _) in segments]
+    kv = sum(att) * cfg.d * 2 * 2
     t0 = time.perf_counter()
-    oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale, rows=rows)
+    oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale, rows=rows, window=window)
     return time.perf_counter() - t0, kv
 
 
@@ -197,6 +200,14 @@ def run_reference(args, rank: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+def variant_note(variant, args):
+    return {"contiguous": "contiguous cache [B,G,Lmax,d]",
+            "paged": f"paged cache, {args.page_size}-position pages in random pool order",
+            "append": "fused append of the new token's K/V rows at position seq_lens[b]-1, then decode",
+            "cross": "cross-attention: seq_lens NULL, all Lmax positions valid",
+            "window": f"sliding window of the last {args.window} positions"}[variant]
+
+
 def config_dict(cfg, inp, extra=None):
     d = {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "G": cfg.G, "d": cfg.d, "Lmax": cfg.Lmax,
          "seq_lens": (list(cfg.fixed_seq) if cfg.fixed_seq else f"U[{cfg.seq_lo},{cfg.seq_hi}] seeded"),
@@ -218,6 +229,11 @@ def main() -> None:
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 simt, 2 tcgen05")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--variant", default="contiguous", choices=["contiguous", "paged", "append", "cross", "window"],
+                    help="contiguous cache (default); paged cache (--page-size); fused append of the new "
+                         "token's K/V rows; cross-attention (every position valid); sliding window (--window)")
+    ap.add_argument("--page-size", type=int, default=64)
+    ap.add_argument("--window", type=int, default=1024)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -242,24 +258,55 @@ def main() -> None:
     gqa.load()
 
     cfg = workload(args.workload)
-    inp = make_decode_inputs(cfg, poison_tail=False)
-    q = torch.from_numpy(inp.q).view(torch.bfloat16).to(dev)
-    k = torch.from_numpy(inp.k).view(torch.bfloat16).to(dev)
-    v = torch.from_numpy(inp.v).view(torch.bfloat16).to(dev)
-    sl = torch.from_numpy(inp.seq_lens).to(dev)
+    variant = args.variant
+    if variant == "cross":   # every one of the Lmax positions is valid
+        inp = make_decode_inputs(cfg, poison_tail=False, seq_lens=[cfg.Lmax] * cfg.B)
+    else:
+        inp = make_decode_inputs(cfg, poison_tail=False)
+    window = args.window if variant == "window" else 0
+    attended = np.minimum(inp.seq_lens.astype(np.int64), window) if window else inp.seq_lens.astype(np.int64)
+    kv_bytes = int(attended.sum()) * cfg.G * cfg.d * 2 * 2   # algorithmic K+V bytes of one step
+    stream = torch.cuda.current_stream(dev)
+    scale = float(inp.scale)
+    path = args.path or gqa.select_path(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax)
+    if variant != "contiguous" and path != gqa.PATH_TCGEN05:
+        ap.error("the decode variants run on the tensor-core path")
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    copies = max(3, math.ceil(L2_COPIES_SPAN * l2 / inp.kv_bytes) + 1)
+
+    def to_dev(a, dtype=torch.bfloat16):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(dtype) if dtype == torch.bfloat16 else t).to(dev)
+
+    q = to_dev(inp.q)
+    sl = to_dev(inp.seq_lens, torch.int32)
+    if variant == "paged":
+        kp, vp, table = make_paged_layout(inp, args.page_size)
+        k, v, tbl = to_dev(kp), to_dev(vp), to_dev(table, torch.int32)
+        host_kv = (kp, vp, table)
+    else:
+        k, v, tbl = to_dev(inp.k), to_dev(inp.v), None
+        host_kv = (inp.k, inp.v)
+    if variant == "append":
+        kn_h, vn_h = make_new_rows(cfg)
+        kn, vn = to_dev(kn_h), to_dev(vn_h)
+    copies = max(3, math.ceil(L2_COPIES_SPAN * l2 / kv_bytes) + 1)
     ks = [k] + [k.clone() for _ in range(copies - 1)]
     vs = [v] + [v.clone() for _ in range(copies - 1)]
     out = torch.empty((cfg.B, cfg.H, cfg.d), dtype=torch.float32, device=dev)
     ws = gqa.alloc_workspace(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax, dev)
-    stream = torch.cuda.current_stream(dev)
-    scale = float(inp.scale)
-    path = args.path or gqa.select_path(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax)
+
+    def call(kk, vv):
+        if variant == "paged":
+            gqa.decode_paged(q, kk, vv, tbl, sl, out=out, workspace=ws, scale=scale, stream=stream)
+        elif variant == "append":
+            gqa.decode_append(q, kn, vn, kk, vv, sl, out=out, workspace=ws, scale=scale, stream=stream)
+        else:
+            gqa.decode(q, kk, vv, None if variant == "cross" else sl, out=out, workspace=ws, scale=scale,
+                       stream=stream, path=path, window=window)
 
     def step(i):
         c = i % copies
-        gqa.decode(q, ks[c], vs[c], sl, out=out, workspace=ws, scale=scale, stream=stream, path=path)
+        call(ks[c], vs[c])
 
     for i in range(args.warmup):
         step(i)
@@ -284,26 +331,30 @@ def main() -> None:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = world * inp.kv_bytes * args.steps / (total_ms / 1e3) / 1e9
+    value = world * kv_bytes * args.steps / (total_ms / 1e3) / 1e9
     flags = gqa.read_flags(ws)
     if flags:
         raise RuntimeError(f"decode reported flags 0x{flags:x} during the benchmark")
 
     # ---- end to end through the public API with host buffers (pinned)
-    hq = torch.from_numpy(inp.q).view(torch.bfloat16).pin_memory()
-    hk = torch.from_numpy(inp.k).view(torch.bfloat16).pin_memory()
-    hv = torch.from_numpy(inp.v).view(torch.bfloat16).pin_memory()
-    hsl = torch.from_numpy(inp.seq_lens).pin_memory()
+    def pinned(a, dtype=torch.bfloat16):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(dtype) if dtype == torch.bfloat16 else t).pin_memory()
+
+    host = [(q, pinned(inp.q)), (sl, pinned(inp.seq_lens, torch.int32)), (k, pinned(host_kv[0])),
+            (v, pinned(host_kv[1]))]
+    if tbl is not None:
+        host.append((tbl, pinned(host_kv[2], torch.int32)))
+    if variant == "append":
+        host += [(kn, pinned(kn_h)), (vn, pinned(vn_h))]
     hout = torch.empty((cfg.B, cfg.H, cfg.d), dtype=torch.float32).pin_memory()
-    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hsl.numel() * 4
+    h2d = sum(h.numel() * h.element_size() for _, h in host)
     d2h = hout.numel() * 4
 
     def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        sl.copy_(hsl, non_blocking=True)
-        gqa.decode(q, k, v, sl, out=out, workspace=ws, scale=scale, stream=stream, path=path)
+        for dst, src in host:
+            dst.copy_(src, non_blocking=True)
+        call(k, v)
         hout.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -317,11 +368,11 @@ def main() -> None:
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    e2e_value = world * inp.kv_bytes / (e2e_ms / 1e3) / 1e9
+    e2e_value = world * kv_bytes / (e2e_ms / 1e3) / 1e9
     if world > 1:
         t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_value = world * inp.kv_bytes / (float(t.item()) / 1e3) / 1e9
+        e2e_value = world * kv_bytes / (float(t.item()) / 1e3) / 1e9
 
     if rank != 0:
         if world > 1:
@@ -330,23 +381,24 @@ def main() -> None:
 
     peak, peak_kind = measured_peak()
     kernel = "gqa_decode_tc_kernel" if path == gqa.PATH_TCGEN05 else "gqa_decode_simt_kernel"
-    achieved = inp.kv_bytes / (ms_per_step / 1e3) / 1e9
+    achieved = kv_bytes / (ms_per_step / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(kernel, cfg.name), "kernel": kernel,
+                "traffic": profiled_traffic(kernel, cfg.name) if variant == "contiguous" else None,
+                "kernel": kernel,
                 "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
-                "algorithmic_bytes_per_launch": inp.kv_bytes,
+                "algorithmic_bytes_per_launch": kv_bytes,
                 "frac_of_8TBps_nominal": achieved / 8000.0}
 
     cpu = None
     if not args.no_cpu_baseline:
         import oracle
         segs = all_segments(cfg)
-        cpu_oracle_step(inp, segs[:1])                       # warm: thread pool, page faults
-        t, _ = cpu_oracle_step(inp, segs[:1])
+        cpu_oracle_step(inp, segs[:1], window)               # warm: thread pool, page faults
+        t, _ = cpu_oracle_step(inp, segs[:1], window)
         nseg = int(max(1, min(len(segs), CPU_BASELINE_SECONDS / max(t, 1e-4))))
         total_t, total_b, passes = 0.0, 0, 0
         while total_t < CPU_BASELINE_SECONDS and passes < 1000:
-            t, b = cpu_oracle_step(inp, segs[:nseg])
+            t, b = cpu_oracle_step(inp, segs[:nseg], window)
             total_t += t
             total_b += b
             passes += 1
@@ -360,6 +412,8 @@ def main() -> None:
         "vs_baseline": None, "dtype": "bf16" if path == gqa.PATH_TCGEN05 else "f32", "data": "synthetic",
         "steps_per_s": world * 1e3 / ms_per_step,
         "config": config_dict(cfg, inp, extra={"path": "tcgen05" if path == gqa.PATH_TCGEN05 else "simt",
+                                               "variant": variant_note(variant, args),
+                                               "kv_bytes_per_step": kv_bytes,
                                                "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                                                "cache_copies": copies,
                                                "l2": f"inputs larger than L2: K/V caches held in {copies} copies, "
@@ -370,8 +424,9 @@ def main() -> None:
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps,
-                "what": "H2D of q, k_cache, v_cache (whole buffers), seq_lens from pinned host memory + "
-                        "gqa.decode + D2H of out, per step"},
+                "what": "H2D of every input (q, seq_lens, the whole K/V caches or page pools, the block table "
+                        "and appended rows where used) from pinned host memory + the decode call + D2H of "
+                        "out, per step"},
         "gpu_launches": 2 * args.steps,   # decode kernel + split-combine kernel per step
         "clocks": clk.summary(),
     }

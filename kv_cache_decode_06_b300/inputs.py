@@ -184,3 +184,45 @@ def make_meanpool_input(H: int, G: int, h: int, d_model: int, config_id: int = 0
     rng = np.random.Generator(np.random.PCG64(ss))
     w = rng.standard_normal((outer, H, h * d_model), dtype=np.float32)
     return w if outer > 1 else w.reshape(H, h, d_model)
+
+
+def make_paged_layout(inp: DecodeInputs, page_size: int, seed: int = 0, spare_pages: int = 0):
+    """The contiguous caches of ``inp`` laid out as a page pool, pages in random pool order.
+
+    Returns (k_pages, v_pages, block_table): pools [num_pages, G, page_size, d]
+    (uint16 bf16 bits) and the int32 table [B, ceil(Lmax / page_size)]: position
+    t of sequence b is row t % page_size of page block_table[b, t // page_size].
+    Each sequence gets the pages its length needs; entries past them are -1 and
+    the ``spare_pages`` unused pages, like the rows past a length, hold bf16 NaN.
+    This only moves data: it is an input layout, not part of the method.
+    """
+    cfg = inp.cfg
+    B, G, L, d = inp.k.shape
+    max_pages = -(-L // page_size)
+    need = [-(-int(t) // page_size) for t in inp.seq_lens]
+    num_pages = sum(need) + spare_pages
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(SEED_BASE + cfg.config_id,
+                                                                      spawn_key=(2000 + page_size, seed))))
+    order = rng.permutation(num_pages)
+    kp = np.full((num_pages, G, page_size, d), BF16_QNAN, dtype=np.uint16)
+    vp = np.full((num_pages, G, page_size, d), BF16_QNAN, dtype=np.uint16)
+    table = np.full((B, max_pages), -1, dtype=np.int32)
+    nxt = 0
+    for b in range(B):
+        for p in range(need[b]):
+            page = int(order[nxt])
+            nxt += 1
+            table[b, p] = page
+            lo, hi = p * page_size, min((p + 1) * page_size, L)
+            kp[page, :, :hi - lo] = inp.k[b, :, lo:hi]
+            vp[page, :, :hi - lo] = inp.v[b, :, lo:hi]
+    return kp, vp, table
+
+
+def make_new_rows(cfg: DecodeConfig, seed: int = 0):
+    """The new token's K and V rows [B, G, d] for a fused append (N(0,1) -> bf16)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(SEED_BASE + cfg.config_id,
+                                                                      spawn_key=(3000, seed))))
+    k = f32_to_bf16_bits(rng.standard_normal((cfg.B, cfg.G, cfg.d), dtype=np.float32))
+    v = f32_to_bf16_bits(rng.standard_normal((cfg.B, cfg.G, cfg.d), dtype=np.float32))
+    return k, v

@@ -127,3 +127,17 @@ def test_oracle_tiny_config_runs(oracle_lib):
     inp = make_decode_inputs(CONFIGS["tiny"])
     out = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale, lib=oracle_lib)
     assert np.isfinite(out).all() and out.shape == (1, 8, 64)
+
+
+def test_paged_layout_generator_round_trips(oracle_lib):
+    """The benchmark's paged layout holds the contiguous cache: the oracle's gather gives it back."""
+    from kv_cache_decode_06_b300.inputs import DecodeConfig, make_paged_layout
+    cfg = DecodeConfig("pg", 70, B=3, H=8, G=2, d=16, Lmax=200, seq_lo=1, seq_hi=200)
+    inp = make_decode_inputs(cfg, seq_lens=[200, 17, 1])
+    for ps in (16, 64, 256):
+        kp, vp, table = make_paged_layout(inp, ps, spare_pages=2)
+        assert table.shape == (3, -(-200 // ps)) and kp.shape[0] == int((table >= 0).sum()) + 2
+        kg = oracle.gather_pages(kp, table, inp.seq_lens, cfg.Lmax, lib=oracle_lib)
+        vg = oracle.gather_pages(vp, table, inp.seq_lens, cfg.Lmax, lib=oracle_lib)
+        for b, T in enumerate(inp.seq_lens):
+            assert np.array_equal(kg[b, :, :T], inp.k[b, :, :T]) and np.array_equal(vg[b, :, :T], inp.v[b, :, :T])
