@@ -81,7 +81,8 @@ enum TraceSlot {
     kTrKIssue = 16,       // + i: K copy of tile i issued
     kTrSIssue = 144,      // + i: score GEMM of tile i issued
     kTrPvIssue = 272,     // + i: value GEMM of tile i issued
-    kTrSFull = 400,       // + i: softmax saw S(i)
+    kTrVIssue = 400,      // + i: V(i) copy issued
+    kTrProbe = 940,       // + 4i + {0,1,2,3}: K(i) copy call entered, returned; V(i) the same
     kTrKReady = 528,      // + i: the MMA issuer first sees K(i) landed
     kTrPFull = 656,       // + i: P(i) handed over
     kTrVReady = 784,      // + i: the MMA issuer first sees V(i) landed
@@ -156,7 +157,8 @@ struct TcCfg {
     static constexpr int kSmallBytes = 4 * (kRedF + kLredF + kMF + kAF) + 33 * 4 + (kMaxBatch + 1) * 4 + kRing * 16;
     static constexpr int bar_bytes(int SK, int SV, int QB) { return (2 * SK + 2 * SV + 2 * QB + 14 + 2 + 2 * kRing) * 8 + 16; }
     static constexpr int fixed_bytes(int QB) {
-        return QB * kQBytes + 2 * kPBufBytes + kSmallBytes + bar_bytes(8, 8, QB) + 1024 /* alignment slack */;
+        return QB * kQBytes + 2 * kPBufBytes + kSmallBytes + bar_bytes(8, 8, QB) + kIdBytes + kIdBars * 8 +
+               1024 /* alignment slack */;
     }
     // Per K or V slot, beside the tile: the appended token's row as copied from
     // global memory, and where it goes (fused append; unused otherwise).
@@ -164,6 +166,14 @@ struct TcCfg {
     static constexpr int kStageRow = kExt ? kRowBytes : 0;
     static constexpr int kStageInfo = kExt ? (int)sizeof(PatchInfo) : 0;
     static constexpr int kSlotCost = kTileBytes + kStageRow + kStageInfo;
+    // page-id ring (variant instances, paged cache): kIdRing entries of kIdStride
+    // ints, the page ids of one tile's boxes followed by the sequence length T_b,
+    // written by the page-id warp ahead of the producer
+    static constexpr int kIdRing = 8;
+    static constexpr int kIdMax = kTilePos / 16;        // boxes per tile at the smallest page (16 positions)
+    static constexpr int kIdStride = kIdMax + 4;        // ids, T_b, padding to 16 bytes
+    static constexpr int kIdBytes = kExt ? kIdRing * kIdStride * 4 : 0;
+    static constexpr int kIdBars = kExt ? 2 * kIdRing : 0;
     // K and V rings: as deep as shared memory allows (at most 8), V one deeper when
     // a single extra tile still fits (V slots are held until the value GEMM is done)
     static constexpr int avail(int QB) { return kSmemLimit - fixed_bytes(QB); }
@@ -176,7 +186,7 @@ struct TcCfg {
     // value GEMM three tiles back before reusing one), else two
     static constexpr int layout_bytes(int pbuf) {
         return (kSK + kSV) * kSlotCost + kQBuf * kQBytes + pbuf * kPBufBytes + kSmallBytes + 8 +
-               (2 * kSK + 2 * kSV + 2 * kQBuf + 12 + pbuf + 2 + 2 * kRing) * 8 + 16 + 1024;
+               (2 * kSK + 2 * kSV + 2 * kQBuf + 12 + pbuf + 2 + 2 * kRing + kIdBars) * 8 + 16 + 1024 + kIdBytes;
     }
     static constexpr int kPBuf = layout_bytes(3) <= kSmemLimit ? 3 : 2;
     // layout (offsets from the 1024-aligned base)
@@ -193,16 +203,18 @@ struct TcCfg {
     static constexpr int kOffRing = (kOffScratch + 33 * 4 + 15) / 16 * 16;  // RangeEntry [kRing]
     static constexpr int kOffStage = kOffRing + kRing * 16;                 // [SK + SV] appended rows
     static constexpr int kOffPatch = kOffStage + (kSK + kSV) * kStageRow;   // PatchInfo [SK + SV]
-    static constexpr int kOffBar = kOffPatch + (kSK + kSV) * kStageInfo;
+    static constexpr int kOffIds = kOffPatch + (kSK + kSV) * kStageInfo;     // int [kIdRing][kIdStride]
+    static constexpr int kOffBar = kOffIds + kIdBytes;
     // barriers: kfull[SK] kempty[SK] vfull[SV] vempty[SV] qfull[QB] qempty[QB] sfull[2] sfree[2]
     //           pfull[PB] ofull[3] ofree[3] red[2] grp done
-    static constexpr int kNumBars = 2 * kSK + 2 * kSV + 2 * kQBuf + 12 + kPBuf + 2 + 2 * kRing;
+    static constexpr int kNumBars = 2 * kSK + 2 * kSV + 2 * kQBuf + 12 + kPBuf + 2 + 2 * kRing + kIdBars;
     static constexpr int kOffFlags = kOffBar + kNumBars * 8;     // abort, tmem base
     static constexpr int kSmemBytes = kOffFlags + 16 + 1024;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory layout too large");
     static_assert(NH < 4 || (kOffRed % 16 == 0 && kOffLred % 16 == 0 && kOffM % 16 == 0 && kOffA % 16 == 0),
                   "float4 alignment");
-    static constexpr int kThreads = 224;
+    // warps: producer, score MMA, 4 softmax, value MMA, and (variant instances) the page-id warp
+    static constexpr int kThreads = kExt ? 256 : 224;
     // TMEM: S accumulators [2][part][N] then O accumulators [3][kOW] (O is folded two tiles behind)
     static constexpr int kOCol = 2 * kParts * N;
     static constexpr int kTmemCols = pow2_cols(kOCol + 3 * kOW);
@@ -316,20 +328,14 @@ __device__ __forceinline__ void store_vec(float *dst, const float (&v)[NH]) {
 
 // A page id read from the block table, or (flagged) one past the pool when it
 // is not a page of the pool: the tensor map then fills the rows with zeros.
+__device__ __noinline__ void flag_bad_page(const DecodeParams &p) { atomicOr(p.flags, 0x4u /* GQA_FLAG_BAD_PAGE */); }
+
 __device__ __forceinline__ int checked_page(const DecodeParams &p, int page) {
     if (page >= 0 && page < p.num_pages) return page;
-    atomicOr(p.flags, 0x4u /* GQA_FLAG_BAD_PAGE */);
+    flag_bad_page(p);
     return p.num_pages;
 }
 
-// Producer: copies the K or V tile at cursor c into `dst` (kColBoxes boxes of
-// 128 tensor-map rows x 128 bytes, 128-byte swizzle), completing on `bar`.
-// Contiguous cache: one box per column box at row (j0 + j) * 128 of segment
-// b*G + g.  Paged cache: the tile's positions come from the pages its block-table
-// entries name; pages smaller than a tile are copied one box each, and pages
-// holding no attended position are skipped (their rows are masked).  With an
-// appended row for the tile (row_new), it is copied beside the tile and `info`
-// says where it goes; `info` is written before the arrival that publishes it.
 // The producer's copy of T_b for the sequence its cursor is in: one load per
 // sequence, and none at all for a contiguous cache without window or append.
 struct SeqLenCache {
@@ -343,90 +349,86 @@ struct SeqLenCache {
     }
 };
 
-// The general case (paged cache, window or appended row), kept out of line so
-// that the producer's loop stays small for the plain contiguous cache.
+// First cache position of tile j of a segment of sequence length T.
 template <class C>
-__device__ __noinline__ void issue_tile_general(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst,
-                                                uint64_t *bar, const Cursor c, uint64_t pol,
-                                                const __nv_bfloat16 *row_new, uint8_t *stage_row, PatchInfo *info,
-                                                __nv_bfloat16 *row_dst, SeqLenCache *lens_p) {
+__device__ __forceinline__ int tile_first_pos(const DecodeParams &p, int T, int j) {
+    return ((window_start(p, T) >> C::kTileShift) + j) << C::kTileShift;
+}
+
+// Producer, variant instances: copies the K or V tile at cursor c (sequence
+// length T) into `dst`, completing on `bar`.  Contiguous cache: one box per
+// column box at the tile's first row.  Paged cache (ids: the tile's page ids in
+// shared memory, from the page-id warp): one box per column box from the page
+// holding the tile, or one per page of the tile, skipping pages without an
+// attended position (id -1; their rows are masked).  With an appended row
+// for the tile (row_new: the tile holds position T - 1), the row is copied
+// beside the tile and `info` says where it goes; `info` is written before the
+// arrival that publishes it.
+template <class C>
+__device__ __forceinline__ void produce_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst, uint64_t *bar,
+                                             const Cursor &c, int T, uint64_t pol, const __nv_bfloat16 *row_new,
+                                             uint8_t *stage_row, PatchInfo *info, __nv_bfloat16 *row_dst,
+                                             const int *ids) {
     constexpr int kPairShift = C::kParts - 1;   // tensor-map rows hold 2 positions in the paired layout
-    constexpr int kMaxBoxes = C::kTilePos / 16;   // pages of 16 positions or more
     const int seg = c.b * p.G + c.g;
-    const bool app = row_new != nullptr && c.j + 1 == c.tiles;        // the tile holds position T - 1
-    const int T = lens_p->get(p, c.b), t0 = window_start(p, T);
-    const int pos0 = ((t0 >> C::kTileShift) + c.j) << C::kTileShift;   // first position of the tile
-    uint32_t bytes = app ? C::kRowBytes : 0;
+    const int pos0 = tile_first_pos<C>(p, T, c.j);
+    const int ps = 1 << p.page_shift;
+    const bool app = row_new != nullptr && c.j + 1 == c.tiles;
+    uint32_t bytes = 0;
     if (app) {
         __nv_bfloat16 *d = nullptr;
-        if (!p.block_table) {
-            d = row_dst + ((size_t)seg * p.Lmax + (T - 1)) * C::kRowBytes / 2;
+        if (!ids) {
+            d = row_dst + ((size_t)seg * p.Lmax + (T - 1)) * (C::kRowBytes / 2);
         } else {
-            const int page = __ldg(p.block_table + (size_t)c.b * p.max_pages + ((T - 1) >> p.page_shift));
+            const int page = ids[ps >= C::kTilePos ? 0 : ((T - 1 - pos0) >> p.page_shift)];   // page of T-1
             if (page >= 0 && page < p.num_pages)
-                d = row_dst + (((size_t)page * p.G + c.g) * ((size_t)1 << p.page_shift) +
-                               ((T - 1) & ((1 << p.page_shift) - 1))) * (C::kRowBytes / 2);
+                d = row_dst + (((size_t)page * p.G + c.g) * (size_t)ps + ((T - 1) & (ps - 1))) * (C::kRowBytes / 2);
         }
         info->dst = d;
         info->rel = T - 1 - pos0;
+        bytes = C::kRowBytes;
     }
     info->on = app ? 1 : 0;
-    if (!p.block_table) {
+    if (!ids) {
         mbar_arrive_expect_tx(bar, bytes + C::kTileBytes);
 #pragma unroll
         for (int cb = 0; cb < C::kColBoxes; ++cb)
             tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, pos0 >> kPairShift, seg, bar, pol);
+    } else if (ps >= C::kTilePos) {
+        const int z = checked_page(p, ids[0]) * p.G + c.g;
+        mbar_arrive_expect_tx(bar, bytes + C::kTileBytes);
+#pragma unroll
+        for (int cb = 0; cb < C::kColBoxes; ++cb)
+            tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, (pos0 & (ps - 1)) >> kPairShift, z, bar, pol);
     } else {
-        const int ps = 1 << p.page_shift, prow = ps >> kPairShift;   // tensor-map rows per page
-        const int32_t *trow = p.block_table + (size_t)c.b * p.max_pages;
-        if (prow >= kTile) {
-            const int page = checked_page(p, __ldg(trow + (pos0 >> p.page_shift)));
-            mbar_arrive_expect_tx(bar, bytes + C::kTileBytes);
+        const int prow = ps >> kPairShift;   // tensor-map rows per page
+        // compact loops: this code runs from the instruction cache beside the
+        // other roles' loops, and a long unrolled body costs more in fetch misses
+        // than the loop overhead
+        const int nb = C::kTilePos / ps;
+        int loads = 0;
+#pragma unroll 1
+        for (int k = 0; k < nb; ++k) loads += ids[k] != -1;
+        mbar_arrive_expect_tx(bar, bytes + (uint32_t)(loads * prow * 128 * C::kColBoxes));
+#pragma unroll 1
+        for (int k = 0; k < nb; ++k) {
+            const int id = ids[k];
+            if (id != -1) {
+                const int z = checked_page(p, id) * p.G + c.g;
 #pragma unroll
-            for (int cb = 0; cb < C::kColBoxes; ++cb)
-                tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, (pos0 & (ps - 1)) >> kPairShift,
-                            page * p.G + c.g, bar, pol);
-        } else {
-            const int nb = kTile / prow;   // pages per tile, <= kMaxBoxes
-            int page[kMaxBoxes];
-            int loads = 0;
-#pragma unroll
-            for (int k = 0; k < kMaxBoxes; ++k) {
-                const int pos = pos0 + k * ps;
-                page[k] = -1;
-                if (k < nb && pos < T && pos + ps > t0) {
-                    page[k] = __ldg(trow + (pos >> p.page_shift));
-                    ++loads;
-                }
-            }
-            mbar_arrive_expect_tx(bar, bytes + (uint32_t)(loads * prow * 128 * C::kColBoxes));
-#pragma unroll
-            for (int k = 0; k < kMaxBoxes; ++k) {
-                if (k < nb && page[k] != -1) {
-                    const int z = checked_page(p, page[k]) * p.G + c.g;
-#pragma unroll
-                    for (int cb = 0; cb < C::kColBoxes; ++cb)
-                        tma_load_3d(dst + cb * kBoxBytes + k * prow * 128, tm, cb * kBoxCols, 0, z, bar, pol);
-                }
+                for (int cb = 0; cb < C::kColBoxes; ++cb)
+                    tma_load_3d(dst + cb * kBoxBytes + k * prow * 128, tm, cb * kBoxCols, 0, z, bar, pol);
             }
         }
     }
     if (app) bulk_load(stage_row, row_new + (size_t)seg * (C::kRowBytes / 2), C::kRowBytes, bar);
 }
 
-template <class C, bool kExt>
-__device__ __forceinline__ void issue_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst, uint64_t *bar,
-                                           const Cursor &c, uint64_t pol, const __nv_bfloat16 *row_new,
-                                           uint8_t *stage_row, PatchInfo *info, __nv_bfloat16 *row_dst,
-                                           SeqLenCache &lens) {
-    if constexpr (kExt) {
-        if (p.block_table || p.window != 0 || (row_new != nullptr && c.j + 1 == c.tiles)) {
-            issue_tile_general<C>(p, tm, dst, bar, c, pol, row_new, stage_row, info, row_dst, &lens);
-            return;
-        }
-        info->on = 0;
-    }
-    // plain contiguous cache: tile j of segment b*G + g is tensor-map rows j*128 ..
+// Producer, plain instances: contiguous cache, every valid position: tile j of
+// segment b*G + g is tensor-map rows j*128 .. (no sequence length needed).
+template <class C>
+__device__ __forceinline__ void produce_plain_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst,
+                                                   uint64_t *bar, const Cursor &c, uint64_t pol) {
     mbar_arrive_expect_tx(bar, C::kTileBytes);
 #pragma unroll
     for (int cb = 0; cb < C::kColBoxes; ++cb)
@@ -453,7 +455,7 @@ __device__ __noinline__ void patch_tile(uint8_t *tile, const uint8_t *stage_row,
 }
 
 template <int D, bool kPair, int N, int NH, bool kExt>
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(kExt ? 256 : 224, 1)
     gqa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
     using C = TcCfg<D, kPair, N, NH, kExt>;
@@ -472,6 +474,8 @@ __global__ void __launch_bounds__(224, 1)
     uint64_t *sfull = qempty + QB, *sfree = sfull + 2, *pfull = sfree + 2, *ofull = pfull + PB, *ofree = ofull + 3;
     uint64_t *redbar = ofree + 3, *grp = redbar + 2, *done = grp + 1, *rfull = done + 1, *rempty = rfull + kRing;
     RangeEntry *ring = reinterpret_cast<RangeEntry *>(smem + C::kOffRing);
+    int *ids_ring = reinterpret_cast<int *>(smem + C::kOffIds);
+    uint64_t *idfull = rempty + kRing, *idempty = idfull + C::kIdRing;   // variant instances only
     uint8_t *kstage = smem + C::kOffStage, *vstage = kstage + SK * C::kRowBytes;
     PatchInfo *kinfo = reinterpret_cast<PatchInfo *>(smem + C::kOffPatch), *vinfo = kinfo + SK;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::kOffFlags);
@@ -511,9 +515,16 @@ __global__ void __launch_bounds__(224, 1)
         mbar_init(grp, 128);
         for (int s = 0; s < kRing; ++s) {
             mbar_init(&rfull[s], 1);
-            mbar_init(&rempty[s], 2 + 128);   // both MMA issuers and the 128 softmax threads
+            // both MMA issuers, the 128 softmax threads and (paged cache) the page-id warp
+            mbar_init(&rempty[s], 2 + 128 + ((kExt && p.block_table) ? 1 : 0));
         }
         mbar_init(done, 2);   // one commit from each MMA issuer
+        if constexpr (kExt) {
+            for (int s = 0; s < C::kIdRing; ++s) {
+                mbar_init(&idfull[s], 32);    // every lane of the page-id warp
+                mbar_init(&idempty[s], 1);    // the producer, once V of the tile is issued
+            }
+        }
         *s_abort = 0;
         fence_mbar_init();
     }
@@ -611,7 +622,8 @@ __global__ void __launch_bounds__(224, 1)
                     // probabilities are ready, and a piece's last value GEMM does not wait long
                     if (vissued >= i &&
                         (!first || piece < QB || mbar_test_wait(&qempty[qb], ((piece / QB) - 1) & 1)) &&
-                        (i < SK || mbar_test_wait(&kempty[st], ((i / SK) - 1) & 1))) {
+                        (i < SK || mbar_test_wait(&kempty[st], ((i / SK) - 1) & 1)) &&
+                        (!kExt || !p.block_table || mbar_test_wait(&idfull[i % C::kIdRing], (i / C::kIdRing) & 1))) {
                         if (first) {
                             if (i == 0) GQA_TRACE_AT(kTrPreQ, clock64());
                             mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
@@ -623,8 +635,17 @@ __global__ void __launch_bounds__(224, 1)
                             ++qissued;
                             if (i == 0) GQA_TRACE_AT(kTrFirstQ, clock64());
                         }
-                        issue_tile<C, kExt>(p, &tm_k, smem + C::kOffK + st * C::kTileBytes, &kfull[st], kc, pol_kv,
-                                      p.k_new, kstage + st * C::kRowBytes, &kinfo[st], p.k_dst, k_lens);
+                        uint8_t *kdst = smem + C::kOffK + st * C::kTileBytes;
+                        if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i, clock64());
+                        if constexpr (kExt) {
+                            const int *ids = p.block_table ? ids_ring + (i % C::kIdRing) * C::kIdStride : nullptr;
+                            const int T = ids ? ids[C::kIdMax] : k_lens.get(p, kc.b);
+                            produce_tile<C>(p, &tm_k, kdst, &kfull[st], kc, T, pol_kv, p.k_new,
+                                            kstage + st * C::kRowBytes, &kinfo[st], p.k_dst, ids);
+                        } else {
+                            produce_plain_tile<C>(p, &tm_k, kdst, &kfull[st], kc, pol_kv);
+                        }
+                        if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i + 1, clock64());
                         if (i == 0) GQA_TRACE_AT(kTrFirstK, clock64());
                         if (i < 128) GQA_TRACE_AT(kTrKIssue + i, clock64());
                         ++kissued;
@@ -650,8 +671,19 @@ __global__ void __launch_bounds__(224, 1)
                 if (v_u < v_end && vissued < kissued) {
                     const int i = vissued, st = i % SV;
                     if (i < SV || mbar_test_wait(&vempty[st], ((i / SV) - 1) & 1)) {
-                        issue_tile<C, kExt>(p, &tm_v, smem + C::kOffV + st * C::kTileBytes, &vfull[st], vc, pol_kv,
-                                      p.v_new, vstage + st * C::kRowBytes, &vinfo[st], p.v_dst, v_lens);
+                        uint8_t *vdst = smem + C::kOffV + st * C::kTileBytes;
+                        if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i + 2, clock64());
+                        if constexpr (kExt) {
+                            const int *ids = p.block_table ? ids_ring + (i % C::kIdRing) * C::kIdStride : nullptr;
+                            const int T = ids ? ids[C::kIdMax] : v_lens.get(p, vc.b);
+                            produce_tile<C>(p, &tm_v, vdst, &vfull[st], vc, T, pol_kv, p.v_new,
+                                            vstage + st * C::kRowBytes, &vinfo[st], p.v_dst, ids);
+                            if (ids) mbar_arrive(&idempty[i % C::kIdRing]);   // K and V of the tile are issued
+                        } else {
+                            produce_plain_tile<C>(p, &tm_v, vdst, &vfull[st], vc, pol_kv);
+                        }
+                        if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i + 3, clock64());
+                        if (i < 128) GQA_TRACE_AT(kTrVIssue + i, clock64());
                         ++vissued;
                         ++v_u;
                         cursor_next(vc, prefix, p.B, G);
@@ -859,7 +891,6 @@ __global__ void __launch_bounds__(224, 1)
             // ---- scores of this tile: S^T row r of every part (heads 0..NH-1); part c of row r
             // is position r, or 2r + c in the paired layout
             if (!mbar_wait(&sfull[bi], (i >> 1) & 1, ab)) { ok = false; break; }
-            if (tg == 0 && i < 128) GQA_TRACE_AT(kTrSFull + i, clock64());
             tc_fence_after_sync();
             uint32_t sraw[NP][NH];
 #pragma unroll
@@ -1025,6 +1056,52 @@ __global__ void __launch_bounds__(224, 1)
           }
         }
         if (tg == 0) GQA_TRACE_AT(kTrTiles, i);
+    } else if (kExt && p.block_table) {
+        // ================================================================ page-id warp (paged cache)
+        // Walks the same tiles as the producer, up to kIdRing tiles ahead, and puts
+        // each tile's page ids (lane k: box k) and T_b into the ring.  The block-table
+        // loads thus never sit in the producer's thread, whose barrier arrivals
+        // would otherwise wait for them.
+        int rr = 0, ti = 0, cached_b = -1, T = 0;
+        bool ok = true;
+        while (ok) {
+            const int rslot = rr % kRing;
+            if (!mbar_wait(&rfull[rslot], (rr / kRing) & 1, ab)) break;
+            const RangeEntry range = ring[rslot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rempty[rslot]);
+            ++rr;
+            if (range.chunk == -2) break;
+            Cursor cur = cursor_at(range.ub, prefix, p.B, G);
+            const int ps = 1 << p.page_shift;
+            for (int k = 0; k < range.len; ++k, ++ti) {
+                const int slot = ti % C::kIdRing;
+                if (ti >= C::kIdRing && !mbar_wait(&idempty[slot], ((ti / C::kIdRing) - 1) & 1, ab)) {
+                    ok = false;
+                    break;
+                }
+                if (cur.b != cached_b) {
+                    cached_b = cur.b;
+                    T = seq_len_of(p, cur.b);
+                }
+                const int t0 = window_start(p, T), pos0 = tile_first_pos<C>(p, T, cur.j);
+                const int32_t *trow = p.block_table + (size_t)cur.b * p.max_pages;
+                int *e = ids_ring + slot * C::kIdStride;
+                if (lane < C::kIdMax) {
+                    int id = -1;
+                    if (ps >= C::kTilePos) {
+                        if (lane == 0) id = __ldg(trow + (pos0 >> p.page_shift));
+                    } else {
+                        const int pos = pos0 + lane * ps;
+                        if (pos < pos0 + C::kTilePos && pos < T && pos + ps > t0) id = __ldg(trow + (pos >> p.page_shift));
+                    }
+                    e[lane] = id;
+                }
+                if (lane == 0) e[C::kIdMax] = T;
+                mbar_arrive(&idfull[slot]);   // every lane: its own writes are released
+                cursor_next(cur, prefix, p.B, G);
+            }
+        }
     }
 
     tc_fence_before_sync();

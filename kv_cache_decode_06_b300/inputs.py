@@ -186,12 +186,14 @@ def make_meanpool_input(H: int, G: int, h: int, d_model: int, config_id: int = 0
     return w if outer > 1 else w.reshape(H, h, d_model)
 
 
-def make_paged_layout(inp: DecodeInputs, page_size: int, seed: int = 0, spare_pages: int = 0):
+def make_paged_layout(inp: DecodeInputs, page_size: int, seed: int = 0, spare_pages: int = 0,
+                      shuffle: bool = True):
     """The contiguous caches of ``inp`` laid out as a page pool, pages in random pool order.
 
     Returns (k_pages, v_pages, block_table): pools [num_pages, G, page_size, d]
     (uint16 bf16 bits) and the int32 table [B, ceil(Lmax / page_size)]: position
     t of sequence b is row t % page_size of page block_table[b, t // page_size].
+    With ``shuffle=False`` the pages follow one another in sequence order.
     Each sequence gets the pages its length needs; entries past them are -1 and
     the ``spare_pages`` unused pages, like the rows past a length, hold bf16 NaN.
     This only moves data: it is an input layout, not part of the method.
@@ -203,7 +205,7 @@ def make_paged_layout(inp: DecodeInputs, page_size: int, seed: int = 0, spare_pa
     num_pages = sum(need) + spare_pages
     rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(SEED_BASE + cfg.config_id,
                                                                       spawn_key=(2000 + page_size, seed))))
-    order = rng.permutation(num_pages)
+    order = rng.permutation(num_pages) if shuffle else np.arange(num_pages)
     kp = np.full((num_pages, G, page_size, d), BF16_QNAN, dtype=np.uint16)
     vp = np.full((num_pages, G, page_size, d), BF16_QNAN, dtype=np.uint16)
     table = np.full((B, max_pages), -1, dtype=np.int32)
