@@ -70,7 +70,6 @@ gqa_status device_info(DeviceInfo *out) {
     return out->ok ? GQA_OK : GQA_ERR_DEVICE;
 }
 
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr size_t kHeaderBytes = 256;
 

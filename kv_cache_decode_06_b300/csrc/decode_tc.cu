@@ -132,10 +132,15 @@ struct RangeEntry {
 // added when O is folded; at kPair, rows m and m + 64 (even and odd positions
 // of dim m) are added at the end of a piece.  One tcgen05.mma then covers
 // 16 positions of every head, part and hi/lo half: 8 instructions per tile.
-// kExt: the instance also serves the variants (paged cache, sliding window,
-// fused append); the plain instance carries none of their code or staging.
-template <int D, bool kPair, int N, int NH, bool kExt = false>
+// kVar: 0 = plain instance (contiguous cache, every valid position); 1 = the
+// contiguous-cache variants (sliding window, fused append); 2 = paged cache (with
+// or without window and append).  Each instance carries only its own code and
+// staging: the producer's loop must stay short (instruction fetch misses on a
+// long loop cost it hundreds of nanoseconds per tile).
+template <int D, bool kPair, int N, int NH, int kVar = 0>
 struct TcCfg {
+    static constexpr bool kExt = kVar != 0;
+    static constexpr bool kPaged = kVar == 2;
     static_assert(!kPair || D == 64, "the paired layout is for D = 64");
     static constexpr int kColBoxes = (D == 128 || kPair) ? 2 : 1;   // 64-column boxes per tile row
     static constexpr int kQBoxes = D / kBoxCols;                     // 64-column boxes per q row
@@ -172,8 +177,8 @@ struct TcCfg {
     static constexpr int kIdRing = 8;
     static constexpr int kIdMax = kTilePos / 16;        // boxes per tile at the smallest page (16 positions)
     static constexpr int kIdStride = kIdMax + 4;        // ids, T_b, padding to 16 bytes
-    static constexpr int kIdBytes = kExt ? kIdRing * kIdStride * 4 : 0;
-    static constexpr int kIdBars = kExt ? 2 * kIdRing : 0;
+    static constexpr int kIdBytes = kPaged ? kIdRing * kIdStride * 4 : 0;
+    static constexpr int kIdBars = kPaged ? 2 * kIdRing : 0;
     // K and V rings: as deep as shared memory allows (at most 8), V one deeper when
     // a single extra tile still fits (V slots are held until the value GEMM is done)
     static constexpr int avail(int QB) { return kSmemLimit - fixed_bytes(QB); }
@@ -214,7 +219,7 @@ struct TcCfg {
     static_assert(NH < 4 || (kOffRed % 16 == 0 && kOffLred % 16 == 0 && kOffM % 16 == 0 && kOffA % 16 == 0),
                   "float4 alignment");
     // warps: producer, score MMA, 4 softmax, value MMA, and (variant instances) the page-id warp
-    static constexpr int kThreads = kExt ? 256 : 224;
+    static constexpr int kThreads = kPaged ? 256 : 224;
     // TMEM: S accumulators [2][part][N] then O accumulators [3][kOW] (O is folded two tiles behind)
     static constexpr int kOCol = 2 * kParts * N;
     static constexpr int kTmemCols = pow2_cols(kOCol + 3 * kOW);
@@ -365,7 +370,7 @@ __device__ __forceinline__ int tile_first_pos(const DecodeParams &p, int T, int 
 // beside the tile and `info` says where it goes; `info` is written before the
 // arrival that publishes it.
 template <class C>
-__device__ __forceinline__ void produce_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst, uint64_t *bar,
+__device__ __noinline__ void produce_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst, uint64_t *bar,
                                              const Cursor &c, int T, uint64_t pol, const __nv_bfloat16 *row_new,
                                              uint8_t *stage_row, PatchInfo *info, __nv_bfloat16 *row_dst,
                                              const int *ids) {
@@ -426,13 +431,62 @@ __device__ __forceinline__ void produce_tile(const DecodeParams &p, const CUtens
 
 // Producer, plain instances: contiguous cache, every valid position: tile j of
 // segment b*G + g is tensor-map rows j*128 .. (no sequence length needed).
+// (j0: the segment's first tile, nonzero only with a window)
 template <class C>
 __device__ __forceinline__ void produce_plain_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst,
-                                                   uint64_t *bar, const Cursor &c, uint64_t pol) {
+                                                   uint64_t *bar, const Cursor &c, uint64_t pol, int j0 = 0) {
     mbar_arrive_expect_tx(bar, C::kTileBytes);
 #pragma unroll
     for (int cb = 0; cb < C::kColBoxes; ++cb)
-        tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, c.j * kTile, c.b * p.G + c.g, bar, pol);
+        tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, (j0 + c.j) * kTile, c.b * p.G + c.g, bar, pol);
+}
+
+// Producer, variant instances: tiles without an appended row stay on a short
+// inline path (contiguous: the plain copy at the window's offset; paged: one box
+// per column box from the page holding the tile, or one per page of the tile);
+// the tile holding an appended row goes to produce_tile, out of line.  Short hot code matters here: the long general
+// path costs several hundred nanoseconds per call in instruction fetches.
+template <class C>
+__device__ __forceinline__ void produce_variant_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst,
+                                                     uint64_t *bar, const Cursor &c, int T, uint64_t pol,
+                                                     const __nv_bfloat16 *row_new, uint8_t *stage_row,
+                                                     PatchInfo *info, __nv_bfloat16 *row_dst, const int *ids) {
+    const bool app = row_new != nullptr && c.j + 1 == c.tiles;
+    if (!app) {
+        if (row_new) info->on = 0;
+        if constexpr (!C::kPaged) {
+            produce_plain_tile<C>(p, tm, dst, bar, c, pol, window_start(p, T) >> C::kTileShift);
+            return;
+        }
+        constexpr int kPairShift = C::kParts - 1;
+        const int ps = 1 << p.page_shift;
+        if (C::kTilePos <= ps) {
+            const int pos0 = tile_first_pos<C>(p, T, c.j);
+            const int z = checked_page(p, ids[0]) * p.G + c.g;
+            mbar_arrive_expect_tx(bar, C::kTileBytes);
+#pragma unroll
+            for (int cb = 0; cb < C::kColBoxes; ++cb)
+                tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, (pos0 & (ps - 1)) >> kPairShift, z, bar, pol);
+        } else {
+            const int prow = ps >> kPairShift, nb = C::kTilePos / ps;
+            int loads = 0;
+#pragma unroll 1
+            for (int k = 0; k < nb; ++k) loads += ids[k] != -1;
+            mbar_arrive_expect_tx(bar, (uint32_t)(loads * prow * 128 * C::kColBoxes));
+#pragma unroll 1
+            for (int k = 0; k < nb; ++k) {
+                const int id = ids[k];
+                if (id != -1) {
+                    const int z = checked_page(p, id) * p.G + c.g;
+#pragma unroll
+                    for (int cb = 0; cb < C::kColBoxes; ++cb)
+                        tma_load_3d(dst + cb * kBoxBytes + k * prow * 128, tm, cb * kBoxCols, 0, z, bar, pol);
+                }
+            }
+        }
+        return;
+    }
+    produce_tile<C>(p, tm, dst, bar, c, T, pol, row_new, stage_row, info, row_dst, ids);
 }
 
 // MMA issuer: writes a slot's staged row (the appended token) into its tile,
@@ -454,11 +508,12 @@ __device__ __noinline__ void patch_tile(uint8_t *tile, const uint8_t *stage_row,
     fence_proxy_async_smem();
 }
 
-template <int D, bool kPair, int N, int NH, bool kExt>
-__global__ void __launch_bounds__(kExt ? 256 : 224, 1)
+template <int D, bool kPair, int N, int NH, int kVar>
+__global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
     gqa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
-    using C = TcCfg<D, kPair, N, NH, kExt>;
+    using C = TcCfg<D, kPair, N, NH, kVar>;
+    constexpr bool kExt = C::kExt, kPaged = C::kPaged;
     constexpr int SK = C::kSK, SV = C::kSV, QB = C::kQBuf, NP = C::kParts, PB = C::kPBuf;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -516,10 +571,10 @@ __global__ void __launch_bounds__(kExt ? 256 : 224, 1)
         for (int s = 0; s < kRing; ++s) {
             mbar_init(&rfull[s], 1);
             // both MMA issuers, the 128 softmax threads and (paged cache) the page-id warp
-            mbar_init(&rempty[s], 2 + 128 + ((kExt && p.block_table) ? 1 : 0));
+            mbar_init(&rempty[s], 2 + 128 + (kPaged ? 1 : 0));
         }
         mbar_init(done, 2);   // one commit from each MMA issuer
-        if constexpr (kExt) {
+        if constexpr (kPaged) {
             for (int s = 0; s < C::kIdRing; ++s) {
                 mbar_init(&idfull[s], 32);    // every lane of the page-id warp
                 mbar_init(&idempty[s], 1);    // the producer, once V of the tile is issued
@@ -623,7 +678,7 @@ __global__ void __launch_bounds__(kExt ? 256 : 224, 1)
                     if (vissued >= i &&
                         (!first || piece < QB || mbar_test_wait(&qempty[qb], ((piece / QB) - 1) & 1)) &&
                         (i < SK || mbar_test_wait(&kempty[st], ((i / SK) - 1) & 1)) &&
-                        (!kExt || !p.block_table || mbar_test_wait(&idfull[i % C::kIdRing], (i / C::kIdRing) & 1))) {
+                        (!kPaged || mbar_test_wait(&idfull[i % C::kIdRing], (i / C::kIdRing) & 1))) {
                         if (first) {
                             if (i == 0) GQA_TRACE_AT(kTrPreQ, clock64());
                             mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
@@ -638,10 +693,10 @@ __global__ void __launch_bounds__(kExt ? 256 : 224, 1)
                         uint8_t *kdst = smem + C::kOffK + st * C::kTileBytes;
                         if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i, clock64());
                         if constexpr (kExt) {
-                            const int *ids = p.block_table ? ids_ring + (i % C::kIdRing) * C::kIdStride : nullptr;
-                            const int T = ids ? ids[C::kIdMax] : k_lens.get(p, kc.b);
-                            produce_tile<C>(p, &tm_k, kdst, &kfull[st], kc, T, pol_kv, p.k_new,
-                                            kstage + st * C::kRowBytes, &kinfo[st], p.k_dst, ids);
+                            const int *ids = kPaged ? ids_ring + (i % C::kIdRing) * C::kIdStride : nullptr;
+                            const int T = kPaged ? ids[C::kIdMax] : k_lens.get(p, kc.b);
+                            produce_variant_tile<C>(p, &tm_k, kdst, &kfull[st], kc, T, pol_kv, p.k_new,
+                                                    kstage + st * C::kRowBytes, &kinfo[st], p.k_dst, ids);
                         } else {
                             produce_plain_tile<C>(p, &tm_k, kdst, &kfull[st], kc, pol_kv);
                         }
@@ -674,11 +729,11 @@ __global__ void __launch_bounds__(kExt ? 256 : 224, 1)
                         uint8_t *vdst = smem + C::kOffV + st * C::kTileBytes;
                         if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i + 2, clock64());
                         if constexpr (kExt) {
-                            const int *ids = p.block_table ? ids_ring + (i % C::kIdRing) * C::kIdStride : nullptr;
-                            const int T = ids ? ids[C::kIdMax] : v_lens.get(p, vc.b);
-                            produce_tile<C>(p, &tm_v, vdst, &vfull[st], vc, T, pol_kv, p.v_new,
-                                            vstage + st * C::kRowBytes, &vinfo[st], p.v_dst, ids);
-                            if (ids) mbar_arrive(&idempty[i % C::kIdRing]);   // K and V of the tile are issued
+                            const int *ids = kPaged ? ids_ring + (i % C::kIdRing) * C::kIdStride : nullptr;
+                            const int T = kPaged ? ids[C::kIdMax] : v_lens.get(p, vc.b);
+                            produce_variant_tile<C>(p, &tm_v, vdst, &vfull[st], vc, T, pol_kv, p.v_new,
+                                                    vstage + st * C::kRowBytes, &vinfo[st], p.v_dst, ids);
+                            if constexpr (kPaged) mbar_arrive(&idempty[i % C::kIdRing]);   // K and V of the tile are issued
                         } else {
                             produce_plain_tile<C>(p, &tm_v, vdst, &vfull[st], vc, pol_kv);
                         }
@@ -1056,7 +1111,7 @@ __global__ void __launch_bounds__(kExt ? 256 : 224, 1)
           }
         }
         if (tg == 0) GQA_TRACE_AT(kTrTiles, i);
-    } else if (kExt && p.block_table) {
+    } else if (kPaged) {
         // ================================================================ page-id warp (paged cache)
         // Walks the same tiles as the producer, up to kIdRing tiles ahead, and puts
         // each tile's page ids (lane k: box k) and T_b into the ring.  The block-table
@@ -1126,11 +1181,11 @@ __global__ void __launch_bounds__(kExt ? 256 : 224, 1)
     }
 }
 
-template <int D, bool kPair, int N, int NH, bool kExt>
+template <int D, bool kPair, int N, int NH, int kVar>
 cudaError_t launch_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const DecodeParams &p,
                         int ctas, cudaStream_t stream) {
-    using C = TcCfg<D, kPair, N, NH, kExt>;
-    auto kern = gqa_decode_tc_kernel<D, kPair, N, NH, kExt>;
+    using C = TcCfg<D, kPair, N, NH, kVar>;
+    auto kern = gqa_decode_tc_kernel<D, kPair, N, NH, kVar>;
     static unsigned long long attr_set = 0;   // one bit per device; setting twice is harmless
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1143,28 +1198,28 @@ cudaError_t launch_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUte
     return launch_pdl(kern, ctas, C::kThreads, C::kSmemBytes, stream, tk, tv, tq, p);
 }
 
-template <int D, bool kPair, bool kExt>
+template <int D, bool kPair, int kVar>
 cudaError_t launch_tc_d(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const DecodeParams &p,
                         int ctas, cudaStream_t stream) {
     const int n = p.n;
-    if (n <= 1) return launch_tc_t<D, kPair, 16, 1, kExt>(tk, tv, tq, p, ctas, stream);
-    if (n <= 2) return launch_tc_t<D, kPair, 16, 2, kExt>(tk, tv, tq, p, ctas, stream);
-    if (n <= 4) return launch_tc_t<D, kPair, 16, 4, kExt>(tk, tv, tq, p, ctas, stream);
-    if (n <= 8) return launch_tc_t<D, kPair, 16, 8, kExt>(tk, tv, tq, p, ctas, stream);
-    if (n <= 16) return launch_tc_t<D, kPair, 16, 16, kExt>(tk, tv, tq, p, ctas, stream);
+    if (n <= 1) return launch_tc_t<D, kPair, 16, 1, kVar>(tk, tv, tq, p, ctas, stream);
+    if (n <= 2) return launch_tc_t<D, kPair, 16, 2, kVar>(tk, tv, tq, p, ctas, stream);
+    if (n <= 4) return launch_tc_t<D, kPair, 16, 4, kVar>(tk, tv, tq, p, ctas, stream);
+    if (n <= 8) return launch_tc_t<D, kPair, 16, 8, kVar>(tk, tv, tq, p, ctas, stream);
+    if (n <= 16) return launch_tc_t<D, kPair, 16, 16, kVar>(tk, tv, tq, p, ctas, stream);
     if constexpr (!kPair) {
-        if (n <= 32) return launch_tc_t<D, kPair, 32, 32, kExt>(tk, tv, tq, p, ctas, stream);
-        return launch_tc_t<D, kPair, 64, 64, kExt>(tk, tv, tq, p, ctas, stream);
+        if (n <= 32) return launch_tc_t<D, kPair, 32, 32, kVar>(tk, tv, tq, p, ctas, stream);
+        return launch_tc_t<D, kPair, 64, 64, kVar>(tk, tv, tq, p, ctas, stream);
     }
     return cudaErrorNotSupported;
 }
 
-template <bool kExt>
+template <int kVar>
 cudaError_t launch_tc_layout(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
                              const DecodeParams &p, int D, bool paired, int ctas, cudaStream_t stream) {
-    if (D == 128) return launch_tc_d<128, false, kExt>(tk, tv, tq, p, ctas, stream);
-    if (paired) return launch_tc_d<64, true, kExt>(tk, tv, tq, p, ctas, stream);
-    return launch_tc_d<64, false, kExt>(tk, tv, tq, p, ctas, stream);
+    if (D == 128) return launch_tc_d<128, false, kVar>(tk, tv, tq, p, ctas, stream);
+    if (paired) return launch_tc_d<64, true, kVar>(tk, tv, tq, p, ctas, stream);
+    return launch_tc_d<64, false, kVar>(tk, tv, tq, p, ctas, stream);
 }
 
 }  // namespace
@@ -1177,9 +1232,10 @@ bool tc_paired(int D, int Lmax, int n) { return D == 64 && Lmax % 2 == 0 && n <=
 
 cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
                              const DecodeParams &p, int D, bool paired, int ctas, cudaStream_t stream) {
-    // the variants (paged cache, window, fused append) run the instances built for them
-    if (p.block_table || p.window > 0 || p.k_new) return launch_tc_layout<true>(tk, tv, tq, p, D, paired, ctas, stream);
-    return launch_tc_layout<false>(tk, tv, tq, p, D, paired, ctas, stream);
+    // the variants run the instances built for them
+    if (p.block_table) return launch_tc_layout<2>(tk, tv, tq, p, D, paired, ctas, stream);
+    if (p.window > 0 || p.k_new) return launch_tc_layout<1>(tk, tv, tq, p, D, paired, ctas, stream);
+    return launch_tc_layout<0>(tk, tv, tq, p, D, paired, ctas, stream);
 }
 
 }  // namespace gqa
