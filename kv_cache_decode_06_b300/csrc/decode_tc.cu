@@ -272,15 +272,17 @@ __device__ __forceinline__ void butterfly_store(const float (&v)[NH], int lane, 
 
 // out[h] = op(src[0*NH + h], src[1*NH + h], src[2*NH + h], src[3*NH + h]) for the
 // four warps' per-head values, read as float4 where NH allows.
-template <int NH, bool kMax>
+// kStride: distance between the warps' rows (NH, or the full head count when
+// reducing a chunk of heads).
+template <int NH, bool kMax, int kStride = NH>
 __device__ __forceinline__ void reduce4(const float *src, float (&out)[NH]) {
     if constexpr (NH >= 4) {
 #pragma unroll
         for (int h = 0; h < NH; h += 4) {
             const float4 a = *reinterpret_cast<const float4 *>(src + h);
-            const float4 b = *reinterpret_cast<const float4 *>(src + NH + h);
-            const float4 c = *reinterpret_cast<const float4 *>(src + 2 * NH + h);
-            const float4 d = *reinterpret_cast<const float4 *>(src + 3 * NH + h);
+            const float4 b = *reinterpret_cast<const float4 *>(src + kStride + h);
+            const float4 c = *reinterpret_cast<const float4 *>(src + 2 * kStride + h);
+            const float4 d = *reinterpret_cast<const float4 *>(src + 3 * kStride + h);
             if (kMax) {
                 out[h] = fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x));
                 out[h + 1] = fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y));
@@ -296,7 +298,7 @@ __device__ __forceinline__ void reduce4(const float *src, float (&out)[NH]) {
     } else {
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-            const float a = src[h], b = src[NH + h], c = src[2 * NH + h], d = src[3 * NH + h];
+            const float a = src[h], b = src[kStride + h], c = src[2 * kStride + h], d = src[3 * kStride + h];
             out[h] = kMax ? fmaxf(fmaxf(a, b), fmaxf(c, d)) : (a + b) + (c + d);
         }
     }
@@ -885,6 +887,12 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
         const int odim = kPair ? (r & 63) : (D == 128) ? r : q4 * 16 + lane;
         const bool has_dim = kPair ? (r < 64) : (D == 128) || lane < 16;
         const uint32_t o_part = (kPair && r >= 64) ? 2 * C::kNPV : 0;   // this row's (part) column block
+        // heads are handled in chunks of CH: at 64 heads per group the per-head
+        // arrays of a whole tile would not fit in registers (up to 32 they do, and a
+        // single pass over the scores is cheaper)
+        constexpr int CH = NH <= 32 ? NH : 16;
+        constexpr int NCH = NH / CH;
+        constexpr int kHalveCH = ilog2(CH) < 5 ? ilog2(CH) : 5;
         zero_empty_sequences<D>(p, prefix, P, tg, 128);
         GroupSync gsync{grp, 0};
         float l_part[NH], acc[NH];
@@ -897,20 +905,20 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
             const int ob = t % 3;
             if (!mbar_wait(&ofull[ob], (t / 3) & 1, ab)) return false;
             tc_fence_after_sync();
-            float al[NH];
-            load_vec<NH>(alpha_s + (t % 4) * NH, al);
-            // hi and lo columns, at most 16 heads at a time (bounds the registers at NH = 64)
-            constexpr int CH = NH < 16 ? NH : 16;
+            // hi and lo columns and the rescale factors, at most 16 heads at a time
+            // (bounds the registers at NH = 64)
             const uint32_t oc = tmem + lane_off + C::kOCol + ob * C::kOW + o_part;
 #pragma unroll
             for (int h0 = 0; h0 < NH; h0 += CH) {
                 uint32_t ohi[CH], olo[CH];
+                float al[CH];
+                load_vec<CH>(alpha_s + (t % 4) * NH + h0, al);
                 tmem_ld_32x32b<CH>(oc + h0, ohi);
                 tmem_ld_32x32b<CH>(oc + C::kNPV + h0, olo);
                 tmem_wait_ld();
 #pragma unroll
                 for (int h = 0; h < CH; ++h)
-                    acc[h0 + h] = fmaf(acc[h0 + h], al[h0 + h], __uint_as_float(ohi[h]) + __uint_as_float(olo[h]));
+                    acc[h0 + h] = fmaf(acc[h0 + h], al[h], __uint_as_float(ohi[h]) + __uint_as_float(olo[h]));
             }
             tc_fence_before_sync();
             mbar_arrive(&ofree[ob]);
@@ -943,6 +951,8 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                     acc[h] = 0.f;
                 }
             }
+            const int pbi = i % PB;   // this tile's P buffer
+            if constexpr (NCH == 1) {
             // ---- scores of this tile: S^T row r of every part (heads 0..NH-1); part c of row r
             // is position r, or 2r + c in the paired layout
             if (!mbar_wait(&sfull[bi], (i >> 1) & 1, ab)) { ok = false; break; }
@@ -1024,7 +1034,6 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
             // ---- probabilities to shared memory as bf16 hi + lo (K-major, 128-byte swizzle):
             // row (c * 2 + hi/lo) * kNPV + h of the value GEMM's B operand, position r;
             // P buffer i % PB last held P(i - PB): its value GEMM must be done with it
-            const int pbi = i % PB;
             if (i >= PB && !mbar_wait(&ofull[(i - PB) % 3], ((i - PB) / 3) & 1, ab)) { ok = false; break; }
 #pragma unroll
             for (int c = 0; c < NP; ++c) {
@@ -1042,6 +1051,108 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         *reinterpret_cast<__nv_bfloat16 *>(plo + off) = lo;
                     }
                 }
+            }
+            } else {
+            // ---- scores of this tile, CH heads at a time: pass 1 takes the tile maxima
+            // (one barrier for all heads), pass 2 reloads the scores from TMEM and turns
+            // them into probabilities; the S buffer is released after pass 2
+            if (!mbar_wait(&sfull[bi], (i >> 1) & 1, ab)) { ok = false; break; }
+            tc_fence_after_sync();
+            const int tile_pos0 = ((win_b >> C::kTileShift) + cur.j) << C::kTileShift;
+            const int valid_cnt = seq_b - tile_pos0;   // hi, >= 1
+            const int lo = kExt ? win_b - tile_pos0 : 0;   // > 0 only in a window's first tile
+            bool valid[NP];
+#pragma unroll
+            for (int c = 0; c < NP; ++c) {
+                const int pos = kPair ? 2 * r + c : r;
+                valid[c] = pos < valid_cnt && pos >= lo;
+            }
+#pragma unroll
+            for (int h0 = 0; h0 < NH; h0 += CH) {
+                uint32_t sr[NP][CH];
+#pragma unroll
+                for (int c = 0; c < NP; ++c) tmem_ld_32x32b<CH>(tmem + lane_off + (bi * NP + c) * N + h0, sr[c]);
+                tmem_wait_ld();
+                float rv[CH];
+#pragma unroll
+                for (int h = 0; h < CH; ++h) {
+                    rv[h] = -INFINITY;
+#pragma unroll
+                    for (int c = 0; c < NP; ++c)
+                        rv[h] = fmaxf(rv[h], valid[c] ? __uint_as_float(sr[c][h]) * p.scale_log2 : -INFINITY);
+                }
+                butterfly_reduce<CH, true>(rv, lane);
+                butterfly_store<CH, kHalveCH>(rv, lane, red + (bi * 4 + q4) * NH + h0);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&redbar[bi]);
+            if (!mbar_wait(&redbar[bi], (i >> 1) & 1, ab)) { ok = false; break; }
+            // P buffer i % PB last held P(i - PB): its value GEMM must be done with it
+            if (i >= PB && !mbar_wait(&ofull[(i - PB) % 3], ((i - PB) / 3) & 1, ab)) { ok = false; break; }
+#pragma unroll
+            for (int h0 = 0; h0 < NH; h0 += CH) {
+                float m_new[CH], alpha[CH];
+                reduce4<CH, true, NH>(red + bi * 4 * NH + h0, m_new);   // tile maximum per head
+                if (i == piece_i0) {
+#pragma unroll
+                    for (int h = 0; h < CH; ++h) alpha[h] = 0.f;      // nothing to rescale yet
+                } else {
+                    float m_old[CH];
+                    load_vec<CH>(mrun_s + ((i + 2) % 3) * NH + h0, m_old);   // state after tile i-1
+#pragma unroll
+                    for (int h = 0; h < CH; ++h) {
+                        m_new[h] = fmaxf(m_old[h], m_new[h]);
+                        alpha[h] = ex2(m_old[h] - m_new[h]);
+                    }
+                }
+                uint32_t sr[NP][CH];
+#pragma unroll
+                for (int c = 0; c < NP; ++c) tmem_ld_32x32b<CH>(tmem + lane_off + (bi * NP + c) * N + h0, sr[c]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int h = 0; h < CH; ++h) {
+                    float sx = 0.f;
+#pragma unroll
+                    for (int c = 0; c < NP; ++c) {
+                        const float xv = valid[c] ? ex2(__uint_as_float(sr[c][h]) * p.scale_log2 - m_new[h]) : 0.f;
+                        sx += xv;
+                        if (h0 + h < n) {
+                            uint8_t *phi = smem + C::kOffP + pbi * C::kPBufBytes + (r >> 6) * (C::kOW * 128) +
+                                           (c * 2) * (C::kNPV * 128);
+                            const int col = r & 63, hh = h0 + h;
+                            const int off = hh * 128 + ((((col >> 3) ^ (hh & 7))) << 4) + (col & 7) * 2;
+                            const __nv_bfloat16 hi = __float2bfloat16_rn(xv);
+                            const __nv_bfloat16 lo2 = __float2bfloat16_rn(xv - __bfloat162float(hi));
+                            *reinterpret_cast<__nv_bfloat16 *>(phi + off) = hi;
+                            *reinterpret_cast<__nv_bfloat16 *>(phi + C::kNPV * 128 + off) = lo2;
+                        }
+                    }
+                    l_part[h0 + h] = fmaf(l_part[h0 + h], alpha[h], sx);
+                }
+                if (tg == 0) {
+                    store_vec<CH>(mrun_s + (i % 3) * NH + h0, m_new);
+                    store_vec<CH>(alpha_s + (i % 4) * NH + h0, alpha);
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&sfree[bi]);
+            // ---- clear V rows outside [lo, hi): past the end of a sequence, before a window's
+            // start, or in pages not copied; they may hold anything, NaN included
+            if (valid_cnt < C::kTilePos || lo > 0) {
+                const int sv = i % SV;
+                if (!mbar_wait(&vfull[sv], (i / SV) & 1, ab)) { ok = false; break; }
+                uint8_t *vrow = smem + C::kOffV + sv * C::kTileBytes + r * 128;
+#pragma unroll
+                for (int c = 0; c < C::kColBoxes; ++c) {
+                    // paired layout: box c holds the positions of part c; otherwise a row's
+                    // boxes hold the dims of one position (part 0)
+                    if (!valid[kPair ? c : 0]) {
+                        uint4 *w = reinterpret_cast<uint4 *>(vrow + c * kBoxBytes);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) w[k] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            }
             }
             fence_proxy_async_smem();
             mbar_arrive(&pfull[pbi]);
@@ -1072,31 +1183,34 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         for (int h = 0; h < NH; ++h) acc[h] += xch[h * 64 + r];
                     }
                 }
-                float L[NH];
-                reduce4<NH, false>(lred, L);
                 const int seg = cur.b * G + cur.g;
                 const long long seg_a = (long long)G * prefix[cur.b] + (long long)cur.g * cur.tiles;
                 const bool owned = (piece_u0 == seg_a) && (cur.j + 1 == cur.tiles);
-                if (owned) {
-                    float *orow = p.out + ((size_t)cur.b * p.H + (size_t)cur.g * n) * D;
+                float *orow = p.out + ((size_t)cur.b * p.H + (size_t)cur.g * n) * D;
+                const int slot = range.chunk < 0 ? (int)blockIdx.x + seg : chunk_slot(p, range.chunk, range_piece);
+                float *sp = owned ? nullptr : slot_ptr(p, slot, D);
+                const int aoff = slot_acc_offset(n);
 #pragma unroll
-                    for (int h = 0; h < NH; ++h)
-                        if (h < n && has_dim) orow[h * D + odim] = acc[h] / L[h];
-                } else {
-                    const int slot = range.chunk < 0 ? (int)blockIdx.x + seg : chunk_slot(p, range.chunk, range_piece);
-                    float *sp = slot_ptr(p, slot, D);
-                    const int aoff = slot_acc_offset(n);
+                for (int h0 = 0; h0 < NH; h0 += CH) {   // CH heads at a time (registers)
+                    float L[CH];
+                    reduce4<CH, false, NH>(lred + h0, L);
+                    if (owned) {
 #pragma unroll
-                    for (int h = 0; h < NH; ++h)
-                        if (h < n && has_dim) sp[aoff + h * D + odim] = acc[h];
-                    if (tg == 0) {
-                        float mcur[NH];
-                        load_vec<NH>(mrun_s + (i % 3) * NH, mcur);
+                        for (int h = 0; h < CH; ++h)
+                            if (h0 + h < n && has_dim) orow[(h0 + h) * D + odim] = acc[h0 + h] / L[h];
+                    } else {
 #pragma unroll
-                        for (int h = 0; h < NH; ++h) {
-                            if (h < n) {
-                                sp[h] = mcur[h];
-                                sp[n + h] = L[h];
+                        for (int h = 0; h < CH; ++h)
+                            if (h0 + h < n && has_dim) sp[aoff + (h0 + h) * D + odim] = acc[h0 + h];
+                        if (tg == 0) {
+                            float mcur[CH];
+                            load_vec<CH>(mrun_s + (i % 3) * NH + h0, mcur);
+#pragma unroll
+                            for (int h = 0; h < CH; ++h) {
+                                if (h0 + h < n) {
+                                    sp[h0 + h] = mcur[h];
+                                    sp[n + h0 + h] = L[h];
+                                }
                             }
                         }
                     }
