@@ -114,7 +114,8 @@ def test_dynamic_pool_with_empty_and_short_sequences(d):
     inp = make_decode_inputs(cfg, seq_lens=[0, Lmax, 5, 0, 8192, 129, 3000, 0])
     ref = oracle_out(inp)
     outs = []
-    for ctas in (1, 2, 3, 5):
+    # 1..5 CTAs: >= 64 tiles each, a pool of 4-tile chunks; 8..40: static ranges only
+    for ctas in (1, 2, 3, 5, 8, 16, 30, 40):
         got = run(inp, path=gqa.PATH_TCGEN05, num_ctas=ctas)
         check_close(got, ref, what=f"pool d={d} ctas={ctas}")
         outs.append(got)
