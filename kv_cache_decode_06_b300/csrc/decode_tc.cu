@@ -221,10 +221,19 @@ struct TcCfg {
     // warps: producer, score MMA, 4 softmax, value MMA, and (variant instances) the page-id warp
     static constexpr int kThreads = kPaged ? 256 : 224;
     // TMEM: S accumulators [2][part][N] then O accumulators [3][kOW] (O is folded two tiles behind)
-    static constexpr int kOCol = 2 * kParts * N;
-    static constexpr int kTmemCols = pow2_cols(kOCol + 3 * kOW);
-    static_assert(kOCol + 3 * kOW <= 512, "TMEM columns");
-    static constexpr int kPvM = kPair ? 128 : D;
+    // Heads on M (64 query heads per group at d = 64): the score GEMM is S = Q·K^T
+    // with the 64 heads as its rows and the tile's 128 positions as columns, so one
+    // softmax thread owns one head's scores and needs no cross-thread reduction;
+    // the value GEMM is O = P·V (P: [heads][positions], K-major, A operand; V: B
+    // operand, MN-major), O [64 heads][d] in TMEM.  P buffer: hi then lo, each two
+    // 64-position halves of 64 rows x 128 bytes (the same 32 KB as otherwise).
+    static constexpr bool kHM = (D == 64 && NH == 64 && !kPair);
+    static constexpr int kOCol = kHM ? 2 * kTile : 2 * kParts * N;   // S buffers first
+    static constexpr int kOBuf = kHM ? D : kOW;                      // columns of one O buffer
+    static constexpr int kTmemCols = pow2_cols(kOCol + 3 * kOBuf);
+    static_assert(kOCol + 3 * kOBuf <= 512, "TMEM columns");
+    static_assert(!kHM || kPBufBytes == 2 * 2 * 64 * 128, "heads-on-M P buffer");
+    static constexpr int kPvM = kHM ? 64 : kPair ? 128 : D;
     static_assert(kOW % 16 == 0 && kOW <= 256, "value GEMM N");
     static_assert(!kPair || NH * 64 * 4 <= kPBufBytes, "piece-end exchange fits a P buffer");
     // butterfly: number of head-halving steps (the rest are plain reductions)
@@ -815,13 +824,22 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         // part c (paired layout: the box of even / odd positions) -> S columns [bi][c];
                         // base descriptors once, then constant offsets (K step = 32 bytes in a box)
                         const uint64_t kd0 = sdesc_sw128(kb, 16, 1024), qd0 = sdesc_sw128(qbase, 16, 1024);
-#pragma unroll
-                        for (int c = 0; c < NP; ++c)
+                        if constexpr (C::kHM) {
+                            // S [64 heads x 128 positions] = Q·K^T: Q is the A operand (d = 64: one K atom)
+                            constexpr uint32_t idS_hm = idesc_bf16_f32(64, kTile, false, false);
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
-                                umma_bf16(tmem + (bi * NP + c) * N,
-                                          sdesc_add(kd0, (kPair ? c : (kk >> 2)) * kBoxBytes + (kk & 3) * 32),
-                                          sdesc_add(qd0, (kk >> 2) * (N * 128) + (kk & 3) * 32), idS, kk != 0);
+                                umma_bf16(tmem + bi * kTile, sdesc_add(qd0, kk * 32), sdesc_add(kd0, kk * 32), idS_hm,
+                                          kk != 0);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < NP; ++c)
+#pragma unroll
+                                for (int kk = 0; kk < D / 16; ++kk)
+                                    umma_bf16(tmem + (bi * NP + c) * N,
+                                              sdesc_add(kd0, (kPair ? c : (kk >> 2)) * kBoxBytes + (kk & 3) * 32),
+                                              sdesc_add(qd0, (kk >> 2) * (N * 128) + (kk & 3) * 32), idS, kk != 0);
+                        }
                         umma_commit(&sfull[bi]);
                         umma_commit(&kempty[st]);
                         if (last) {
@@ -851,14 +869,26 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         if (kExt && p.v_new && vinfo[st].on)   // the appended value replaces its row first
                             patch_tile<C>(smem + C::kOffV + st * C::kTileBytes, vstage + st * C::kRowBytes, vinfo[st]);
                         const uint32_t vb = sbase + C::kOffV + st * C::kTileBytes;
-                        const uint32_t d_o = tmem + C::kOCol + ob * C::kOW;
+                        const uint32_t d_o = tmem + C::kOCol + ob * C::kOBuf;
                         // A = V^T, MN-major: the column boxes are the M atoms (LBO), 16 positions = 2 KB
                         const uint64_t vd0 = sdesc_sw128(vb, kBoxBytes, 1024);
                         const uint64_t pd0 = sdesc_sw128(sbase + C::kOffP + pbi * C::kPBufBytes, 16, 1024);
+                        if constexpr (C::kHM) {
+                            // O [64 heads x d] = P_hi·V + P_lo·V: P is the A operand (K-major, two
+                            // 64-position halves of 8 KB), V the B operand (MN-major, 16 positions = 2 KB)
+                            constexpr uint32_t idPV_hm = idesc_bf16_f32(64, D, false, true);
 #pragma unroll
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            umma_bf16(d_o, sdesc_add(vd0, kk * 2048),
-                                      sdesc_add(pd0, (kk >> 2) * (C::kOW * 128) + (kk & 3) * 32), idPV, kk != 0);
+                            for (int half = 0; half < 2; ++half)
+#pragma unroll
+                                for (int kk = 0; kk < kTile / 16; ++kk)
+                                    umma_bf16(d_o, sdesc_add(pd0, half * 16384 + (kk >> 2) * 8192 + (kk & 3) * 32),
+                                              sdesc_add(vd0, kk * 2048), idPV_hm, (half | kk) != 0);
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < kTile / 16; ++kk)
+                                umma_bf16(d_o, sdesc_add(vd0, kk * 2048),
+                                          sdesc_add(pd0, (kk >> 2) * (C::kOW * 128) + (kk & 3) * 32), idPV, kk != 0);
+                        }
                         umma_commit(&ofull[ob]);
                         umma_commit(&vempty[st]);
                         if (pv_i < 128) GQA_TRACE_AT(kTrPvIssue + pv_i, clock64());
@@ -876,6 +906,185 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
             mbar_wait_teardown(done, 0);
         }
     } else if (warp < 6) {
+        if constexpr (C::kHM) {
+        // ================================================================ softmax, heads on M
+        // Thread (warp quadrant q4, lane < 16) owns head q4*16 + lane: the TMEM row of its
+        // scores and of its O accumulator.  Per tile: the tile maximum and the sums are
+        // per thread, so no barrier joins the softmax threads; P is written as whole
+        // 16-byte chunks of the head's row.
+        const int q4 = warp & 3;
+        const int tg = tid - 64;                 // 0..127 within the group (V row cleared by this thread)
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        const int hd = q4 * 16 + lane;
+        const bool has_head = lane < 16 && hd < n;
+        zero_empty_sequences<D>(p, prefix, P, tg, 128);
+        float accv[D];
+        float l_run = 0.f, m_run = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f;   // rescale factors of tiles i, i-1, i-2
+        int seq_b = 0, win_b = 0, piece_i0 = 0, npe = 0, i = 0, rr = 0;
+        long long piece_u0 = 0;
+        bool ok = true;
+#pragma unroll
+        for (int j = 0; j < D; ++j) accv[j] = 0.f;
+
+        // fold O of tile t into accv with that tile's rescale factor
+        auto fold_hm = [&](int t, float al) -> bool {
+            const int ob = t % 3;
+            if (!mbar_wait(&ofull[ob], (t / 3) & 1, ab)) return false;
+            tc_fence_after_sync();
+            const uint32_t oc = tmem + lane_off + C::kOCol + ob * C::kOBuf;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld_32x32b<32>(oc + c0, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) accv[c0 + j] = fmaf(accv[c0 + j], al, __uint_as_float(o[j]));
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&ofree[ob]);
+            return true;
+        };
+
+        while (ok) {
+          const int rslot = rr % kRing;
+          if (!mbar_wait(&rfull[rslot], (rr / kRing) & 1, ab)) { ok = false; break; }
+          const RangeEntry range = ring[rslot];
+          mbar_arrive(&rempty[rslot]);
+          ++rr;
+          if (range.chunk == -2) break;
+          Cursor cur = cursor_at(range.ub, prefix, p.B, G);
+          int range_piece = 0;
+          for (int k = 0; k < range.len && ok; ++k, ++i) {
+            const long long u = range.ub + k;
+            const bool first = (k == 0) || (cur.j == 0);
+            const bool last = (k + 1 == range.len) || (cur.j + 1 == cur.tiles);
+            const int bi = i & 1;
+            if (first) {
+                piece_u0 = u;
+                piece_i0 = i;
+                seq_b = seq_len_of(p, cur.b);
+                win_b = kExt ? window_start(p, seq_b) : 0;
+                l_run = 0.f;
+#pragma unroll
+                for (int j = 0; j < D; ++j) accv[j] = 0.f;
+            }
+            if (!mbar_wait(&sfull[bi], (i >> 1) & 1, ab)) { ok = false; break; }
+            if (tg == 0 && i < 128) GQA_TRACE_AT(kTrPFull + i, clock64());
+            tc_fence_after_sync();
+            const int tile_pos0 = ((win_b >> C::kTileShift) + cur.j) << C::kTileShift;
+            const int hi_pos = seq_b - tile_pos0;              // >= 1
+            const int lo_pos = kExt ? win_b - tile_pos0 : 0;   // > 0 only in a window's first tile
+            const uint32_t sc = tmem + lane_off + bi * kTile;
+            // pass 1: the tile maximum of this head
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c0 = 0; c0 < kTile; c0 += 32) {
+                uint32_t sv[32];
+                tmem_ld_32x32b<32>(sc + c0, sv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int pos = c0 + j;
+                    if (pos < hi_pos && pos >= lo_pos) mt = fmaxf(mt, __uint_as_float(sv[j]) * p.scale_log2);
+                }
+            }
+            const float m_new = (i == piece_i0) ? mt : fmaxf(m_run, mt);   // finite: every tile has a position
+            const float alpha = (i == piece_i0) ? 0.f : ex2(m_run - m_new);
+            m_run = m_new;
+            a2 = a1;
+            a1 = a0;
+            a0 = alpha;
+            // P buffer i % PB last held P(i - PB): its value GEMM must be done with it
+            const int pbi = i % PB;
+            if (i >= PB && !mbar_wait(&ofull[(i - PB) % 3], ((i - PB) / 3) & 1, ab)) { ok = false; break; }
+            // pass 2: probabilities, the sum, and P row hd as bf16 hi (first 16 KB) + lo (next 16 KB),
+            // K-major with 128-byte swizzle: half pos/64, row hd, 16-byte chunk ((pos%64)/8) ^ (hd%8)
+            uint8_t *prow = smem + C::kOffP + pbi * C::kPBufBytes + hd * 128;
+            float sum = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < kTile; c0 += 32) {
+                uint32_t sv[32];
+                tmem_ld_32x32b<32>(sc + c0, sv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int j2 = 0; j2 < 4; ++j2) {
+                        float pv[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int j = g8 * 8 + j2 * 2 + e, pos = c0 + j;
+                            pv[e] = (pos < hi_pos && pos >= lo_pos)
+                                        ? ex2(__uint_as_float(sv[j]) * p.scale_log2 - m_new) : 0.f;
+                            sum += pv[e];
+                        }
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(pv[0], pv[1]);
+                        const float2 hf = __bfloat1622float2(h2);
+                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(pv[0] - hf.x, pv[1] - hf.y);
+                        hw[j2] = *reinterpret_cast<const uint32_t *>(&h2);
+                        lw[j2] = *reinterpret_cast<const uint32_t *>(&l2);
+                    }
+                    if (lane < 16) {
+                        const int pos8 = c0 + g8 * 8;
+                        uint8_t *dst = prow + (pos8 >> 6) * 8192 + ((((pos8 & 63) >> 3) ^ (hd & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(dst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4 *>(dst + 16384) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                }
+            }
+            l_run = fmaf(l_run, alpha, sum);
+            tc_fence_before_sync();
+            mbar_arrive(&sfree[bi]);
+            // ---- clear V rows outside [lo, hi) (they may hold anything, NaN included): row tg
+            if (hi_pos < C::kTilePos || lo_pos > 0) {
+                const int sv = i % SV;
+                if (!mbar_wait(&vfull[sv], (i / SV) & 1, ab)) { ok = false; break; }
+                if (!(tg < hi_pos && tg >= lo_pos)) {
+                    uint4 *w = reinterpret_cast<uint4 *>(smem + C::kOffV + sv * C::kTileBytes + tg * 128);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) w[q] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&pfull[pbi]);
+            // ---- fold O of the tile before the previous one
+            if (i - 2 >= piece_i0 && !fold_hm(i - 2, a2)) { ok = false; break; }
+
+            if (last) {
+                if (tg == 0) GQA_TRACE_AT(kTrPieceEnd + 2 * npe, clock64());
+                if (i - 1 >= piece_i0 && !fold_hm(i - 1, a1)) { ok = false; break; }
+                if (!fold_hm(i, a0)) { ok = false; break; }
+                const int seg = cur.b * G + cur.g;
+                const long long seg_a = (long long)G * prefix[cur.b] + (long long)cur.g * cur.tiles;
+                const bool owned = (piece_u0 == seg_a) && (cur.j + 1 == cur.tiles);
+                if (has_head) {
+                    if (owned) {
+                        float4 *o4 = reinterpret_cast<float4 *>(p.out + ((size_t)cur.b * p.H + (size_t)cur.g * n + hd) * D);
+#pragma unroll
+                        for (int c = 0; c < D / 4; ++c)
+                            o4[c] = make_float4(accv[4 * c] / l_run, accv[4 * c + 1] / l_run, accv[4 * c + 2] / l_run,
+                                                accv[4 * c + 3] / l_run);
+                    } else {
+                        const int slot = range.chunk < 0 ? (int)blockIdx.x + seg : chunk_slot(p, range.chunk, range_piece);
+                        float *sp = slot_ptr(p, slot, D);
+                        sp[hd] = m_run;
+                        sp[n + hd] = l_run;
+                        float4 *a4 = reinterpret_cast<float4 *>(sp + slot_acc_offset(n) + hd * D);
+#pragma unroll
+                        for (int c = 0; c < D / 4; ++c)
+                            a4[c] = make_float4(accv[4 * c], accv[4 * c + 1], accv[4 * c + 2], accv[4 * c + 3]);
+                    }
+                }
+                if (tg == 0) GQA_TRACE_AT(kTrPieceEnd + 2 * npe + 1, clock64());
+                ++npe;
+                ++range_piece;
+            }
+            cursor_next(cur, prefix, p.B, G);
+          }
+        }
+        if (tg == 0) GQA_TRACE_AT(kTrTiles, i);
+        } else {
         // ================================================================ softmax + epilogue
         const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
         const int r = q4 * 32 + lane;            // tile position (S) / head dim (O, d = 128)
@@ -907,7 +1116,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
             tc_fence_after_sync();
             // hi and lo columns and the rescale factors, at most 16 heads at a time
             // (bounds the registers at NH = 64)
-            const uint32_t oc = tmem + lane_off + C::kOCol + ob * C::kOW + o_part;
+            const uint32_t oc = tmem + lane_off + C::kOCol + ob * C::kOBuf + o_part;
 #pragma unroll
             for (int h0 = 0; h0 < NH; h0 += CH) {
                 uint32_t ohi[CH], olo[CH];
@@ -1225,6 +1434,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
           }
         }
         if (tg == 0) GQA_TRACE_AT(kTrTiles, i);
+        }
     } else if (kPaged) {
         // ================================================================ page-id warp (paged cache)
         // Walks the same tiles as the producer, up to kIdRing tiles ahead, and puts

@@ -72,6 +72,10 @@ SMALL = [
     (2, 64, 8, 128, 1024, [1024, 777]),
     (2, 8, 2, 64, 257, [257, 100]),        # d = 64, odd Lmax: unpaired layout
     (3, 32, 4, 64, 1030, [1030, 513, 2]),  # d = 64, even Lmax: paired layout, odd lengths
+    (2, 64, 1, 64, 515, [515, 130]),       # 64 heads per group at d = 64: heads on M
+    (3, 128, 2, 64, 300, [300, 1, 64]),
+    (2, 40, 1, 64, 200, [200, 77]),        # 40 heads: padded to 64
+    (2, 64, 1, 128, 300, [300, 129]),      # 64 heads at d = 128
 ]
 
 

@@ -36,8 +36,9 @@ def _cfg(name, cid, B, H, G, d, Lmax):
     return DecodeConfig(name, cid, B=B, H=H, G=G, d=d, Lmax=Lmax, seq_lo=1, seq_hi=Lmax)
 
 
-# (B, H, G, d, Lmax): d=128; d=64 paired (even Lmax); d=64 unpaired (odd Lmax); H/G = 4 and 16
-SHAPES = [(3, 32, 8, 128, 1200), (2, 16, 4, 64, 1030), (3, 8, 2, 64, 777), (2, 64, 4, 128, 600)]
+# (B, H, G, d, Lmax): d=128; d=64 paired (even Lmax); d=64 unpaired (odd Lmax); H/G = 4, 16 and 64
+SHAPES = [(3, 32, 8, 128, 1200), (2, 16, 4, 64, 1030), (3, 8, 2, 64, 777), (2, 64, 4, 128, 600),
+          (2, 64, 1, 64, 700)]   # the last: 64 heads per group at d = 64 (heads on M)
 
 
 def _dev(a):
@@ -88,7 +89,7 @@ def _paged_inputs(shape, page_size, lens, seed, cid):
 
 # page sizes are powers of two, so Lmax is even: d = 64 is paired up to H/G = 16 and
 # unpaired above (the last shape, H/G = 32)
-PAGED_SHAPES = SHAPES[:3] + [(2, 64, 2, 64, 500)]
+PAGED_SHAPES = SHAPES[:3] + [(2, 64, 2, 64, 500), (2, 64, 1, 64, 500)]
 
 
 @pytest.mark.parametrize("page_size", [16, 32, 64, 128, 256, 1024])
