@@ -639,7 +639,9 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
             Cursor kc{0, 0, 0, 1}, vc{0, 0, 0, 1};
             SeqLenCache k_lens, v_lens;
             IdlePoll poll;
-            while (!v_done) {
+            // paged instances: the page-id warp copies the V tiles, so this thread stops
+            // once the K side has issued everything
+            while (kPaged ? !k_done : !v_done) {
                 bool progress = false;
                 // ---- the next range, once the K side has issued the current one
                 if (!k_done && k_u == k_end) {
@@ -662,7 +664,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                     }
                     const int slot = pushed % kRing;
                     if (pushed < kRing ||
-                        (v_r > pushed - kRing && mbar_test_wait(&rempty[slot], ((pushed / kRing) - 1) & 1))) {
+                        ((kPaged || v_r > pushed - kRing) && mbar_test_wait(&rempty[slot], ((pushed / kRing) - 1) & 1))) {
                         ring[slot] = next;
                         mbar_arrive(&rfull[slot]);   // release: the entry is visible to the waiters
                         if (pushed == 0) GQA_TRACE_AT(kTrRing0, clock64());
@@ -686,7 +688,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                     const int st = i % SK, qb = piece % QB;
                     // K runs at most one tile ahead of V: a tile's V then lands about when its
                     // probabilities are ready, and a piece's last value GEMM does not wait long
-                    if (vissued >= i &&
+                    if ((kPaged || vissued >= i) &&
                         (!first || piece < QB || mbar_test_wait(&qempty[qb], ((piece / QB) - 1) & 1)) &&
                         (i < SK || mbar_test_wait(&kempty[st], ((i / SK) - 1) & 1)) &&
                         (!kPaged || mbar_test_wait(&idfull[i % C::kIdRing], (i / C::kIdRing) & 1))) {
@@ -711,6 +713,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         } else {
                             produce_plain_tile<C>(p, &tm_k, kdst, &kfull[st], kc, pol_kv);
                         }
+                        if constexpr (kPaged) mbar_arrive(&idempty[i % C::kIdRing]);   // the ids are no longer read here
                         if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i + 1, clock64());
                         if (i == 0) GQA_TRACE_AT(kTrFirstK, clock64());
                         if (i < 128) GQA_TRACE_AT(kTrKIssue + i, clock64());
@@ -722,7 +725,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                     }
                 }
                 // ---- V of the next tile (walks the same ranges, never ahead of K)
-                if (v_u == v_end && v_r < pushed) {
+                if (!kPaged && v_u == v_end && v_r < pushed) {
                     const RangeEntry e = ring[v_r % kRing];   // written by this thread
                     ++v_r;
                     if (e.chunk == -2) {
@@ -734,7 +737,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                     }
                     progress = true;
                 }
-                if (v_u < v_end && vissued < kissued) {
+                if (!kPaged && v_u < v_end && vissued < kissued) {
                     const int i = vissued, st = i % SV;
                     if (i < SV || mbar_test_wait(&vempty[st], ((i / SV) - 1) & 1)) {
                         uint8_t *vdst = smem + C::kOffV + st * C::kTileBytes;
@@ -744,7 +747,6 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                             const int T = kPaged ? ids[C::kIdMax] : v_lens.get(p, vc.b);
                             produce_variant_tile<C>(p, &tm_v, vdst, &vfull[st], vc, T, pol_kv, p.v_new,
                                                     vstage + st * C::kRowBytes, &vinfo[st], p.v_dst, ids);
-                            if constexpr (kPaged) mbar_arrive(&idempty[i % C::kIdRing]);   // K and V of the tile are issued
                         } else {
                             produce_plain_tile<C>(p, &tm_v, vdst, &vfull[st], vc, pol_kv);
                         }
@@ -1441,8 +1443,9 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
         // each tile's page ids (lane k: box k) and T_b into the ring.  The block-table
         // loads thus never sit in the producer's thread, whose barrier arrivals
         // would otherwise wait for them.
-        int rr = 0, ti = 0, cached_b = -1, T = 0;
+        int rr = 0, ti = 0, cached_b = -1, T = 0, v_copies = 0;
         bool ok = true;
+        const uint64_t pol_v = l2_policy_evict_first();
         while (ok) {
             const int rslot = rr % kRing;
             if (!mbar_wait(&rfull[rslot], (rr / kRing) & 1, ab)) break;
@@ -1478,8 +1481,28 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                 }
                 if (lane == 0) e[C::kIdMax] = T;
                 mbar_arrive(&idfull[slot]);   // every lane: its own writes are released
+                __syncwarp();
+                // ---- the V copy of this tile (the producer thread copies K): a second
+                // issuing thread halves the serial copy time when pages are small
+                if (lane == 0) {
+                    const int sv = ti % SV;
+                    if (ti >= SV && !mbar_wait(&vempty[sv], ((ti / SV) - 1) & 1, ab)) {
+                        ok = false;
+                    } else {
+                        produce_variant_tile<C>(p, &tm_v, smem + C::kOffV + sv * C::kTileBytes, &vfull[sv], cur, T,
+                                                pol_v, p.v_new, vstage + sv * C::kRowBytes, &vinfo[sv], p.v_dst, e);
+                        ++v_copies;
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
                 cursor_next(cur, prefix, p.B, G);
             }
+        }
+        if (lane == 0 && *s_abort) {
+            // let this warp's V copies in flight land before the CTA's shared memory is released
+            for (int k = v_copies > SV ? v_copies - SV : 0; k < v_copies; ++k)
+                mbar_wait_teardown(&vfull[k % SV], (k / SV) & 1);
         }
     }
 

@@ -197,3 +197,38 @@ def test_paged_fused_append(page_size):
     vg = oracle.gather_pages(vd.cpu().view(torch.int16).numpy().view(np.uint16), table, inp.seq_lens, cfg.Lmax)
     for b, T in enumerate(inp.seq_lens):
         assert np.array_equal(kg[b, :, :T], k_ref[b, :, :T]) and np.array_equal(vg[b, :, :T], v_ref[b, :, :T])
+
+
+@pytest.mark.parametrize("page_size", [16, 256])
+def test_paged_append_and_window_together(page_size):
+    """All three at once: paged cache, fused append and a window, with pages before the window unlisted."""
+    shape = (3, 32, 8, 128, 1000)
+    cfg, inp, kp, vp, table = _paged_inputs(shape, page_size, [1000, 300, 2], seed=11, cid=67)
+    kn, vn = _new_rows(cfg, 5)
+    W = 333
+    k_ref = oracle.append_row(inp.k, kn, inp.seq_lens)
+    v_ref = oracle.append_row(inp.v, vn, inp.seq_lens)
+    ref = oracle.gqa_decode_f64(inp.q, k_ref, v_ref, inp.seq_lens, inp.scale, window=W)
+    t2 = table.copy()
+    for b, T in enumerate(inp.seq_lens):
+        t2[b, :max(0, int(T) - W) // page_size] = -1
+    q = torch.from_numpy(inp.q).view(torch.bfloat16).cuda()
+    kd, vd = _dev(kp).view(torch.bfloat16), _dev(vp).view(torch.bfloat16)
+    ws = gqa.alloc_workspace(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax)
+    got = gqa.decode_paged(q, kd, vd, _dev(t2), _dev(inp.seq_lens), k_new=_dev(kn).view(torch.bfloat16),
+                           v_new=_dev(vn).view(torch.bfloat16), workspace=ws, scale=float(inp.scale), window=W)
+    torch.cuda.synchronize()
+    check_close(got.cpu().numpy(), ref, what=f"paged+append+window ps={page_size}")
+    assert gqa.read_flags(ws) == 0
+
+
+def test_cross_attention_on_the_cuda_core_path():
+    """The CUDA-core path also takes seq_lens = NULL (it rejects only the window, paging and append)."""
+    cfg = _cfg("cross_simt", 68, 2, 16, 4, 128, 700)
+    inp = make_decode_inputs(cfg, seq_lens=[700, 700])
+    q, k, v, _ = to_device(inp)
+    got = gqa.decode(q, k, v, None, scale=float(inp.scale), path=gqa.PATH_SIMT)
+    torch.cuda.synchronize()
+    check_close(got.cpu().numpy(), oracle.gqa_decode_f64(inp.q, inp.k, inp.v, None, inp.scale), what="simt cross")
+    with pytest.raises(gqa.GQAError):
+        gqa.decode(q, k, v, to_device(inp)[3], scale=float(inp.scale), path=gqa.PATH_SIMT, window=100)
