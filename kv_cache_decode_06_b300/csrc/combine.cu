@@ -14,12 +14,13 @@
 // Launched right after the decode kernel with programmatic stream
 // serialisation: its CTAs build the tile prefix and the work split (from
 // seq_lens, which the decode kernel does not write) while the decode grid
-// drains, then wait for it to complete.  The CTAs take segments in a
-// grid-stride loop; a segment whose single piece covered it whole was written by
-// the decode kernel, the others are merged here from the slots the work split
-// assigns to their pieces.  A thread owns four consecutive dims of one head and
-// loads the pieces in batches of eight, each batch one round trip to L2,
-// merging online.
+// drains, then wait for it to complete.  The CTAs take (segment, 256-float4
+// part of its n x D outputs) work items in a grid-stride loop, so large head
+// groups spread over several CTAs; a segment whose single piece covered it whole
+// was written by the decode kernel, the others are merged here from the slots
+// the work split assigns to their pieces.  A thread owns four consecutive dims
+// of one head and loads the pieces in batches of eight, each batch one round
+// trip to L2, merging online.
 #include <cuda_runtime.h>
 
 #include "decode_common.cuh"
@@ -45,7 +46,9 @@ __global__ void __launch_bounds__(kCombThreads) gqa_split_combine_kernel(const D
     const size_t stride = (size_t)slot_floats(n, D);
     const int aoff = slot_acc_offset(n);
     const int nd4 = n * D / 4;
-    for (int s = blockIdx.x; s < p.B * G; s += gridDim.x) {
+    const int parts = (nd4 + kCombThreads - 1) / kCombThreads;   // CTAs per segment (one float4 per thread each)
+    for (int wi = blockIdx.x; wi < p.B * G * parts; wi += gridDim.x) {
+        const int s = wi / parts, e = (wi - s * parts) * kCombThreads + threadIdx.x;
         const int b = s / G, g = s - b * G;
         const int T = prefix[b + 1] - prefix[b];
         if (T == 0) continue;
@@ -54,7 +57,7 @@ __global__ void __launch_bounds__(kCombThreads) gqa_split_combine_kernel(const D
         const int count = sl.count();
         if (count < 2) continue;   // one piece covered the segment: the decode kernel wrote it
         float4 *orow = reinterpret_cast<float4 *>(p.out + ((size_t)b * p.H + (size_t)g * n) * D);
-        for (int e = threadIdx.x; e < nd4; e += kCombThreads) {
+        if (e < nd4) {
             const int h = (e * 4) / D;
             float M = -INFINITY, L = 0.f;
             float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -102,9 +105,11 @@ __global__ void __launch_bounds__(kCombThreads) gqa_split_combine_kernel(const D
 }  // namespace
 
 cudaError_t launch_split_combine(const DecodeParams &p, int D, int grid_main, cudaStream_t stream) {
-    // one CTA per segment, at most 4096 (the others loop over the rest)
-    const int segs = p.B * p.G;
-    const int grid = segs < 4 * kMaxCtas ? segs : 4 * kMaxCtas;
+    // one CTA per segment and 256 float4 of its n x D outputs, at most 4096 (the others
+    // loop over the rest): large head groups spread over several CTAs
+    const int nd4 = p.n * D / 4;
+    const long long work = (long long)p.B * p.G * ((nd4 + kCombThreads - 1) / kCombThreads);
+    const int grid = work < 4 * kMaxCtas ? (int)work : 4 * kMaxCtas;
     if (D == 128) return launch_pdl(gqa_split_combine_kernel<128>, grid, kCombThreads, 0, stream, p, grid_main);
     return launch_pdl(gqa_split_combine_kernel<64>, grid, kCombThreads, 0, stream, p, grid_main);
 }

@@ -1,37 +1,42 @@
 // GQA decode on the fifth-generation tensor cores (tcgen05 + TMEM).
 //
-// The query heads of one group form the N side of two small GEMMs per
-// 128-position tile, with the positions (scores) or the head dims (values) on
-// the M side, so every K/V tile read from HBM serves all n = H/G heads:
-//   S^T [128 pos x N]  = K_tile [128 x d] . Q_g^T [d x N]       (K-major A and B)
-//   O^T [d x N]        = V_tile^T [d x 128] . P^T [128 x N]     (MN-major A, K-major B)
-// N is n rounded up to at least 16 (the extra columns are never read).
+// The query heads of one group are one operand of two small GEMMs per tile, so
+// every K/V tile read from HBM serves all n = H/G heads:
+//   S^T [128 pos x N]  = K_tile [128 x d] . Q_g^T [d x N]            (K-major A and B)
+//   O^T [M x kOW]      = V_tile^T [M x 128] . [P_hi; P_lo]^T          (MN-major A, K-major B)
+// N is n rounded up to 16, 32 or 64 (the extra columns are never read).  The
+// value GEMM stacks the probabilities' bf16 hi and lo parts (and, in the paired
+// d = 64 layout, the even and odd positions) as column blocks of one GEMM, so
+// the probabilities enter it with ~16 significant bits in 8 instructions per
+// tile.  At 64 heads per group and d = 64 the heads are the GEMM rows instead
+// (S = Q.K^T, O = P.V): one softmax thread then owns one head's scores.
 // Operands come from 128-byte-swizzled shared memory written by TMA;
-// accumulators live in TMEM.  P is split into bf16 hi + lo parts (two MMAs), so
-// the probabilities enter the value GEMM with ~16 significant bits, not 8.
+// accumulators live in TMEM.
 // ["Grouped-query attention (GQA)" concept page, "Implementation sketch",
 //  decode-step pseudocode; arxiv:2305.13245 §2.2]
 //
-// Warp roles (224 threads): warp 0 = TMA producer, warp 1 = score-GEMM issuer and
-// TMEM owner, warp 6 = value-GEMM issuer, warps 2-5 = softmax + epilogue
-// (thread <-> TMEM lane: a position of the tile for S, a head dim for O).
+// Warp roles (224 threads): warp 0 = TMA producer (Q, K, V; hands the work
+// ranges to the others), warp 1 = score-GEMM issuer and TMEM owner, warp 6 =
+// value-GEMM issuer, warps 2-5 = softmax + epilogue (thread <-> TMEM lane).
+// Paged-cache instances add warp 7 (256 threads): block-table ids and the V copies.
 //
-// Producer and MMA issuer are event loops: each issues the next operation
+// Producer and MMA issuers are event loops: each issues the next operation
 // whose inputs are ready.  K slot s is handed back as soon as the score GEMM of
-// its tile has read it, V slot s after the value GEMM, so K loads run ahead of
-// V loads and more bytes are in flight.  Per tile the softmax group
-//   1. loads its S row, reduces the per-head maximum over the 128 positions
+// its tile has read it, V slot s after the value GEMM.  Per tile the softmax group
+//   1. loads its S row, reduces the per-head maximum over the tile's positions
 //      (transposed butterfly in the warp, then the 4 warps via shared memory),
-//   2. writes P(i) and hands it to the MMA warp,
+//   2. writes P(i) and hands it to the value-GEMM warp,
 //   3. folds the O of the tile two steps back into register accumulators with
 //      that tile's rescale factor (so TMEM never needs rescaling); O is triple
 //      buffered in TMEM, so a value GEMM has two softmax steps to finish.
-// Work split and pieces are shared with the CUDA-core path (decode_common.cuh);
-// pieces that are not a whole segment leave their partial state in the
-// workspace for the split-combine kernel (combine.cu).
+// Three instance families (kVar): the plain contiguous cache; the contiguous
+// cache with a window or a fused append; the paged cache.  Each carries only its
+// own producer code.  Work split and pieces are shared with the CUDA-core path
+// (decode_common.cuh); pieces that are not a whole segment leave their partial
+// state in the workspace for the split-combine kernel (combine.cu).
 //
-// Build with -DGQA_TRACE for a per-CTA timeline (clock64 stamps of every
-// pipeline event, see the slot map at TraceSlot) readable with gqa_trace_copy.
+// Build with -DGQA_TRACE for a per-CTA timeline (clock64 stamps of the
+// pipeline events, see the slot map at TraceSlot) readable with gqa_trace_copy.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
