@@ -219,6 +219,18 @@ gqa_status gqa_decode_paged(const void *q, void *k_pages, void *v_pages, const i
 int gqa_decode_select_path(int B, int H, int G, int d, int Lmax);
 
 /*
+ * Test hook for the failure path.  In the next decode call on the tensor-core
+ * path (any thread, any entry point), thread block 0 skips its K copy number
+ * `tile` (counted from 0 in its own copy order): nothing ever arrives on that
+ * copy's barrier, so the score GEMM's bounded wait runs out after about one
+ * second, the block abandons its work, GQA_FLAG_WAIT_TIMEOUT is set in the
+ * workspace flag word and the call's output is invalid.  The context stays
+ * usable; zero the workspace header before the next call.  A negative `tile`
+ * cancels a pending request.
+ */
+void gqa_debug_withhold_copy(int tile);
+
+/*
  * Copy the workspace flag word (GQA_FLAG_* bits, OR-ed by earlier decode calls)
  * to *flags.  Enqueued on `stream` and then synchronises that stream.
  * With clear != 0 the word is reset to zero afterwards (also on `stream`).

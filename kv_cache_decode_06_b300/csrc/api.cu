@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "gqa.h"
@@ -169,6 +170,9 @@ bool make_page_map(CUtensorMap *map, const void *base, int num_pages, int G, int
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Test hook (gqa_debug_withhold_copy): applies to the next decode call only.
+std::atomic<int> g_withhold_k{-1};
+
 // Every decode variant: contiguous or paged cache, with or without the fused
 // append, a window, or all positions valid (seq_lens null).
 struct DecodeRequest {
@@ -238,6 +242,7 @@ gqa_status decode_impl(const DecodeRequest &r) {
     p.k_dst = r.k_new ? static_cast<__nv_bfloat16 *>(const_cast<void *>(r.k)) : nullptr;
     p.v_dst = r.v_new ? static_cast<__nv_bfloat16 *>(const_cast<void *>(r.v)) : nullptr;
     p.out = r.out;
+    p.withhold_k = g_withhold_k.exchange(-1);
     p.flags = reinterpret_cast<unsigned int *>(ws);
     p.ticket = reinterpret_cast<unsigned int *>(ws + 4);
     p.fails = reinterpret_cast<unsigned int *>(ws + 8);
@@ -395,6 +400,8 @@ gqa_status gqa_decode_paged(const void *q, void *k_pages, void *v_pages, const i
     r.opts = opts;
     return decode_impl(r);
 }
+
+void gqa_debug_withhold_copy(int tile) { g_withhold_k.store(tile < 0 ? -1 : tile); }
 
 gqa_status gqa_decode_read_flags(void *workspace, uint32_t *flags, int clear, void *stream) {
     if (!workspace || !flags || !aligned(workspace, 256)) return GQA_ERR_INVALID_ARG;

@@ -64,6 +64,7 @@ struct DecodeParams {
     // the contiguous cache or the page pool)
     const __nv_bfloat16 *k_new, *v_new;
     __nv_bfloat16 *k_dst, *v_dst;
+    int withhold_k;           // test hook: CTA 0 skips its K copy number withhold_k (-1: none)
     float *out;               // [B, H, D]
     unsigned int *flags;      // workspace flag word
     unsigned int *ticket;     // dynamic-pool claims (zero between calls)

@@ -710,7 +710,10 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         }
                         uint8_t *kdst = smem + C::kOffK + st * C::kTileBytes;
                         if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i, clock64());
-                        if constexpr (kExt) {
+                        if (i == p.withhold_k && blockIdx.x == 0) {
+                            // test hook: this copy is never made, so the score GEMM's bounded
+                            // wait for it runs out and the CTA takes its abort path
+                        } else if constexpr (kExt) {
                             const int *ids = kPaged ? ids_ring + (i % C::kIdRing) * C::kIdStride : nullptr;
                             const int T = kPaged ? ids[C::kIdMax] : k_lens.get(p, kc.b);
                             produce_variant_tile<C>(p, &tm_k, kdst, &kfull[st], kc, T, pol_kv, p.k_new,

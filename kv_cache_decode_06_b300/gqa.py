@@ -30,7 +30,7 @@ FLAG_BAD_PAGE = 0x4
 # Every symbol include/gqa.h declares.
 EXPORTS = ("gqa_status_string", "gqa_abi_version", "gqa_decode_workspace_size", "gqa_decode", "gqa_decode_ex",
            "gqa_decode_select_path", "gqa_decode_read_flags", "gqa_meanpool_kv", "gqa_meanpool_kv_strided",
-           "gqa_decode_noalloc", "gqa_decode_append", "gqa_decode_paged")
+           "gqa_decode_noalloc", "gqa_decode_append", "gqa_decode_paged", "gqa_debug_withhold_copy")
 NOALLOC_WORKSPACE_BYTES = 8 << 20
 
 _lock = threading.Lock()
@@ -76,6 +76,8 @@ def load(path: Optional[str] = None):
         lib.gqa_decode_paged.restype = I
         lib.gqa_decode_paged.argtypes = [V, V, V, V, V, V, V, V, V, Z, I, I, I, I, I, I, I, F, V,
                                          ctypes.POINTER(DecodeOptions)]
+        lib.gqa_debug_withhold_copy.restype = None
+        lib.gqa_debug_withhold_copy.argtypes = [I]
         lib.gqa_decode_select_path.restype = I
         lib.gqa_decode_select_path.argtypes = [I, I, I, I, I]
         lib.gqa_decode_read_flags.restype = I
@@ -264,6 +266,11 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                                      _stream_handle(stream, dev)),
            f"gqa_decode_noalloc (scratch limit {NOALLOC_WORKSPACE_BYTES} bytes)")
     return out
+
+
+def debug_withhold_copy(tile: int) -> None:
+    """Test hook: the next decode call's block 0 skips its K copy number ``tile`` (see gqa.h)."""
+    load().gqa_debug_withhold_copy(int(tile))
 
 
 def read_flags(workspace: torch.Tensor, clear: bool = False, stream: Optional[torch.cuda.Stream] = None) -> int:

@@ -259,3 +259,26 @@ def test_llama3_70b_workload():
 def test_long_ragged_workload():
     inp = make_decode_inputs(CONFIGS["long_ragged"])
     check_close(run(inp), oracle_out(inp), what="long_ragged")
+
+
+def test_wait_timeout_sets_flag_and_context_survives():
+    """Failure detection without a fault: a K copy that is never made (test hook) leaves a barrier that
+    nothing completes; block 0's bounded wait runs out after about a second, the call sets
+    GQA_FLAG_WAIT_TIMEOUT and returns, and after the workspace header is zeroed the next call is exact."""
+    import time
+    cfg = CONFIGS["mistral7b"].with_(B=4)
+    inp = make_decode_inputs(cfg)
+    q, k, v, sl = to_device(inp)
+    ws = gqa.alloc_workspace(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax)
+    gqa.debug_withhold_copy(1)
+    t0 = time.time()
+    gqa.decode(q, k, v, sl, workspace=ws, scale=float(inp.scale), path=gqa.PATH_TCGEN05)
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert gqa.read_flags(ws) & gqa.FLAG_WAIT_TIMEOUT
+    assert 0.5 < elapsed < 30.0, elapsed
+    ws[:256].zero_()
+    got = gqa.decode(q, k, v, sl, workspace=ws, scale=float(inp.scale))
+    torch.cuda.synchronize()
+    check_close(got.cpu().numpy(), oracle_out(inp), what="after a timed-out call")
+    assert gqa.read_flags(ws) == 0
