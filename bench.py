@@ -200,6 +200,22 @@ def run_reference(args, rank: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank runs its own replica, the job ends with the last."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(kv_bytes_per_step: int, steps: int, world: int, total_ms: float) -> float:
+    """Algorithmic KV bytes of all ranks' steps over the slowest rank's time (weak scaling)."""
+    return world * kv_bytes_per_step * steps / (total_ms / 1e3) / 1e9
+
+
 def variant_note(variant, args):
     return {"contiguous": "contiguous cache [B,G,Lmax,d]",
             "paged": f"paged cache, {args.page_size}-position pages in random pool order",
@@ -325,13 +341,9 @@ def main() -> None:
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    total_ms = float(t0.elapsed_time(t1))
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(t0.elapsed_time(t1)), world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * kv_bytes * args.steps / (total_ms / 1e3) / 1e9
+    value = whole_job_gbs(kv_bytes, args.steps, world, total_ms)
     flags = gqa.read_flags(ws)
     if flags:
         raise RuntimeError(f"decode reported flags 0x{flags:x} during the benchmark")
@@ -367,12 +379,8 @@ def main() -> None:
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    e2e_value = world * kv_bytes / (e2e_ms / 1e3) / 1e9
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_value = world * kv_bytes / (float(t.item()) / 1e3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    e2e_value = whole_job_gbs(kv_bytes, 1, world, e2e_ms)
 
     if rank != 0:
         if world > 1:

@@ -232,3 +232,49 @@ def test_cross_attention_on_the_cuda_core_path():
     check_close(got.cpu().numpy(), oracle.gqa_decode_f64(inp.q, inp.k, inp.v, None, inp.scale), what="simt cross")
     with pytest.raises(gqa.GQAError):
         gqa.decode(q, k, v, to_device(inp)[3], scale=float(inp.scale), path=gqa.PATH_SIMT, window=100)
+
+
+# ------------------------------------------------ full-size workloads (the benchmark's launch configuration)
+
+from kv_cache_decode_06_b300.inputs import CONFIGS, make_new_rows, make_paged_layout  # noqa: E402
+
+
+def _sample_rows(cfg, every=37):
+    return np.arange(0, cfg.B * cfg.H, every, dtype=np.int64)
+
+
+@pytest.mark.slow
+def test_paged_mistral7b_full():
+    """The Mistral-7B-shaped step on a paged cache of 64-position pages in random pool order, every row."""
+    cfg = CONFIGS["mistral7b"]
+    inp = make_decode_inputs(cfg)
+    kp, vp, table = make_paged_layout(inp, 64)
+    q = torch.from_numpy(inp.q).view(torch.bfloat16).cuda()
+    got = gqa.decode_paged(q, _dev(kp).view(torch.bfloat16), _dev(vp).view(torch.bfloat16), _dev(table),
+                           _dev(inp.seq_lens), scale=float(inp.scale))
+    torch.cuda.synchronize()
+    ref = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale)
+    check_close(got.cpu().numpy(), ref, what="paged mistral7b")
+
+
+@pytest.mark.slow
+def test_append_and_window_llama3_70b_full():
+    """The Llama-3-70B-shaped step with the fused append, then with a 4096-position window: sampled rows."""
+    cfg = CONFIGS["llama3_70b"]
+    inp = make_decode_inputs(cfg)
+    rows = _sample_rows(cfg)
+    kn, vn = make_new_rows(cfg)
+    q, k, v, sl = to_device(inp)
+    got = gqa.decode_append(q, _dev(kn).view(torch.bfloat16), _dev(vn).view(torch.bfloat16), k, v, sl,
+                            scale=float(inp.scale))
+    torch.cuda.synchronize()
+    k_ref = oracle.append_row(inp.k, kn, inp.seq_lens)
+    v_ref = oracle.append_row(inp.v, vn, inp.seq_lens)
+    ref = oracle.gqa_decode_f64(inp.q, k_ref, v_ref, inp.seq_lens, inp.scale, rows=rows)
+    check_close(got.cpu().numpy(), ref, rows=rows, what="append llama3_70b")
+    del k_ref, v_ref
+    q, k, v, sl = to_device(inp)
+    got = gqa.decode(q, k, v, sl, scale=float(inp.scale), window=4096)
+    torch.cuda.synchronize()
+    ref = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale, rows=rows, window=4096)
+    check_close(got.cpu().numpy(), ref, rows=rows, what="window llama3_70b")
