@@ -163,26 +163,45 @@ def all_segments(cfg):
     return [(b, g) for b in range(cfg.B) for g in range(cfg.G)]
 
 
+def cpu_oracle_rows(inp, rows):
+    """Time the float64 oracle on the given output rows (b*H + i); returns (seconds, kv bytes).
+
+    A row's share of the algorithmic bytes is its sequence's K+V rows divided by the
+    n = H/G query heads that share them.
+    """
+    import oracle
+    cfg = inp.cfg
+    kv = sum(int(inp.seq_lens[r // cfg.H]) for r in rows) * cfg.d * 2 * 2 / cfg.n
+    t0 = time.perf_counter()
+    oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale, rows=np.asarray(rows, dtype=np.int64))
+    return time.perf_counter() - t0, kv
+
+
 def run_reference(args, rank: int) -> None:
-    """The float64 CPU oracle as the reference arm, rank 0 only."""
+    """The float64 CPU oracle as the reference arm, rank 0 only.
+
+    Each step is a bounded sample of the workload's output rows (at least one), sized
+    so that the whole --steps/--warmup run spends about 150 s in the oracle.
+    """
     if rank != 0:
         return
     import oracle
     cfg = workload(args.workload)
     inp = make_decode_inputs(cfg, poison_tail=False)
-    segs = all_segments(cfg)
+    nrows_all = cfg.B * cfg.H
     cores = oracle.num_threads()
-    # calibrate: seconds per segment on this host
-    t, _ = cpu_oracle_step(inp, segs[:1])
-    per_seg = max(t, 1e-4)
+    # calibrate: seconds per row on this host (a whole group of rows, to use the threads)
+    t, _ = cpu_oracle_rows(inp, list(range(min(nrows_all, cfg.n))))
+    per_row = max(t / min(nrows_all, cfg.n), 1e-5)
     budget = 150.0 / max(1, args.steps + args.warmup)
-    nseg = int(max(1, min(len(segs), budget / per_seg)))
+    nrow = int(max(1, min(nrows_all, budget / per_row)))
+    order = np.random.default_rng(0).permutation(nrows_all)
     for i in range(args.warmup):
-        cpu_oracle_step(inp, [segs[(i * nseg + k) % len(segs)] for k in range(nseg)])
-    total_t, total_b = 0.0, 0
+        cpu_oracle_rows(inp, [int(order[(i * nrow + k) % nrows_all]) for k in range(nrow)])
+    total_t, total_b = 0.0, 0.0
     for i in range(args.steps):
-        sel = [segs[(i * nseg + k) % len(segs)] for k in range(nseg)]
-        t, b = cpu_oracle_step(inp, sel)
+        sel = [int(order[(i * nrow + k) % nrows_all]) for k in range(nrow)]
+        t, b = cpu_oracle_rows(inp, sel)
         total_t += t
         total_b += b
     value = total_b / total_t / 1e9
@@ -191,10 +210,10 @@ def run_reference(args, rank: int) -> None:
         "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": config_dict(cfg, inp, extra={"sample_segments_per_step": nseg}),
+        "config": config_dict(cfg, inp, extra={"sample_rows_per_step": nrow}),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{nseg} of {len(segs)} (batch, K/V head) segments per step, all H/G heads "
-                                   f"of each, float64 oracle (OpenMP over rows)"},
+                         "sample": f"{nrow} of {nrows_all} output rows (query heads of sequences) per step, "
+                                   f"seeded order, float64 oracle (OpenMP over rows)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
