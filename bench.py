@@ -367,6 +367,21 @@ def main() -> None:
     if flags:
         raise RuntimeError(f"decode reported flags 0x{flags:x} during the benchmark")
 
+    # ---- per-step distribution (extra information): each of a few hundred steps between its own
+    # pair of events; the events themselves serialise the steps, so this is not the headline number
+    nper = min(200, args.steps)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nper)]
+    for i, (ea, eb) in enumerate(evs):
+        ea.record(stream)
+        step(i)
+        eb.record(stream)
+    torch.cuda.synchronize()
+    per_us = sorted(1e3 * ea.elapsed_time(eb) for ea, eb in evs)
+    per_step = {"samples": nper, "median_us": statistics.median(per_us),
+                "p10_us": per_us[int(0.1 * (nper - 1))], "p90_us": per_us[int(0.9 * (nper - 1))],
+                "what": "each step alone between its own event pair: launch gaps included and no overlap "
+                        "with the neighbouring steps (the headline times K steps back to back)"}
+
     # ---- end to end through the public API with host buffers (pinned)
     def pinned(a, dtype=torch.bfloat16):
         t = torch.from_numpy(np.ascontiguousarray(a))
@@ -454,6 +469,7 @@ def main() -> None:
                 "what": "H2D of every input (q, seq_lens, the whole K/V caches or page pools, the block table "
                         "and appended rows where used) from pinned host memory + the decode call + D2H of "
                         "out, per step"},
+        "per_step_events": per_step,
         "gpu_launches": 2 * args.steps,   # decode kernel + split-combine kernel per step
         "clocks": clk.summary(),
     }
