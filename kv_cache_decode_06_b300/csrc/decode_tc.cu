@@ -153,7 +153,10 @@ struct TcCfg {
     static constexpr int kTileShift = kPair ? 8 : 7;                 // log2(positions per tile)
     static constexpr int kTilePos = 1 << kTileShift;
     static constexpr int kTileBytes = kColBoxes * kBoxBytes;         // one K or V tile
-    static constexpr int kQBytes = kQBoxes * N * 128;                // one Q buffer (N rows x d)
+    // heads on M (64 query heads per group at d = 64), see below: Q is stored twice, as
+    // the 128 rows of the score GEMM's A operand
+    static constexpr bool kHM = (D == 64 && NH == 64 && !kPair);
+    static constexpr int kQBytes = kQBoxes * N * 128 * (kHM ? 2 : 1);   // one Q buffer (N rows x d)
     // rows of one (part, hi/lo) block of the value GEMM's B operand: the heads,
     // padded to 8 (the value GEMM's N = kOW stays a multiple of 16)
     static constexpr int kNPV = NH <= 8 ? 8 : N;
@@ -226,13 +229,14 @@ struct TcCfg {
     // warps: producer, score MMA, 4 softmax, value MMA, and (variant instances) the page-id warp
     static constexpr int kThreads = kPaged ? 256 : 224;
     // TMEM: S accumulators [2][part][N] then O accumulators [3][kOW] (O is folded two tiles behind)
-    // Heads on M (64 query heads per group at d = 64): the score GEMM is S = Q·K^T
-    // with the 64 heads as its rows and the tile's 128 positions as columns, so one
-    // softmax thread owns one head's scores and needs no cross-thread reduction;
-    // the value GEMM is O = P·V (P: [heads][positions], K-major, A operand; V: B
-    // operand, MN-major), O [64 heads][d] in TMEM.  P buffer: hi then lo, each two
-    // 64-position halves of 64 rows x 128 bytes (the same 32 KB as otherwise).
-    static constexpr bool kHM = (D == 64 && NH == 64 && !kPair);
+    // Heads on M (64 query heads per group at d = 64): the score GEMM is S = [Q; Q]·K^T
+    // with the 64 heads twice as its 128 rows and the tile's 128 positions as
+    // columns; TMEM lane r holds head r % 64, and its thread takes positions
+    // 64 * (r / 64) .. + 63, so two threads share a head and every lane works.  The
+    // value GEMM is O = P·V (P: [heads][positions], K-major, A operand; V: B
+    // operand, MN-major), O [64 heads][d] in TMEM (M = 64: 16 lanes per quadrant).
+    // P buffer: hi then lo, each two 64-position halves of 64 rows x 128 bytes (the
+    // same 32 KB as otherwise).
     static constexpr int kOCol = kHM ? 2 * kTile : 2 * kParts * N;   // S buffers first
     static constexpr int kOBuf = kHM ? D : kOW;                      // columns of one O buffer
     static constexpr int kTmemCols = pow2_cols(kOCol + 3 * kOBuf);
@@ -705,6 +709,8 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
 #pragma unroll
                             for (int c = 0; c < C::kQBoxes; ++c)
                                 tma_load_2d(qdst + c * N * 128, &tm_q, c * kBoxCols, y, &qfull[qb], pol_q);
+                            if constexpr (C::kHM)   // the second copy: rows 64..127 of the A operand
+                                tma_load_2d(qdst + N * 128, &tm_q, 0, y, &qfull[qb], pol_q);
                             ++qissued;
                             if (i == 0) GQA_TRACE_AT(kTrFirstQ, clock64());
                         }
@@ -835,8 +841,8 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         // base descriptors once, then constant offsets (K step = 32 bytes in a box)
                         const uint64_t kd0 = sdesc_sw128(kb, 16, 1024), qd0 = sdesc_sw128(qbase, 16, 1024);
                         if constexpr (C::kHM) {
-                            // S [64 heads x 128 positions] = Q·K^T: Q is the A operand (d = 64: one K atom)
-                            constexpr uint32_t idS_hm = idesc_bf16_f32(64, kTile, false, false);
+                            // S [2 x 64 heads x 128 positions] = [Q; Q]·K^T: Q is the A operand (d = 64: one K atom)
+                            constexpr uint32_t idS_hm = idesc_bf16_f32(128, kTile, false, false);
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk)
                                 umma_bf16(tmem + bi * kTile, sdesc_add(qd0, kk * 32), sdesc_add(kd0, kk * 32), idS_hm,
@@ -918,29 +924,34 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
     } else if (warp < 6) {
         if constexpr (C::kHM) {
         // ================================================================ softmax, heads on M
-        // Thread (warp quadrant q4, lane < 16) owns head q4*16 + lane: the TMEM row of its
-        // scores and of its O accumulator.  Per tile: the tile maximum and the sums are
-        // per thread, so no barrier joins the softmax threads; P is written as whole
-        // 16-byte chunks of the head's row.
+        // S side: TMEM lane r = q4*32 + lane holds head hs = r % 64; its thread takes the
+        // positions of half hf = r / 64 of the tile.  The two threads of a head agree on the
+        // tile maximum through shared memory (one barrier per tile).  O side: the O
+        // accumulator of head ho = q4*16 + lane lives in TMEM lane q4*32 + lane (lanes < 16),
+        // folded by that thread with the rescale factors the S side publishes.
         const int q4 = warp & 3;
         const int tg = tid - 64;                 // 0..127 within the group (V row cleared by this thread)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const int hd = q4 * 16 + lane;
-        const bool has_head = lane < 16 && hd < n;
+        const int r = q4 * 32 + lane;
+        const int hs = r & 63, hf = r >> 6;      // S side: head and position half
+        const int ho = q4 * 16 + lane;           // O side: head (lanes < 16)
+        const bool has_out = lane < 16 && ho < n;
         zero_empty_sequences<D>(p, prefix, P, tg, 128);
+        GroupSync gsync{grp, 0};
         float accv[D];
-        float l_run = 0.f, m_run = 0.f, a0 = 0.f, a1 = 0.f, a2 = 0.f;   // rescale factors of tiles i, i-1, i-2
+        float l_half = 0.f, m_run = 0.f;
         int seq_b = 0, win_b = 0, piece_i0 = 0, npe = 0, i = 0, rr = 0;
         long long piece_u0 = 0;
         bool ok = true;
 #pragma unroll
         for (int j = 0; j < D; ++j) accv[j] = 0.f;
 
-        // fold O of tile t into accv with that tile's rescale factor
-        auto fold_hm = [&](int t, float al) -> bool {
+        // fold O of tile t into accv with that tile's rescale factor (published by the S side)
+        auto fold_hm = [&](int t) -> bool {
             const int ob = t % 3;
             if (!mbar_wait(&ofull[ob], (t / 3) & 1, ab)) return false;
             tc_fence_after_sync();
+            const float al = alpha_s[(t % 4) * NH + (ho & 63)];
             const uint32_t oc = tmem + lane_off + C::kOCol + ob * C::kOBuf;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -974,7 +985,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                 piece_i0 = i;
                 seq_b = seq_len_of(p, cur.b);
                 win_b = kExt ? window_start(p, seq_b) : 0;
-                l_run = 0.f;
+                l_half = 0.f;
 #pragma unroll
                 for (int j = 0; j < D; ++j) accv[j] = 0.f;
             }
@@ -984,35 +995,42 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
             const int tile_pos0 = ((win_b >> C::kTileShift) + cur.j) << C::kTileShift;
             const int hi_pos = seq_b - tile_pos0;              // >= 1
             const int lo_pos = kExt ? win_b - tile_pos0 : 0;   // > 0 only in a window's first tile
-            const uint32_t sc = tmem + lane_off + bi * kTile;
-            // pass 1: the tile maximum of this head
+            const uint32_t sc = tmem + lane_off + bi * kTile + hf * 64;
+            // pass 1: this half's maximum, then the head's from both halves
             float mt = -INFINITY;
 #pragma unroll
-            for (int c0 = 0; c0 < kTile; c0 += 32) {
+            for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t sv[32];
                 tmem_ld_32x32b<32>(sc + c0, sv);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const int pos = c0 + j;
+                    const int pos = hf * 64 + c0 + j;
                     if (pos < hi_pos && pos >= lo_pos) mt = fmaxf(mt, __uint_as_float(sv[j]) * p.scale_log2);
                 }
             }
-            const float m_new = (i == piece_i0) ? mt : fmaxf(m_run, mt);   // finite: every tile has a position
+            red[bi * 128 + r] = mt;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&redbar[bi]);
+            if (!mbar_wait(&redbar[bi], (i >> 1) & 1, ab)) { ok = false; break; }
+            const float mh = fmaxf(red[bi * 128 + hs], red[bi * 128 + hs + 64]);   // finite: a tile has a position
+            const float m_new = (i == piece_i0) ? mh : fmaxf(m_run, mh);
             const float alpha = (i == piece_i0) ? 0.f : ex2(m_run - m_new);
             m_run = m_new;
-            a2 = a1;
-            a1 = a0;
-            a0 = alpha;
+            if (hf == 0) {
+                alpha_s[(i % 4) * NH + hs] = alpha;
+                mrun_s[(i % 3) * NH + hs] = m_new;
+            }
             // P buffer i % PB last held P(i - PB): its value GEMM must be done with it
             const int pbi = i % PB;
             if (i >= PB && !mbar_wait(&ofull[(i - PB) % 3], ((i - PB) / 3) & 1, ab)) { ok = false; break; }
-            // pass 2: probabilities, the sum, and P row hd as bf16 hi (first 16 KB) + lo (next 16 KB),
-            // K-major with 128-byte swizzle: half pos/64, row hd, 16-byte chunk ((pos%64)/8) ^ (hd%8)
-            uint8_t *prow = smem + C::kOffP + pbi * C::kPBufBytes + hd * 128;
+            // pass 2: probabilities of this half, the half's sum, and P row hs, half hf, as bf16
+            // hi (first 16 KB) + lo (next 16 KB), K-major, 128-byte swizzle: 16-byte chunk
+            // (pos % 64) / 8 stored at chunk ((pos % 64) / 8) ^ (hs % 8)
+            uint8_t *prow = smem + C::kOffP + pbi * C::kPBufBytes + hf * 8192 + hs * 128;
             float sum = 0.f;
 #pragma unroll
-            for (int c0 = 0; c0 < kTile; c0 += 32) {
+            for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t sv[32];
                 tmem_ld_32x32b<32>(sc + c0, sv);
                 tmem_wait_ld();
@@ -1024,26 +1042,24 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         float pv[2];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const int j = g8 * 8 + j2 * 2 + e, pos = c0 + j;
+                            const int j = g8 * 8 + j2 * 2 + e, pos = hf * 64 + c0 + j;
                             pv[e] = (pos < hi_pos && pos >= lo_pos)
                                         ? ex2(__uint_as_float(sv[j]) * p.scale_log2 - m_new) : 0.f;
                             sum += pv[e];
                         }
                         const __nv_bfloat162 h2 = __floats2bfloat162_rn(pv[0], pv[1]);
-                        const float2 hf = __bfloat1622float2(h2);
-                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(pv[0] - hf.x, pv[1] - hf.y);
+                        const float2 hf2 = __bfloat1622float2(h2);
+                        const __nv_bfloat162 l2 = __floats2bfloat162_rn(pv[0] - hf2.x, pv[1] - hf2.y);
                         hw[j2] = *reinterpret_cast<const uint32_t *>(&h2);
                         lw[j2] = *reinterpret_cast<const uint32_t *>(&l2);
                     }
-                    if (lane < 16) {
-                        const int pos8 = c0 + g8 * 8;
-                        uint8_t *dst = prow + (pos8 >> 6) * 8192 + ((((pos8 & 63) >> 3) ^ (hd & 7)) << 4);
-                        *reinterpret_cast<uint4 *>(dst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4 *>(dst + 16384) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    }
+                    const int ch = (c0 + g8 * 8) >> 3;   // 16-byte chunk of the half row
+                    uint8_t *dst = prow + ((ch ^ (hs & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(dst + 16384) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
             }
-            l_run = fmaf(l_run, alpha, sum);
+            l_half = fmaf(l_half, alpha, sum);
             tc_fence_before_sync();
             mbar_arrive(&sfree[bi]);
             // ---- clear V rows outside [lo, hi) (they may hold anything, NaN included): row tg
@@ -1058,34 +1074,39 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
             }
             fence_proxy_async_smem();
             mbar_arrive(&pfull[pbi]);
-            // ---- fold O of the tile before the previous one
-            if (i - 2 >= piece_i0 && !fold_hm(i - 2, a2)) { ok = false; break; }
+            // ---- fold O of the tile before the previous one (its alpha was published two
+            // barriers ago)
+            if (i - 2 >= piece_i0 && !fold_hm(i - 2)) { ok = false; break; }
 
             if (last) {
                 if (tg == 0) GQA_TRACE_AT(kTrPieceEnd + 2 * npe, clock64());
-                if (i - 1 >= piece_i0 && !fold_hm(i - 1, a1)) { ok = false; break; }
-                if (!fold_hm(i, a0)) { ok = false; break; }
+                lred[r] = l_half;
+                if (!gsync(ab)) { ok = false; break; }        // also publishes tile i's alpha and m
+                if (i - 1 >= piece_i0 && !fold_hm(i - 1)) { ok = false; break; }
+                if (!fold_hm(i)) { ok = false; break; }
                 const int seg = cur.b * G + cur.g;
                 const long long seg_a = (long long)G * prefix[cur.b] + (long long)cur.g * cur.tiles;
                 const bool owned = (piece_u0 == seg_a) && (cur.j + 1 == cur.tiles);
-                if (has_head) {
+                if (has_out) {
+                    const float L = lred[ho] + lred[ho + 64];
                     if (owned) {
-                        float4 *o4 = reinterpret_cast<float4 *>(p.out + ((size_t)cur.b * p.H + (size_t)cur.g * n + hd) * D);
+                        float4 *o4 = reinterpret_cast<float4 *>(p.out + ((size_t)cur.b * p.H + (size_t)cur.g * n + ho) * D);
 #pragma unroll
                         for (int c = 0; c < D / 4; ++c)
-                            o4[c] = make_float4(accv[4 * c] / l_run, accv[4 * c + 1] / l_run, accv[4 * c + 2] / l_run,
-                                                accv[4 * c + 3] / l_run);
+                            o4[c] = make_float4(accv[4 * c] / L, accv[4 * c + 1] / L, accv[4 * c + 2] / L,
+                                                accv[4 * c + 3] / L);
                     } else {
                         const int slot = range.chunk < 0 ? (int)blockIdx.x + seg : chunk_slot(p, range.chunk, range_piece);
                         float *sp = slot_ptr(p, slot, D);
-                        sp[hd] = m_run;
-                        sp[n + hd] = l_run;
-                        float4 *a4 = reinterpret_cast<float4 *>(sp + slot_acc_offset(n) + hd * D);
+                        sp[ho] = mrun_s[(i % 3) * NH + ho];
+                        sp[n + ho] = L;
+                        float4 *a4 = reinterpret_cast<float4 *>(sp + slot_acc_offset(n) + ho * D);
 #pragma unroll
                         for (int c = 0; c < D / 4; ++c)
                             a4[c] = make_float4(accv[4 * c], accv[4 * c + 1], accv[4 * c + 2], accv[4 * c + 3]);
                     }
                 }
+                // lred is next written at the next piece's end, after that piece's barriers
                 if (tg == 0) GQA_TRACE_AT(kTrPieceEnd + 2 * npe + 1, clock64());
                 ++npe;
                 ++range_piece;
