@@ -41,14 +41,27 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from kv_cache_decode_06_b300.inputs import (  # noqa: E402
-    CONFIGS, T5XXL_SWEEP_GS, make_decode_inputs, make_new_rows, make_paged_layout,
+    CONFIGS, MEANPOOL_T5XXL, MEANPOOL_TINY, T5XXL_SWEEP_GS, make_decode_inputs, make_meanpool_input,
+    make_new_rows, make_paged_layout,
 )
 
 METRIC = "GQA decode KV-cache HBM GB/s (% of B300 peak) and decode steps/s, 1 GPU"
+MEANPOOL_METRIC = "GQA K/V mean-pool conversion HBM GB/s (% of B300 peak), 1 GPU"
 UNIT = "GB/s"
 L2_COPIES_SPAN = 3            # L2 capacities streamed between two reads of one cache copy
 CPU_BASELINE_SECONDS = 10.0   # host time spent on the float64 oracle for the cpu_baseline field
 FALLBACK_HBM_GBS = 6400.0
+
+
+def meanpool_workload(name: str):
+    """Shape of one mean-pool conversion (one projection of one layer)."""
+    if name == "tiny":
+        return "meanpool_tiny", dict(MEANPOOL_TINY)
+    if name.startswith("t5xxl_sweep_G"):
+        d = dict(MEANPOOL_T5XXL)
+        d["G"] = int(name.split("_G")[1])
+        return f"meanpool_t5xxl_G{d['G']}", d
+    raise SystemExit(f"--variant meanpool takes --workload tiny or t5xxl_sweep_G<g>, not {name}")
 
 
 def workload(name: str):
@@ -67,13 +80,25 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+# Source files of a kernel that has a file of its own; every other kernel is
+# hashed over all of csrc except those files.
+KERNEL_SOURCES = {"meanpool_kernel": ("meanpool.cu", "launch.h")}
+
+
+def kernel_source_hash(kernel: str = "gqa_decode_tc_kernel") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kv_cache_decode_06_b300", "csrc")
+    own = {fn for srcs in KERNEL_SOURCES.values() for fn in srcs if fn.endswith(".cu")}
     for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
+        if not fn.endswith((".cu", ".cuh", ".h")):
+            continue
+        if kernel in KERNEL_SOURCES:
+            if fn not in KERNEL_SOURCES[kernel]:
+                continue
+        elif fn in own:
+            continue
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -85,7 +110,7 @@ def profiled_traffic(kernel: str, wl: str):
     except OSError:
         return None
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)\s+source_hash:\s*([0-9a-f]+)", txt)
-    if not m or m.group(2) != kernel_source_hash():
+    if not m or m.group(2) != kernel_source_hash(kernel):
         return None
     return float(m.group(1))
 
@@ -186,7 +211,10 @@ def run_reference(args, rank: int) -> None:
     if rank != 0:
         return
     import oracle
-    cfg = workload(args.workload)
+    if args.variant == "meanpool":
+        run_reference_meanpool(args)
+        return
+    cfg = workload(args.workload or "mistral7b")
     inp = make_decode_inputs(cfg, poison_tail=False)
     nrows_all = cfg.B * cfg.H
     cores = oracle.num_threads()
@@ -214,6 +242,33 @@ def run_reference(args, rank: int) -> None:
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{nrow} of {nrows_all} output rows (query heads of sequences) per step, "
                                    f"seeded order, float64 oracle (OpenMP over rows)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_meanpool(args) -> None:
+    """The fp32 mean-pool oracle as the reference arm: one whole conversion per step."""
+    import oracle
+    name, shp = meanpool_workload(args.workload or "t5xxl_sweep_G8")
+    H, G, h, dm = shp["H"], shp["G"], shp["h"], shp["d_model"]
+    w_h = make_meanpool_input(H, G, h, dm, shp["config_id"])
+    alg = w_h.nbytes + G * h * dm * 4
+    for _ in range(args.warmup):
+        oracle.meanpool_f32(w_h, H, G)
+    total_t = 0.0
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.meanpool_f32(w_h, H, G)
+        total_t += time.perf_counter() - t
+    value = args.steps * alg / total_t / 1e9
+    line = {
+        "metric": MEANPOOL_METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
+        "config": {"workload": name, "H": H, "G": G, "h": h, "d_model": dm, "bytes_per_step": alg},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "one whole conversion per step, fp32 oracle (one thread)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -253,20 +308,123 @@ def config_dict(cfg, inp, extra=None):
     return d
 
 
+def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
+    """Times gqa_meanpool_kv: [H, h, d_model] fp32 -> [G, h, d_model] fp32, one call per step."""
+    name, shp = meanpool_workload(args.workload or "t5xxl_sweep_G8")
+    H, G, h, dm = shp["H"], shp["G"], shp["h"], shp["d_model"]
+    w_h = make_meanpool_input(H, G, h, dm, shp["config_id"])
+    in_bytes, out_bytes = w_h.nbytes, G * h * dm * 4
+    alg = in_bytes + out_bytes                  # each input read once, each output written once
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(3, math.ceil(L2_COPIES_SPAN * l2 / alg) + 1)
+    w = torch.from_numpy(w_h).to(dev)
+    ws = [w] + [w.clone() for _ in range(copies - 1)]
+    outs = [torch.empty((G, h, dm), dtype=torch.float32, device=dev) for _ in range(copies)]
+
+    def step(i):
+        c = i % copies
+        gqa.meanpool_kv(ws[c], G, out=outs[c], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = max_over_ranks(float(t0.elapsed_time(t1)), world, dev)
+    ms_per_step = total_ms / args.steps
+    value = whole_job_gbs(alg, args.steps, world, total_ms)
+
+    hw = torch.from_numpy(w_h).pin_memory()
+    hout = torch.empty((G, h, dm), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        w.copy_(hw, non_blocking=True)
+        gqa.meanpool_kv(w, G, out=outs[0], stream=stream)
+        hout.copy_(outs[0], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    if rank != 0:
+        return
+
+    peak, peak_kind = measured_peak()
+    achieved = alg / (ms_per_step / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.meanpool_f32(w_h, H, G)               # warm: page faults
+        total_t, passes = 0.0, 0
+        while total_t < CPU_BASELINE_SECONDS / 4 and passes < 10000:
+            t = time.perf_counter()
+            oracle.meanpool_f32(w_h, H, G)
+            total_t += time.perf_counter() - t
+            passes += 1
+        cpu = {"value": passes * alg / total_t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{passes} whole conversion(s) of the same projection, fp32 oracle (one thread), "
+                         f"{total_t:.1f} s after one warm-up pass"}
+    line = {
+        "metric": MEANPOOL_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": name, "H": H, "G": G, "h": h, "d_model": dm,
+                   "layout": "[H, h, d_model] -> [G, h, d_model] fp32, head-major",
+                   "bytes_per_step": alg, "inputs": "N(0,1) float32, seeded",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU", "copies": copies,
+                   "l2": f"inputs larger than L2: {copies} input/output copies, step i uses copy i % {copies}"
+                         if copies * alg > l2 else "fits in L2: launch-bound, not an HBM figure",
+                   "timing": "K calls back to back between one pair of CUDA events"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": profiled_traffic("meanpool_kernel", name), "kernel": "meanpool_kernel",
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+                     "algorithmic_bytes_per_launch": alg, "frac_of_8TBps_nominal": achieved / 8000.0},
+        "cpu_baseline": cpu,
+        "e2e": {"value": alg / (e2e_ms / 1e3) / 1e9 * world, "unit": UNIT, "h2d_bytes_per_step": in_bytes,
+                "d2h_bytes_per_step": out_bytes, "steps": args.e2e_steps,
+                "what": "H2D of the projection from pinned host memory + the conversion + D2H of the result"},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--workload", default="mistral7b",
-                    help="mistral7b | llama3_70b | long_ragged | tiny | t5xxl_sweep_G<1..64>")
+    ap.add_argument("--workload", default=None,
+                    help="mistral7b (default) | llama3_70b | long_ragged | tiny | t5xxl_sweep_G<1..64>; "
+                         "--variant meanpool: tiny | t5xxl_sweep_G<g> (default t5xxl_sweep_G8)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 simt, 2 tcgen05")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--variant", default="contiguous", choices=["contiguous", "paged", "append", "cross", "window"],
+    ap.add_argument("--variant", default="contiguous",
+                    choices=["contiguous", "paged", "append", "cross", "window", "meanpool"],
                     help="contiguous cache (default); paged cache (--page-size); fused append of the new "
-                         "token's K/V rows; cross-attention (every position valid); sliding window (--window)")
+                         "token's K/V rows; cross-attention (every position valid); sliding window (--window); "
+                         "meanpool: the K/V mean-pool conversion instead of the decode")
     ap.add_argument("--page-size", type=int, default=64)
     ap.add_argument("--window", type=int, default=1024)
     args = ap.parse_args()
@@ -291,8 +449,13 @@ def main() -> None:
     dev = torch.device("cuda", local_rank)
     build_lib.build()
     gqa.load()
+    if args.variant == "meanpool":
+        run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
-    cfg = workload(args.workload)
+    cfg = workload(args.workload or "mistral7b")
     variant = args.variant
     if variant == "cross":   # every one of the Lmax positions is valid
         inp = make_decode_inputs(cfg, poison_tail=False, seq_lens=[cfg.Lmax] * cfg.B)

@@ -6,7 +6,7 @@
 // addition and the division rounded in fp32 in that order, so the result is
 // bit-identical to that sequence.  One pass over HBM: each input element is
 // read once, each output element written once, 16-byte accesses when the
-// layout allows.
+// layout allows; each thread keeps up to 8 loads in flight.
 #include <cuda_runtime.h>
 
 #include "launch.h"
@@ -15,36 +15,39 @@ namespace gqa {
 
 namespace {
 
-__global__ void meanpool_vec4_kernel(const float4 *__restrict__ w, float4 *__restrict__ out, long long outer,
-                                     int H, int G, long long inner4) {
-    const int n = H / G;
-    const float fn = (float)n;
-    const long long total = outer * G * inner4;
-    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
-         e += (long long)gridDim.x * blockDim.x) {
-        const long long x = e % inner4;
-        const long long og = e / inner4;
-        const int g = (int)(og % G);
-        const long long o = og / G;
-        const float4 *src = w + ((o * H + (long long)g * n) * inner4 + x);
-        float4 acc = __ldg(src);
-        for (int j = 1; j < n; ++j) {
-            const float4 y = __ldg(src + (long long)j * inner4);
-            acc.x = __fadd_rn(acc.x, y.x);
-            acc.y = __fadd_rn(acc.y, y.y);
-            acc.z = __fadd_rn(acc.z, y.z);
-            acc.w = __fadd_rn(acc.w, y.w);
-        }
-        acc.x = __fdiv_rn(acc.x, fn);
-        acc.y = __fdiv_rn(acc.y, fn);
-        acc.z = __fdiv_rn(acc.z, fn);
-        acc.w = __fdiv_rn(acc.w, fn);
-        out[e] = acc;
-    }
+// Loads in flight per thread: the n terms of one output are fetched in batches
+// of kBatch independent loads, then added in head order.
+constexpr int kBatch = 8;
+
+__device__ __forceinline__ float4 add4_rn(float4 a, float4 b) {
+    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
 }
 
-__global__ void meanpool_scalar_kernel(const float *__restrict__ w, float *__restrict__ out, long long outer,
-                                       int H, int G, long long inner) {
+// T is float4 (16-byte accesses) or float.  The first term is assigned, not
+// added to zero, so a -0.0 input keeps its sign as in the plain sequence.
+template <typename T>
+__device__ __forceinline__ T fold_heads(const T *__restrict__ src, long long stride, int n) {
+    T acc{};
+    for (int j0 = 0; j0 < n; j0 += kBatch) {
+        T y[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            if (j0 + u < n) y[u] = __ldg(src + (long long)(j0 + u) * stride);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            if (j0 + u >= n) break;
+            if constexpr (sizeof(T) == 16)
+                acc = (j0 + u == 0) ? y[u] : add4_rn(acc, y[u]);
+            else
+                acc = (j0 + u == 0) ? y[u] : __fadd_rn(acc, y[u]);
+        }
+    }
+    return acc;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) meanpool_kernel(const T *__restrict__ w, T *__restrict__ out,
+                                                       long long outer, int H, int G, long long inner) {
     const int n = H / G;
     const float fn = (float)n;
     const long long total = outer * G * inner;
@@ -54,34 +57,45 @@ __global__ void meanpool_scalar_kernel(const float *__restrict__ w, float *__res
         const long long og = e / inner;
         const int g = (int)(og % G);
         const long long o = og / G;
-        const float *src = w + ((o * H + (long long)g * n) * inner + x);
-        float acc = __ldg(src);
-        for (int j = 1; j < n; ++j) acc = __fadd_rn(acc, __ldg(src + (long long)j * inner));
-        out[e] = __fdiv_rn(acc, fn);
+        T acc = fold_heads(w + ((o * H + (long long)g * n) * inner + x), inner, n);
+        if constexpr (sizeof(T) == 16)
+            acc = make_float4(__fdiv_rn(acc.x, fn), __fdiv_rn(acc.y, fn), __fdiv_rn(acc.z, fn),
+                              __fdiv_rn(acc.w, fn));
+        else
+            acc = __fdiv_rn(acc, fn);
+        out[e] = acc;
     }
+}
+
+template <typename T>
+cudaError_t launch_typed(const T *w_in, T *w_out, long long outer, int H, int G, long long inner,
+                         cudaStream_t stream) {
+    const long long total = outer * G * inner;
+    if (total == 0) return cudaSuccess;
+    constexpr int threads = 256;
+    int dev = 0, sms = 148, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, meanpool_kernel<T>, threads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    // one resident wave: every SM holds the same number of blocks
+    long long blocks = (total + threads - 1) / threads;
+    const long long cap = (long long)sms * per_sm;
+    if (blocks > cap) blocks = cap;
+    meanpool_kernel<T><<<(int)blocks, threads, 0, stream>>>(w_in, w_out, outer, H, G, inner);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_meanpool(const float *w_in, float *w_out, long long outer, int H, int G, long long inner,
                             cudaStream_t stream) {
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const bool vec = (inner % 4 == 0) && ((reinterpret_cast<uintptr_t>(w_in) | reinterpret_cast<uintptr_t>(w_out)) % 16 == 0);
-    const long long total = outer * G * (vec ? inner / 4 : inner);
-    if (total == 0) return cudaSuccess;
-    const int threads = 256;
-    long long blocks = (total + threads - 1) / threads;
-    const long long cap = (long long)sms * 8;
-    if (blocks > cap) blocks = cap;
     if (vec)
-        meanpool_vec4_kernel<<<(int)blocks, threads, 0, stream>>>(reinterpret_cast<const float4 *>(w_in),
-                                                                  reinterpret_cast<float4 *>(w_out), outer, H, G,
-                                                                  inner / 4);
-    else
-        meanpool_scalar_kernel<<<(int)blocks, threads, 0, stream>>>(w_in, w_out, outer, H, G, inner);
-    return cudaGetLastError();
+        return launch_typed(reinterpret_cast<const float4 *>(w_in), reinterpret_cast<float4 *>(w_out), outer, H, G,
+                            inner / 4, stream);
+    return launch_typed(w_in, w_out, outer, H, G, inner, stream);
 }
 
 }  // namespace gqa

@@ -94,6 +94,10 @@ CONFIGS = {c.name: c for c in (TINY, MISTRAL_7B, T5XXL_SWEEP, LLAMA3_70B, LONG_R
 # Mean-pool conversion workload: a random fp32 K (or V) projection stored
 # head-major [H, h, d_model] = [8, 64, 512], pooled to [G=2, 64, 512].
 MEANPOOL_TINY = dict(H=8, G=2, h=64, d_model=512, config_id=0)
+# Checkpoint-sized conversion: one K (or V) projection of T5-XXL, 64 heads of
+# 64 over a 4096-wide model (64 MiB fp32), pooled to G groups (G = 8 in the
+# GQA paper's main setting).
+MEANPOOL_T5XXL = dict(H=64, G=8, h=64, d_model=4096, config_id=2)
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:

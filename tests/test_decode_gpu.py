@@ -207,13 +207,40 @@ def test_meanpool_bit_exact_tiny_workload():
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("H,G,h,dm", [(8, 8, 16, 32), (8, 1, 16, 32), (12, 4, 8, 24), (6, 2, 5, 7), (64, 8, 128, 64)])
+@pytest.mark.parametrize("H,G,h,dm", [(8, 8, 16, 32), (8, 1, 16, 32), (12, 4, 8, 24), (6, 2, 5, 7), (64, 8, 128, 64),
+                                      (20, 2, 4, 16), (24, 2, 5, 7), (64, 4, 8, 16), (64, 1, 8, 16), (72, 1, 3, 5)])
 def test_meanpool_bit_exact_shapes(H, G, h, dm):
     from kv_cache_decode_06_b300.inputs import make_meanpool_input
     w = make_meanpool_input(H, G, h, dm, config_id=7)
     got = gqa.meanpool_kv(torch.from_numpy(w).cuda(), G).cpu().numpy()
     ref = oracle.meanpool_f32(w, H, G)
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("G", [8, 1])
+def test_meanpool_bit_exact_t5xxl_checkpoint(G):
+    """One T5-XXL-sized projection [64, 64, 4096] (64 MiB), pooled to 8 groups and to 1."""
+    from kv_cache_decode_06_b300.inputs import MEANPOOL_T5XXL, make_meanpool_input
+    c = MEANPOOL_T5XXL
+    w = make_meanpool_input(c["H"], G, c["h"], c["d_model"], c["config_id"])
+    got = gqa.meanpool_kv(torch.from_numpy(w).cuda(), G).cpu().numpy()
+    ref = oracle.meanpool_f32(w, c["H"], G)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("H,G", [(4, 1), (16, 1), (12, 2)])
+def test_meanpool_special_values(H, G):
+    """Signed zeros, infinities, NaN and subnormals: the same IEEE results as the fp32 sequence."""
+    rng = np.random.default_rng(H * 10 + G)
+    specials = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-40, -1e-40, 3.4e38, 1.0], dtype=np.float32)
+    w = specials[rng.integers(0, len(specials), size=(H, 8, 64))].astype(np.float32)
+    w[:, 0, :] = -0.0                                  # every head -0.0: the mean keeps the sign
+    got = gqa.meanpool_kv(torch.from_numpy(w).cuda(), G).cpu().numpy()
+    ref = oracle.meanpool_f32(w, H, G)
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+    assert np.all(np.signbit(got[:, 0, :]))
 
 
 def test_meanpool_pages_layout_bit_exact():
