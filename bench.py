@@ -12,8 +12,12 @@ copy stream at least three L2 capacities of other data; no step finds its
 cache in L2.  (A write-flush between steps is not used: the dirty lines it
 leaves slow the next kernel down by write-back traffic that is not its own.)
 The K steps run back to back on one stream between one pair of CUDA events;
-the step is a single kernel launch, so total time / K is that kernel's average
-launch-to-launch duration.
+a step is the decode kernel plus the split-combine kernel that follows it
+(programmatic dependent launch), so total time / K is the average duration of
+one whole step.
+
+``--variant meanpool`` times the K/V mean-pool conversion instead (one call per
+step on one projection; GB/s counts its input and output bytes).
 
 Under torchrun (N > 1) every rank runs an independent replica of the step on
 its own GPU (nothing is sharded); value = bytes of all ranks / max time.

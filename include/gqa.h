@@ -280,6 +280,15 @@ gqa_status gqa_decode_noalloc(const void *q, const void *k_cache, const void *v_
  * nearest), in that order: the result is bit-identical to that sequence.
  * Call it once for W_K and once for W_V; the query and output projections are
  * left unchanged by the conversion.
+ *
+ * Asynchronous on `stream` (one kernel, no allocation, no synchronisation).
+ * w_in and w_out must not overlap.  Rows of 16-byte aligned pointers with
+ * h*d_model a multiple of 4 are read and written 16 bytes at a time; any
+ * 4-byte aligned layout is accepted.
+ * Returns GQA_ERR_INVALID_ARG (nothing enqueued) for a NULL pointer, H, G, h or
+ * d_model <= 0, G > H, H not a multiple of G, or a pointer that is not 4-byte
+ * aligned; GQA_ERR_DEVICE if no CUDA device is current; GQA_ERR_LAUNCH if the
+ * kernel launch fails.
  */
 gqa_status gqa_meanpool_kv(const float *w_in, float *w_out, int H, int G, int h, int d_model,
                            void *stream);
