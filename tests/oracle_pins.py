@@ -445,6 +445,24 @@ def check_meanpool_small_integers(lib):
     assert oracle.meanpool_f32(w3, 3, 1, lib=lib)[0, 0, 0] == np.float32(7.0) / np.float32(3.0)
 
 
+def check_meanpool_fp32_head_order(lib):
+    """The fp32 sum runs in increasing head order, rounding after every addition.
+
+    Heads holding 1e8, 1, -1e8, 1 (all exact in fp32; the spacing of fp32 values
+    near 1e8 is 8): in head order 1e8 + 1 rounds to 1e8, + (-1e8) gives 0, + 1
+    gives 1, and 1 / 4 = 0.25.  Summing in reverse gives 0 (1 - 1e8 rounds to
+    -1e8), summing in pairs gives 0, and an exact (or float64) sum gives 0.5, so
+    only the stated order reaches 0.25.  The float64 twin gives the exact 0.5.
+    """
+    w = np.array([1e8, 1.0, -1e8, 1.0], dtype=np.float32).reshape(4, 1, 1)
+    assert oracle.meanpool_f32(w, 4, 1, lib=lib)[0, 0, 0] == np.float32(0.25)
+    assert oracle.meanpool_f64(w, 4, 1, lib=lib)[0, 0, 0] == 0.5
+    # the same four heads as the second group of two, behind a group of zeros
+    w2 = np.concatenate([np.zeros((4, 1, 1), np.float32), w])
+    got = oracle.meanpool_f32(w2, 8, 2, lib=lib)[:, 0, 0]
+    assert got[0] == 0.0 and got[1] == np.float32(0.25)
+
+
 def check_meanpool_pages_layout(lib):
     """The pages' [d_model, H*h] layout (head i = columns i*h..(i+1)*h-1) pools to
     [d_model, G*h], the transpose of the head-major result."""
@@ -474,5 +492,5 @@ VARIANT_CHECKS = [
 ]
 MEANPOOL_CHECKS = [
     check_meanpool_identical_heads, check_meanpool_identity_and_mean,
-    check_meanpool_small_integers, check_meanpool_pages_layout,
+    check_meanpool_small_integers, check_meanpool_pages_layout, check_meanpool_fp32_head_order,
 ]

@@ -243,6 +243,16 @@ def test_meanpool_special_values(H, G):
     assert np.all(np.signbit(got[:, 0, :]))
 
 
+@pytest.mark.parametrize("inner", [1, 4])
+def test_meanpool_fp32_head_order(inner):
+    """Heads 1e8, 1, -1e8, 1 pool to 0.25 only when summed in head order with fp32 rounding
+    after every addition (reverse order gives 0, an exact sum 0.5); inner 1 takes the scalar
+    kernel, inner 4 the float4 one."""
+    w = np.repeat(np.array([1e8, 1.0, -1e8, 1.0], dtype=np.float32).reshape(4, 1, 1), inner, axis=2)
+    got = gqa.meanpool_kv(torch.from_numpy(np.ascontiguousarray(w)).cuda(), 1).cpu().numpy()
+    assert np.all(got == np.float32(0.25))
+
+
 def test_meanpool_pages_layout_bit_exact():
     """The pages' [d_model, H*h] projection pooled per column block."""
     from kv_cache_decode_06_b300.inputs import make_meanpool_input

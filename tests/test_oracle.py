@@ -55,6 +55,15 @@ MUTANTS = {
     "exp_of_unshifted_sum": ("l += s[t];", "l += s[t] * s[t];"),
     "meanpool_divides_by_H": ("out[(o * G + g) * inner + x] = acc / (float)n;",
                               "out[(o * G + g) * inner + x] = acc / (float)H;"),
+    "meanpool_reverse_head_order": (
+        "float acc = w[(o * H + (int64_t)g * n) * inner + x];\n"
+        "                for (int j = 1; j < n; ++j)\n"
+        "                    acc = acc + w[(o * H + (int64_t)g * n + j) * inner + x];",
+        "float acc = w[(o * H + (int64_t)g * n + n - 1) * inner + x];\n"
+        "                for (int j = 1; j < n; ++j)\n"
+        "                    acc = acc + w[(o * H + (int64_t)g * n + n - 1 - j) * inner + x];"),
+    "meanpool_sums_in_double": ("float acc = w[(o * H + (int64_t)g * n) * inner + x];",
+                                "double acc = w[(o * H + (int64_t)g * n) * inner + x];"),
     "meanpool_drops_last_member": ("for (int j = 1; j < n; ++j)\n                    acc = acc + w",
                                    "for (int j = 1; j < n - 1; ++j)\n                    acc = acc + w"),
 }
