@@ -190,6 +190,14 @@ def test_meanpool_rejects(gqa_lib):
     assert lib.gqa_meanpool_kv(FAKE, FAKE, 8, 2, 0, 512, None) == 1
     assert lib.gqa_meanpool_kv_strided(FAKE, FAKE, 0, 8, 2, 64, None) == 1
     assert lib.gqa_meanpool_kv_strided(FAKE + 2, FAKE, 1, 8, 2, 64, None) == 1
+    assert lib.gqa_meanpool_kv_strided(FAKE, FAKE + 2, 1, 8, 2, 64, None) == 1   # w_out not 4-byte aligned
+    assert lib.gqa_meanpool_kv_strided(FAKE, FAKE, 1, 8, 2, 0, None) == 1
+    assert lib.gqa_meanpool_kv_strided(FAKE, FAKE, 1, 8, 2, -4, None) == 1
+    assert lib.gqa_meanpool_kv(FAKE, FAKE, 8, 2, 64, 0, None) == 1                 # d_model <= 0
+    assert lib.gqa_meanpool_kv(FAKE, FAKE, 8, 2, -1, 512, None) == 1
+    assert lib.gqa_meanpool_kv(FAKE, FAKE, 0, 1, 64, 512, None) == 1               # H <= 0
+    assert lib.gqa_meanpool_kv(FAKE, FAKE, 8, 0, 64, 512, None) == 1               # G <= 0
+    assert lib.gqa_meanpool_kv(FAKE, FAKE, -8, -2, 64, 512, None) == 1
 
 
 def test_read_flags_rejects(gqa_lib):
