@@ -106,6 +106,8 @@ def _stream_handle(stream: Optional[torch.cuda.Stream], device: torch.device) ->
 def _require(t: torch.Tensor, name: str, dtype: torch.dtype, device: torch.device) -> None:
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device.type != "cuda":   # the library takes device pointers only
+        raise ValueError(f"{name} must be a CUDA tensor, got {t.device}")
     if t.device != device:
         raise ValueError(f"{name} must be on {device}, got {t.device}")
     if not t.is_contiguous():

@@ -209,3 +209,18 @@ def test_read_flags_rejects(gqa_lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         gqa.load(str(tmp_path / "missing.so"))
+
+
+def test_binding_rejects_host_tensors():
+    """Host tensors never reach the library (it takes device pointers only)."""
+    import torch
+    from kv_cache_decode_06_b300 import gqa
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gqa.meanpool_kv(torch.zeros((8, 4, 16)), 2)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gqa.meanpool_kv_strided(torch.zeros((3, 8, 16)), 2)
+    q = torch.zeros((1, 8, 64), dtype=torch.bfloat16)
+    kv = torch.zeros((1, 2, 128, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gqa.decode(q, kv, kv, torch.full((1,), 128, dtype=torch.int32))
+
