@@ -64,6 +64,8 @@ MUTANTS = {
         "                    acc = acc + w[(o * H + (int64_t)g * n + n - 1 - j) * inner + x];"),
     "meanpool_sums_in_double": ("float acc = w[(o * H + (int64_t)g * n) * inner + x];",
                                 "double acc = w[(o * H + (int64_t)g * n) * inner + x];"),
+    "meanpool_interleaved_groups": ("acc = acc + w[(o * H + (int64_t)g * n + j) * inner + x];",
+                                    "acc = acc + w[(o * H + (int64_t)j * G + g) * inner + x];"),
     "meanpool_drops_last_member": ("for (int j = 1; j < n; ++j)\n                    acc = acc + w",
                                    "for (int j = 1; j < n - 1; ++j)\n                    acc = acc + w"),
 }
