@@ -27,6 +27,9 @@
  *   - Thread safety: calls from several host threads are safe; two calls that
  *     share a workspace must not overlap on the device (calls on one stream
  *     never do).
+ *   - Per-device facts (SM count, kernel attributes, the no-alloc scratch
+ *     address) are looked up on the first call on each device and kept for the
+ *     life of the process: do not use the library across a cudaDeviceReset.
  */
 #ifndef GQA_B300_GQA_H
 #define GQA_B300_GQA_H
@@ -38,7 +41,14 @@
 extern "C" {
 #endif
 
-#define GQA_ABI_VERSION 1
+#define GQA_ABI_VERSION 2
+
+/* scale value that selects 1/sqrt(d) (see gqa_decode). */
+#define GQA_SCALE_DEFAULT 0.0f
+
+/* Leading bytes of a decode workspace that hold its counters (see
+ * gqa_decode_workspace_size); the same for every shape. */
+#define GQA_WORKSPACE_HEADER_BYTES 256u
 
 typedef enum gqa_status {
     GQA_OK = 0,
@@ -77,15 +87,17 @@ int gqa_abi_version(void);
  * Writes *bytes and returns GQA_OK, or returns the status gqa_decode would
  * return for the same shape.
  *
- * Layout: a 256-byte header (the flag word, the claim ticket and the failed-
- * claim count of the dynamic work pool) followed by the split-combine partial
- * results (one (m, l, acc) triple per query head per piece of a sequence).
+ * Layout: GQA_WORKSPACE_HEADER_BYTES of counters (the flag word, the claim
+ * ticket and the failed-claim count of the dynamic work pool), then the
+ * split-combine partial results (one (m, l, acc) triple per query head per
+ * piece of a sequence).
  * It MUST be zero-filled before its first use (for example
- * cudaMemsetAsync(ws, 0, bytes, stream)) so that the header starts clear.
- * Every call leaves the two pool counters at zero again, so nothing needs
- * resetting between calls, whatever their shapes — except after a call that
- * set GQA_FLAG_WAIT_TIMEOUT: zero the header (its first 256 bytes) again before
- * the next call.  The flag word is only ever OR-ed into.
+ * cudaMemsetAsync(ws, 0, bytes, stream)) so that the counters start clear.
+ * Every call leaves the two pool counters at zero again, so nothing needs resetting
+ * between calls, whatever their shapes (one workspace of the largest size
+ * serves them all) — except after a call that set GQA_FLAG_WAIT_TIMEOUT: zero
+ * the first GQA_WORKSPACE_HEADER_BYTES again before the next call.  The flag
+ * word is only ever OR-ed into.
  */
 gqa_status gqa_decode_workspace_size(int B, int H, int G, int d, int Lmax, size_t *bytes);
 
@@ -120,7 +132,10 @@ gqa_status gqa_decode_workspace_size(int B, int H, int G, int d, int Lmax, size_
  * H, G      H >= G >= 1, H % G == 0, H/G <= 64
  * d         head dimension: 64 or 128
  * Lmax      >= 1, cache capacity per sequence, at most 2^24; B*G*ceil(Lmax/128) <= 2^30
- * scale     score scale, normally 1/sqrt(d), used as given (fp32)
+ * scale     score scale (fp32), finite.  GQA_SCALE_DEFAULT (0) selects 1/sqrt(d),
+ *           the pages' scale ["Grouped-query attention (GQA)" concept page,
+ *           "Implementation sketch": scores divided by sqrt(h)], rounded once to
+ *           fp32; any other value is used as given.
  *
  * Arithmetic: exact bf16 products accumulated in fp32, softmax in fp32 with a
  * running maximum, fp32 output.  Measured against a float64 evaluation of the
@@ -130,8 +145,9 @@ gqa_status gqa_decode_workspace_size(int B, int H, int G, int d, int Lmax, size_
  * Two kernels are enqueued: the split decode kernel and the split-combine
  * kernel that merges the sequences the work split cut across thread blocks.
  * Both use programmatic stream serialisation: each may start its on-chip
- * set-up while the previous kernel on `stream` drains, and touches global
- * memory only after that kernel has completed.
+ * set-up while the previous kernel on `stream` drains (the split-combine sits
+ * beside the decode kernel's blocks, the next decode beside the split-combine's),
+ * and touches global memory only after that kernel has completed.
  */
 gqa_status gqa_decode(const void *q, const void *k_cache, const void *v_cache,
                       const int32_t *seq_lens, float *out,
@@ -218,17 +234,21 @@ gqa_status gqa_decode_paged(const void *q, void *k_pages, void *v_pages, const i
  * GQA_PATH_TCGEN05), or a negative gqa_status if the shape is rejected. */
 int gqa_decode_select_path(int B, int H, int G, int d, int Lmax);
 
+#ifdef GQA_TEST_HOOKS
 /*
- * Test hook for the failure path.  In the next decode call on the tensor-core
- * path (any thread, any entry point), thread block 0 skips its K copy number
- * `tile` (counted from 0 in its own copy order): nothing ever arrives on that
- * copy's barrier, so the score GEMM's bounded wait runs out after about one
- * second, the block abandons its work, GQA_FLAG_WAIT_TIMEOUT is set in the
- * workspace flag word and the call's output is invalid.  The context stays
- * usable; zero the workspace header before the next call.  A negative `tile`
+ * Test hook for the failure path, exported only by the test-hooks build of the
+ * library (compiled with -DGQA_TEST_HOOKS; the product build has neither the
+ * symbol nor the check in its kernels).  In the next decode call on the
+ * tensor-core path (any thread, any entry point), thread block 0 skips its K
+ * copy number `tile` (counted from 0 in its own copy order): nothing ever
+ * arrives on that copy's barrier, so the score GEMM's bounded wait runs out
+ * after about one second, the block abandons its work, GQA_FLAG_WAIT_TIMEOUT is
+ * set in the workspace flag word and the call's output is invalid.  The context
+ * stays usable; zero the workspace before the next call.  A negative `tile`
  * cancels a pending request.
  */
 void gqa_debug_withhold_copy(int tile);
+#endif
 
 /*
  * Copy the workspace flag word (GQA_FLAG_* bits, OR-ed by earlier decode calls)
@@ -253,10 +273,16 @@ gqa_status gqa_decode_read_flags(void *workspace, uint32_t *flags, int clear, vo
  * error codes are those of gqa_decode, except:
  *   - shapes whose gqa_decode_workspace_size exceeds GQA_NOALLOC_WORKSPACE_BYTES
  *     return GQA_ERR_WORKSPACE and enqueue nothing;
+ *   - every argument check of gqa_decode runs first: a rejected call enqueues
+ *     nothing and leaves the scratch alone;
  *   - the first call on a device looks up the scratch address on that device
  *     (make it before any stream capture on that device);
- *   - every call clears the scratch's flag word on `stream` before the
- *     kernels (cudaMemsetAsync, no allocation);
+ *   - every call clears the scratch's header and piece counts on `stream`
+ *     before the kernel (cudaMemsetAsync, no allocation): the flag word, the
+ *     dynamic-pool counters and the per-segment counts.  A call that ran into a
+ *     wait limit leaves those counters where its aborted blocks stopped; the
+ *     next call starts clean without anything to do for the caller.  The flag
+ *     word cannot be read back through this entry point;
  *   - all calls share the one array: calls that overlap on the GPU (other
  *     streams, other host threads) race and corrupt each other's results, so
  *     order them on one stream or synchronise between them.

@@ -1,12 +1,15 @@
 """Build the CUDA library ``libgqa_b300.so`` in-tree with nvcc for sm_103a.
 
-Usage: ``python -m kv_cache_decode_06_b300.build_lib [--force] [--verbose] [--trace]``.
+Usage: ``python -m kv_cache_decode_06_b300.build_lib [--force] [--verbose] [--trace] [--test-hooks]``.
 The shared library lands next to this file and is what the Python binding and
 any C caller load.  ``-Xptxas -v`` output (registers, spills, shared memory) is
 printed with ``--verbose``.  ``--trace`` builds ``libgqa_b300_trace.so`` instead:
 the same library compiled with -DGQA_TRACE, whose tensor-core decode kernel
 records a per-CTA timeline of its pipeline events (clock64 stamps) in a device
-array that ``gqa_trace_copy(dst, bytes)`` copies to the host.
+array that ``gqa_trace_copy(dst, bytes)`` copies to the host.  ``--test-hooks``
+builds ``libgqa_b300_testhooks.so``: the same library compiled with
+-DGQA_TEST_HOOKS, which also exports ``gqa_debug_withhold_copy`` (the failure-
+path test's way to make a pipeline wait run out without a fault).
 """
 from __future__ import annotations
 
@@ -24,6 +27,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libgqa_b300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 TRACE_LIB_PATH = os.path.join(HERE, "libgqa_b300_trace.so")
+TEST_HOOKS_LIB_PATH = os.path.join(HERE, "libgqa_b300_testhooks.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -51,16 +55,20 @@ def _stale(lib: str) -> bool:
     return any(os.path.getmtime(f) > t for f in deps)
 
 
-def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
-    lib = TRACE_LIB_PATH if trace else LIB_PATH
+def build(force: bool = False, verbose: bool = False, trace: bool = False, test_hooks: bool = False) -> str:
+    if trace and test_hooks:
+        raise ValueError("build either the trace or the test-hooks library, not both")
+    lib = TRACE_LIB_PATH if trace else TEST_HOOKS_LIB_PATH if test_hooks else LIB_PATH
     if not force and not _stale(lib):
         return lib
-    build_dir = BUILD_DIR + ("_trace" if trace else "")
+    build_dir = BUILD_DIR + ("_trace" if trace else "_testhooks" if test_hooks else "")
     os.makedirs(build_dir, exist_ok=True)
     objs = []
     extra = ["-Xptxas", "-v"] if verbose else []
     if trace:
         extra += ["-DGQA_TRACE"]
+    if test_hooks:
+        extra += ["-DGQA_TEST_HOOKS"]
     procs = []
     for src in sources():
         obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
@@ -88,8 +96,9 @@ def main() -> None:
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
     ap.add_argument("--trace", action="store_true")
+    ap.add_argument("--test-hooks", action="store_true")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose, trace=a.trace))
+    print(build(force=a.force, verbose=a.verbose, trace=a.trace, test_hooks=a.test_hooks))
 
 
 if __name__ == "__main__":

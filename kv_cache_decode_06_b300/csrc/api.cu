@@ -85,13 +85,22 @@ int dyn_cap_for(int B, int G, int Lmax) {
     return (int)(cap - cap % gqa::kChunk);
 }
 
-// Workspace: a 256-byte header (flag word, dynamic-pool ticket, failed-claim
-// count) and the partial slots: one per static piece (slot c + s <
-// GQA_MAX_CTAS + B*G), then one per dynamic-pool tile.
+static_assert(GQA_WORKSPACE_HEADER_BYTES == kHeaderBytes, "header size mismatch");
+
+// Bytes that must be zero before a call: the header (flag word, dynamic-pool
+// ticket, failed-claim count), the same for every shape.
+size_t zero_prefix_bytes(int B, int G) {
+    (void)B;
+    (void)G;
+    return kHeaderBytes;
+}
+
+// Workspace: the zeroed prefix, then the partial slots: one per static piece
+// (slot c + s < GQA_MAX_CTAS + B*G), then one per dynamic-pool tile.
 size_t workspace_bytes_for(int B, int H, int G, int d, int Lmax) {
     const int n = H / G;
     const size_t slots = (size_t)GQA_MAX_CTAS + (size_t)B * G + (size_t)dyn_cap_for(B, G, Lmax);
-    return kHeaderBytes + slots * (size_t)gqa::slot_floats(n, d) * sizeof(float);
+    return zero_prefix_bytes(B, G) + slots * (size_t)gqa::slot_floats(n, d) * sizeof(float);
 }
 
 gqa_status check_shape(int B, int H, int G, int d, int Lmax) {
@@ -170,8 +179,11 @@ bool make_page_map(CUtensorMap *map, const void *base, int num_pages, int G, int
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Test hook (gqa_debug_withhold_copy): applies to the next decode call only.
+#ifdef GQA_TEST_HOOKS
+// Test hook (gqa_debug_withhold_copy, test-hooks build only): applies to the
+// next decode call only.
 std::atomic<int> g_withhold_k{-1};
+#endif
 
 // Every decode variant: contiguous or paged cache, with or without the fused
 // append, a window, or all positions valid (seq_lens null).
@@ -190,7 +202,16 @@ struct DecodeRequest {
     const gqa_decode_options *opts = nullptr;
 };
 
-gqa_status decode_impl(const DecodeRequest &r) {
+// The score scale a call uses: the caller's value, or 1/sqrt(d) for
+// GQA_SCALE_DEFAULT (0), rounded once from the double-precision value.
+float resolve_scale(float scale, int d) {
+    return scale == 0.f ? (float)(1.0 / std::sqrt((double)d)) : scale;
+}
+
+// Every check that needs no device work, in the order the header documents:
+// arguments, workspace, path, device.  On GQA_OK, *path_out and *dev_out hold
+// the path the call takes and the device's facts.
+gqa_status validate(const DecodeRequest &r, int *path_out, DeviceInfo *dev_out) {
     if (!r.q || !r.k || !r.v || !r.out) return GQA_ERR_INVALID_ARG;
     const int B = r.B, H = r.H, G = r.G, d = r.d, Lmax = r.Lmax;
     gqa_status s = check_shape(B, H, G, d, Lmax);
@@ -214,9 +235,21 @@ gqa_status decode_impl(const DecodeRequest &r) {
     // the CUDA-core path reads a contiguous cache, every valid position
     if (path == GQA_PATH_SIMT && (r.block_table || r.k_new || o.window > 0)) return GQA_ERR_UNSUPPORTED;
 
-    DeviceInfo dev;
-    s = device_info(&dev);
+    s = device_info(dev_out);
     if (s != GQA_OK) return s;
+    *path_out = path;
+    return GQA_OK;
+}
+
+gqa_status decode_impl(const DecodeRequest &r) {
+    int path = 0;
+    DeviceInfo dev;
+    const gqa_status s = validate(r, &path, &dev);
+    if (s != GQA_OK) return s;
+    const int B = r.B, H = r.H, G = r.G, d = r.d, Lmax = r.Lmax;
+    const int n = H / G;
+    gqa_decode_options o{};
+    if (r.opts) o = *r.opts;
 
     const bool paired = path == GQA_PATH_TCGEN05 && gqa::tc_paired(d, Lmax, n);
     const int tile_pos = paired ? 2 * gqa::kTile : gqa::kTile;
@@ -242,7 +275,11 @@ gqa_status decode_impl(const DecodeRequest &r) {
     p.k_dst = r.k_new ? static_cast<__nv_bfloat16 *>(const_cast<void *>(r.k)) : nullptr;
     p.v_dst = r.v_new ? static_cast<__nv_bfloat16 *>(const_cast<void *>(r.v)) : nullptr;
     p.out = r.out;
+#ifdef GQA_TEST_HOOKS
     p.withhold_k = g_withhold_k.exchange(-1);
+#else
+    p.withhold_k = -1;
+#endif
     p.flags = reinterpret_cast<unsigned int *>(ws);
     p.ticket = reinterpret_cast<unsigned int *>(ws + 4);
     p.fails = reinterpret_cast<unsigned int *>(ws + 8);
@@ -250,13 +287,13 @@ gqa_status decode_impl(const DecodeRequest &r) {
     // piece ends (two GEMM parts per tile) cost more than per-SM balancing wins back.
     p.dyn_cap = (path == GQA_PATH_TCGEN05 && !paired) ? dyn_cap_for(B, G, Lmax) : 0;
     p.tile_shift = paired ? 8 : 7;
-    p.partials = reinterpret_cast<float *>(ws + kHeaderBytes);
+    p.partials = reinterpret_cast<float *>(ws + zero_prefix_bytes(B, G));
     p.B = B;
     p.H = H;
     p.G = G;
     p.n = n;
     p.Lmax = Lmax;
-    p.scale_log2 = r.scale * 1.4426950408889634f;
+    p.scale_log2 = resolve_scale(r.scale, d) * 1.4426950408889634f;
 
     CUtensorMap tk, tv;
     const bool maps_ok = r.block_table
@@ -285,10 +322,24 @@ gqa_status decode_impl(const DecodeRequest &r) {
 }  // namespace
 
 namespace gqa {
-size_t decode_workspace_zero_prefix(int B, int G) {
-    (void)B;
-    (void)G;
-    return kHeaderBytes;
+size_t decode_workspace_zero_prefix(int B, int G) { return zero_prefix_bytes(B, G); }
+
+gqa_status decode_check(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                        float *out, void *workspace, size_t workspace_bytes, int B, int H, int G, int d, int Lmax,
+                        float scale) {
+    DecodeRequest r;
+    r.q = q;
+    r.k = k_cache;
+    r.v = v_cache;
+    r.seq_lens = seq_lens;
+    r.out = out;
+    r.ws = workspace;
+    r.ws_bytes = workspace_bytes;
+    r.B = B, r.H = H, r.G = G, r.d = d, r.Lmax = Lmax;
+    r.scale = scale;
+    int path = 0;
+    DeviceInfo dev;
+    return validate(r, &path, &dev);
 }
 }  // namespace gqa
 
@@ -401,7 +452,9 @@ gqa_status gqa_decode_paged(const void *q, void *k_pages, void *v_pages, const i
     return decode_impl(r);
 }
 
+#ifdef GQA_TEST_HOOKS
 void gqa_debug_withhold_copy(int tile) { g_withhold_k.store(tile < 0 ? -1 : tile); }
+#endif
 
 gqa_status gqa_decode_read_flags(void *workspace, uint32_t *flags, int clear, void *stream) {
     if (!workspace || !flags || !aligned(workspace, 256)) return GQA_ERR_INVALID_ARG;

@@ -14,7 +14,10 @@
 // Launched right after the decode kernel with programmatic stream
 // serialisation: its CTAs build the tile prefix and the work split (from
 // seq_lens, which the decode kernel does not write) while the decode grid
-// drains, then wait for it to complete.  The CTAs take (segment, 256-float4
+// drains, then wait for it to complete.  Their shared memory is sized to the
+// batch (the prefix of B sequences), so that a split-combine block fits on an
+// SM beside a decode block: beside the decode kernel it serves, and beside the
+// next decode kernel, which it lets start its on-chip set-up at once.  The CTAs take (segment, 256-float4
 // part of its n x D outputs) work items in a grid-stride loop, so large head
 // groups spread over several CTAs; a segment whose single piece covered it whole
 // was written by the decode kernel, the others are merged here from the slots
@@ -33,10 +36,16 @@ namespace {
 constexpr int kCombThreads = 256;
 constexpr int kBatch = 8;   // pieces per round trip
 
+// Dynamic shared memory: prefix[B + 1], scratch[33].
+__host__ __device__ constexpr size_t combine_smem_bytes(int B) { return (size_t)(B + 1 + 33) * sizeof(int); }
+
 template <int D>
 __global__ void __launch_bounds__(kCombThreads) gqa_split_combine_kernel(const DecodeParams p, int grid_main) {
-    __shared__ int prefix[kMaxBatch + 1];
-    __shared__ int scratch[33];
+    extern __shared__ int cmb_smem[];
+    int *prefix = cmb_smem, *scratch = cmb_smem + p.B + 1;
+    // The next grid on the stream (normally the next decode step) may start its
+    // on-chip set-up as SMs have room; it touches memory only once this one is done.
+    griddep_launch_dependents();
     build_prefix(p, p.tile_shift, prefix, scratch, nullptr);   // ends with __syncthreads
     const int G = p.G, n = p.n;
     const WorkSplit split = make_split((long long)G * prefix[p.B], grid_main,
@@ -110,8 +119,9 @@ cudaError_t launch_split_combine(const DecodeParams &p, int D, int grid_main, cu
     const int nd4 = p.n * D / 4;
     const long long work = (long long)p.B * p.G * ((nd4 + kCombThreads - 1) / kCombThreads);
     const int grid = work < 4 * kMaxCtas ? (int)work : 4 * kMaxCtas;
-    if (D == 128) return launch_pdl(gqa_split_combine_kernel<128>, grid, kCombThreads, 0, stream, p, grid_main);
-    return launch_pdl(gqa_split_combine_kernel<64>, grid, kCombThreads, 0, stream, p, grid_main);
+    const size_t smem = combine_smem_bytes(p.B);
+    if (D == 128) return launch_pdl(gqa_split_combine_kernel<128>, grid, kCombThreads, smem, stream, p, grid_main);
+    return launch_pdl(gqa_split_combine_kernel<64>, grid, kCombThreads, smem, stream, p, grid_main);
 }
 
 }  // namespace gqa

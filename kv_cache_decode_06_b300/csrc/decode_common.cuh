@@ -64,7 +64,7 @@ struct DecodeParams {
     // the contiguous cache or the page pool)
     const __nv_bfloat16 *k_new, *v_new;
     __nv_bfloat16 *k_dst, *v_dst;
-    int withhold_k;           // test hook: CTA 0 skips its K copy number withhold_k (-1: none)
+    int withhold_k;           // test-hooks build only: CTA 0 skips its K copy number withhold_k (-1: none)
     float *out;               // [B, H, D]
     unsigned int *flags;      // workspace flag word
     unsigned int *ticket;     // dynamic-pool claims (zero between calls)
@@ -226,6 +226,46 @@ __device__ inline void build_prefix(const DecodeParams &p, int shift, int *prefi
     if (tid == 0) prefix[B] = total;
     if (bad && flags && blockIdx.x == 0) atomicOr(flags, 0x1u /* GQA_FLAG_SEQ_LEN_CLAMPED */);
     __syncthreads();
+}
+
+// Warp-wide version of build_prefix for the calling warp alone (no block
+// barrier): lane l takes sequences [l*per, (l+1)*per).  *last_long receives the
+// last sequence whose segments are too long for the dynamic pool (-1 if none).
+// Ends with __syncwarp().
+__device__ inline void build_prefix_warp(const DecodeParams &p, int shift, int *prefix, int *last_long,
+                                         unsigned int *flags) {
+    const int lane = threadIdx.x & 31, B = p.B;
+    const int per = (B + 31) >> 5;
+    const int b0 = min(B, lane * per), b1 = min(B, b0 + per);
+    int local = 0, ll = -1;
+    bool bad = false;
+    for (int b = b0; b < b1; ++b) {
+        int T = p.Lmax;
+        if (p.seq_lens) {
+            const int sv = __ldg(p.seq_lens + b);
+            bad |= (sv < 0 || sv > p.Lmax);
+            T = clamp_seq(sv, p.Lmax);
+        }
+        const int tb = segment_tiles(p, T, shift);
+        prefix[b] = local;   // exclusive within this lane; offset below
+        local += tb;
+        if (tb > kPoolSegChunks * kChunk) ll = b;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int before = incl - local;
+    for (int b = b0; b < b1; ++b) prefix[b] += before;
+    if (lane == 31) prefix[B] = incl;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ll = max(ll, __shfl_xor_sync(0xffffffffu, ll, o));
+    if (lane == 0) *last_long = ll;
+    if (__any_sync(0xffffffffu, bad) && flags && blockIdx.x == 0 && lane == 0)
+        atomicOr(flags, 0x1u /* GQA_FLAG_SEQ_LEN_CLAMPED */);
+    __syncwarp();
 }
 
 // Segments with no valid position get out = 0 (the empty sum).  CTA c takes

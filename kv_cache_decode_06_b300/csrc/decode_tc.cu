@@ -168,7 +168,7 @@ struct TcCfg {
     static constexpr int kMF = 3 * NH;                           // [3][NH] running max after tile i
     static constexpr int kAF = 4 * NH;                           // [4][NH] rescale factor of tile i
     static constexpr int kSmallBytes = 4 * (kRedF + kLredF + kMF + kAF) + 33 * 4 + (kMaxBatch + 1) * 4 + kRing * 16;
-    static constexpr int bar_bytes(int SK, int SV, int QB) { return (2 * SK + 2 * SV + 2 * QB + 14 + 2 + 2 * kRing) * 8 + 16; }
+    static constexpr int bar_bytes(int SK, int SV, int QB) { return (2 * SK + 2 * SV + 2 * QB + 14 + 2 + 2 * kRing + 1) * 8 + 16; }
     static constexpr int fixed_bytes(int QB) {
         return QB * kQBytes + 2 * kPBufBytes + kSmallBytes + bar_bytes(8, 8, QB) + kIdBytes + kIdBars * 8 +
                1024 /* alignment slack */;
@@ -199,7 +199,7 @@ struct TcCfg {
     // value GEMM three tiles back before reusing one), else two
     static constexpr int layout_bytes(int pbuf) {
         return (kSK + kSV) * kSlotCost + kQBuf * kQBytes + pbuf * kPBufBytes + kSmallBytes + 8 +
-               (2 * kSK + 2 * kSV + 2 * kQBuf + 12 + pbuf + 2 + 2 * kRing + kIdBars) * 8 + 16 + 1024 + kIdBytes;
+               (2 * kSK + 2 * kSV + 2 * kQBuf + 12 + pbuf + 2 + 2 * kRing + kIdBars + 1) * 8 + 16 + 1024 + kIdBytes;
     }
     static constexpr int kPBuf = layout_bytes(3) <= kSmemLimit ? 3 : 2;
     // layout (offsets from the 1024-aligned base)
@@ -219,8 +219,9 @@ struct TcCfg {
     static constexpr int kOffIds = kOffPatch + (kSK + kSV) * kStageInfo;     // int [kIdRing][kIdStride]
     static constexpr int kOffBar = kOffIds + kIdBytes;
     // barriers: kfull[SK] kempty[SK] vfull[SV] vempty[SV] qfull[QB] qempty[QB] sfull[2] sfree[2]
-    //           pfull[PB] ofull[3] ofree[3] red[2] grp done
-    static constexpr int kNumBars = 2 * kSK + 2 * kSV + 2 * kQBuf + 12 + kPBuf + 2 + 2 * kRing + kIdBars;
+    //           pfull[PB] ofull[3] ofree[3] red[2] grp done rfull[kRing] rempty[kRing]
+    //           (paged) idfull[kIdRing] idempty[kIdRing]; pre
+    static constexpr int kNumBars = 2 * kSK + 2 * kSV + 2 * kQBuf + 12 + kPBuf + 2 + 2 * kRing + kIdBars + 1;
     static constexpr int kOffFlags = kOffBar + kNumBars * 8;     // abort, tmem base
     static constexpr int kSmemBytes = kOffFlags + 16 + 1024;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory layout too large");
@@ -550,7 +551,8 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
     uint64_t *redbar = ofree + 3, *grp = redbar + 2, *done = grp + 1, *rfull = done + 1, *rempty = rfull + kRing;
     RangeEntry *ring = reinterpret_cast<RangeEntry *>(smem + C::kOffRing);
     int *ids_ring = reinterpret_cast<int *>(smem + C::kOffIds);
-    uint64_t *idfull = rempty + kRing, *idempty = idfull + C::kIdRing;   // variant instances only
+    uint64_t *idfull = rempty + kRing, *idempty = idfull + C::kIdRing;   // paged instances only
+    uint64_t *prebar = rempty + kRing + C::kIdBars;
     uint8_t *kstage = smem + C::kOffStage, *vstage = kstage + SK * C::kRowBytes;
     PatchInfo *kinfo = reinterpret_cast<PatchInfo *>(smem + C::kOffPatch), *vinfo = kinfo + SK;
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + C::kOffFlags);
@@ -594,6 +596,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
             mbar_init(&rempty[s], 2 + 128 + (kPaged ? 1 : 0));
         }
         mbar_init(done, 2);   // one commit from each MMA issuer
+        mbar_init(prebar, 32);   // the producer warp, once the tile prefix is in shared memory
         if constexpr (kPaged) {
             for (int s = 0; s < C::kIdRing; ++s) {
                 mbar_init(&idfull[s], 32);    // every lane of the page-id warp
@@ -612,14 +615,24 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
         tmem_alloc(s_tmem, C::kTmemCols);
         tmem_relinquish();
     }
+    __syncthreads();   // barriers initialised, TMEM allocated
+    tc_fence_after_sync();
+    const uint32_t tmem = *s_tmem;
+    // The next grid on the stream (the split-combine) may start as SMs have room.
+    griddep_launch_dependents();
     // Everything above is on-chip; inputs and outputs are touched only once the
     // grids this one depends on have completed.
     griddep_wait();
     if (tid == 64) GQA_TRACE_AT(kTrDepDone, clock64());
-    griddep_launch_dependents();
-    build_prefix(p, C::kTileShift, prefix, scratch, p.flags);   // ends with __syncthreads
-    tc_fence_after_sync();
-    const uint32_t tmem = *s_tmem;
+    // The producer warp builds the tile prefix alone and goes straight on to its
+    // first copies; the other roles wait for it on an mbarrier.
+    bool pre_ok = true;
+    if (warp == 0) {
+        build_prefix_warp(p, C::kTileShift, prefix, scratch + 32, p.flags);
+        mbar_arrive(prebar);
+    } else {
+        pre_ok = mbar_wait(prebar, 0, ab);   // false only if the CTA aborts: its roles then do nothing
+    }
     if (tid == 64) GQA_TRACE_AT(kTrSetup, clock64());
 
     const int G = p.G, n = p.n;
@@ -627,7 +640,9 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                                         p.dyn_cap);
     int kissued = 0, vissued = 0, qissued = 0;
 
-    if (warp == 0) {
+    if (!pre_ok) {
+        // the producer warp never published the tile prefix: nothing to do
+    } else if (warp == 0) {
         // ================================================================ producer
         // Hands every work range to the other roles through the ring: the static
         // range first, then one claimed chunk at a time, then an end marker.
@@ -716,10 +731,13 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         }
                         uint8_t *kdst = smem + C::kOffK + st * C::kTileBytes;
                         if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i, clock64());
+#ifdef GQA_TEST_HOOKS
                         if (i == p.withhold_k && blockIdx.x == 0) {
                             // test hook: this copy is never made, so the score GEMM's bounded
                             // wait for it runs out and the CTA takes its abort path
-                        } else if constexpr (kExt) {
+                        } else
+#endif
+                        if constexpr (kExt) {
                             const int *ids = kPaged ? ids_ring + (i % C::kIdRing) * C::kIdStride : nullptr;
                             const int T = kPaged ? ids[C::kIdMax] : k_lens.get(p, kc.b);
                             produce_variant_tile<C>(p, &tm_k, kdst, &kfull[st], kc, T, pol_kv, p.k_new,

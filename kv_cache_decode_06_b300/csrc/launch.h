@@ -7,6 +7,7 @@
 #include <utility>
 
 #include "decode_common.cuh"
+#include "gqa.h"
 
 namespace gqa {
 
@@ -42,8 +43,16 @@ cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const
                              const DecodeParams &p, int D, bool paired, int ctas, cudaStream_t stream);
 
 // Leading bytes of a decode workspace that must be zero before its first call:
-// the flag word.
+// GQA_WORKSPACE_HEADER_BYTES (flag word, dynamic-pool ticket, failed-claim
+// count), the same for every shape.
 size_t decode_workspace_zero_prefix(int B, int G);
+
+// Every host-side check gqa_decode makes (arguments, workspace, path, device),
+// without enqueueing anything: the status gqa_decode would return before its
+// first launch.
+gqa_status decode_check(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
+                        float *out, void *workspace, size_t workspace_bytes, int B, int H, int G, int d, int Lmax,
+                        float scale);
 
 // The split-combine kernel (combine.cu), launched after a decode kernel of
 // grid_main CTAs.

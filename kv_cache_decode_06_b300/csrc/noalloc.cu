@@ -1,8 +1,8 @@
 // gqa_decode_noalloc: the decode step for callers that cannot allocate device
 // memory.
 //
-// gqa_decode needs a caller-provided workspace (split-combine partials, arrival
-// counters, a flag word).  Some callers have no way to provide one: a plugin
+// gqa_decode needs a caller-provided workspace (split-combine partials, the
+// dynamic work pool's counters, a flag word).  Some callers have no way to provide one: a plugin
 // that only receives the tensors it works on from a host framework that owns
 // all device memory, a runtime that reserves its memory once at start-up and
 // forbids allocation afterwards, or a latency-critical loop that cannot afford
@@ -13,8 +13,10 @@
 // library holds GQA_NOALLOC_WORKSPACE_BYTES of it until the process exits.  In
 // host code its name is only a host-side stand-in, so the device address is
 // looked up with cudaGetSymbolAddress, once per device, with that device
-// current, and passed to the kernel like any workspace.  Nothing here calls
-// cudaMalloc, cudaFree or an allocating library routine.
+// current, and passed to the kernel like any workspace.  The address is kept
+// for the life of the process: after a cudaDeviceReset it would be stale, so
+// the library must not be used across one.  Nothing here calls cudaMalloc,
+// cudaFree or an allocating library routine.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -67,9 +69,19 @@ extern "C" gqa_status gqa_decode_noalloc(const void *q, const void *k_cache, con
     void *ws = nullptr;
     const gqa_status a = scratch_address(&ws);
     if (a != GQA_OK) return a;
-    // Clear the flag word every time (on the caller's stream): the scratch is
-    // shared by every call, and a flag left by an earlier call would otherwise
-    // stay set.  Nothing else in the workspace needs resetting.
+    // Every host-side check of gqa_decode (pointer alignment, scale, path and
+    // head limits, device) runs before anything is enqueued: a rejected call
+    // leaves the stream, and the scratch that a call on another stream may be
+    // using, untouched.
+    const gqa_status c = gqa::decode_check(q, k_cache, v_cache, seq_lens, out, ws, kScratchBytes, B, H, G, d, Lmax,
+                                           scale);
+    if (c != GQA_OK) return c;
+    // Clear the scratch's whole header every time, on the caller's stream: the
+    // flag word, so that a flag left by an earlier call does not stay set, and
+    // the dynamic-pool ticket and failed-claim count.  A call that ran into a
+    // wait limit (GQA_FLAG_WAIT_TIMEOUT) leaves those two counters wherever its
+    // aborted thread blocks stopped, and clearing them here is what lets the next
+    // call run exactly without any reset by the caller.
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, gqa::decode_workspace_zero_prefix(B, G), st) != cudaSuccess) {
         cudaGetLastError();

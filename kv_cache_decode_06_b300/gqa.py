@@ -8,8 +8,8 @@ first call raises: there is no CPU fallback.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
-import math
 import os
 import threading
 from typing import Optional
@@ -18,6 +18,7 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgqa_b300.so")
+TEST_HOOKS_LIB_PATH = os.path.join(_HERE, "libgqa_b300_testhooks.so")
 
 GQA_OK = 0
 STATUS_NAMES = {0: "GQA_OK", 1: "GQA_ERR_INVALID_ARG", 2: "GQA_ERR_UNSUPPORTED", 3: "GQA_ERR_WORKSPACE",
@@ -26,11 +27,15 @@ PATH_AUTO, PATH_SIMT, PATH_TCGEN05 = 0, 1, 2
 FLAG_SEQ_LEN_CLAMPED = 0x1
 FLAG_WAIT_TIMEOUT = 0x2
 FLAG_BAD_PAGE = 0x4
+SCALE_DEFAULT = 0.0   # GQA_SCALE_DEFAULT: the library then uses the pages' scale for head dim d
+WORKSPACE_HEADER_BYTES = 256   # GQA_WORKSPACE_HEADER_BYTES: zero them again after a timed-out call
 
-# Every symbol include/gqa.h declares.
+# Every symbol include/gqa.h declares for the product library.
 EXPORTS = ("gqa_status_string", "gqa_abi_version", "gqa_decode_workspace_size", "gqa_decode", "gqa_decode_ex",
            "gqa_decode_select_path", "gqa_decode_read_flags", "gqa_meanpool_kv", "gqa_meanpool_kv_strided",
-           "gqa_decode_noalloc", "gqa_decode_append", "gqa_decode_paged", "gqa_debug_withhold_copy")
+           "gqa_decode_noalloc", "gqa_decode_append", "gqa_decode_paged")
+# Declared in include/gqa.h under GQA_TEST_HOOKS: exported by the test-hooks build only.
+TEST_HOOK_EXPORTS = ("gqa_debug_withhold_copy",)
 NOALLOC_WORKSPACE_BYTES = 8 << 20
 
 _lock = threading.Lock()
@@ -76,8 +81,9 @@ def load(path: Optional[str] = None):
         lib.gqa_decode_paged.restype = I
         lib.gqa_decode_paged.argtypes = [V, V, V, V, V, V, V, V, V, Z, I, I, I, I, I, I, I, F, V,
                                          ctypes.POINTER(DecodeOptions)]
-        lib.gqa_debug_withhold_copy.restype = None
-        lib.gqa_debug_withhold_copy.argtypes = [I]
+        if hasattr(lib, "gqa_debug_withhold_copy"):   # test-hooks build only
+            lib.gqa_debug_withhold_copy.restype = None
+            lib.gqa_debug_withhold_copy.argtypes = [I]
         lib.gqa_decode_select_path.restype = I
         lib.gqa_decode_select_path.argtypes = [I, I, I, I, I]
         lib.gqa_decode_read_flags.restype = I
@@ -91,6 +97,29 @@ def load(path: Optional[str] = None):
         if path is None:
             _lib = lib
     return lib
+
+
+def load_test_hooks():
+    """Load the test-hooks build (``build_lib --test-hooks``), which also exports
+    gqa_debug_withhold_copy.  It is a separate shared object with its own device
+    code; the product library is not affected."""
+    if not os.path.exists(TEST_HOOKS_LIB_PATH):
+        raise RuntimeError(f"{TEST_HOOKS_LIB_PATH} is missing: build it with "
+                           "`python -m kv_cache_decode_06_b300.build_lib --test-hooks`")
+    return load(TEST_HOOKS_LIB_PATH)
+
+
+@contextlib.contextmanager
+def using_library(lib):
+    """Route this module's calls through ``lib`` (a handle from :func:`load`) inside the block."""
+    global _lib
+    with _lock:
+        saved, _lib = _lib, lib
+    try:
+        yield lib
+    finally:
+        with _lock:
+            _lib = saved
 
 
 def _check(status: int, what: str) -> None:
@@ -151,7 +180,7 @@ def _prepare(q, seq_lens, out, workspace, scale, G, Lmax):
         workspace = alloc_workspace(B, H, G, d, Lmax, dev)
     _require(workspace, "workspace", torch.uint8, dev)
     if scale is None:
-        scale = 1.0 / math.sqrt(d)
+        scale = SCALE_DEFAULT
     return out, workspace, float(scale)
 
 
@@ -165,7 +194,8 @@ def decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_le
     to the last ``window`` valid positions only.  Enqueued on ``stream`` (default:
     the current stream); returns ``out``.  ``workspace`` must come from
     :func:`alloc_workspace` (zero-filled) and may be reused by later calls of any
-    shape that fits it.
+    shape that fits it.  ``scale=None`` passes GQA_SCALE_DEFAULT: the library
+    uses the reciprocal square root of the head dim.
     """
     dev = q.device
     B, H, d = q.shape
@@ -262,7 +292,7 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
     if seq_lens is not None:
         _require(seq_lens, "seq_lens", torch.int32, dev)
     if scale is None:
-        scale = 1.0 / math.sqrt(d)
+        scale = SCALE_DEFAULT
     _check(load().gqa_decode_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), _ptr_or_null(seq_lens),
                                      out.data_ptr(), B, H, G, d, Lmax, float(scale),
                                      _stream_handle(stream, dev)),
@@ -271,8 +301,12 @@ def decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
 
 
 def debug_withhold_copy(tile: int) -> None:
-    """Test hook: the next decode call's block 0 skips its K copy number ``tile`` (see gqa.h)."""
-    load().gqa_debug_withhold_copy(int(tile))
+    """Test hook (test-hooks build only, see :func:`load_test_hooks`): the next decode call's
+    block 0 skips its K copy number ``tile`` (see gqa.h)."""
+    lib = load()
+    if not hasattr(lib, "gqa_debug_withhold_copy"):
+        raise RuntimeError("gqa_debug_withhold_copy is exported by the test-hooks build only")
+    lib.gqa_debug_withhold_copy(int(tile))
 
 
 def read_flags(workspace: torch.Tensor, clear: bool = False, stream: Optional[torch.cuda.Stream] = None) -> int:

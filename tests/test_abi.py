@@ -16,19 +16,40 @@ HEADER = os.path.join(ROOT, "include", "gqa.h")
 FAKE = 0x10000
 
 
-def declared_functions():
+def declared_functions(test_hooks=False):
+    """Functions the header declares; with test_hooks, those under GQA_TEST_HOOKS instead."""
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    hooks = "".join(re.findall(r"#ifdef GQA_TEST_HOOKS(.*?)#endif", src, flags=re.S))
+    if test_hooks:
+        src = hooks
+    else:
+        src = re.sub(r"#ifdef GQA_TEST_HOOKS.*?#endif", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(gqa_[a-z_0-9]+)\s*\(", src)))
 
 
 def test_header_declarations_match_binding():
     assert declared_functions() == sorted(gqa.EXPORTS)
+    assert declared_functions(test_hooks=True) == sorted(gqa.TEST_HOOK_EXPORTS)
 
 
 def test_library_exports_every_declared_symbol(gqa_lib):
     for name in declared_functions():
         assert hasattr(gqa_lib, name), name
+
+
+def test_product_library_has_no_test_hook(gqa_lib):
+    """The failure-path hook lives in the test-hooks build only."""
+    for name in gqa.TEST_HOOK_EXPORTS:
+        assert not hasattr(gqa_lib, name), name
+
+
+def test_test_hooks_library_exports_the_hook():
+    from kv_cache_decode_06_b300 import build_lib
+    build_lib.build(test_hooks=True)
+    lib = gqa.load_test_hooks()
+    for name in declared_functions() + declared_functions(test_hooks=True):
+        assert hasattr(lib, name), name
 
 
 def test_library_does_not_link_the_oracle(gqa_lib):
@@ -101,6 +122,23 @@ def test_decode_rejects_bad_shapes_and_values(gqa_lib):
     assert _decode(gqa_lib, shape=(1, 8, 2, 64, 0)) == 1            # Lmax = 0
     assert _decode(gqa_lib, scale=float("nan")) == 1
     assert _decode(gqa_lib, scale=float("inf")) == 1
+
+
+def test_decode_accepts_the_default_scale_sentinel(gqa_lib):
+    """GQA_SCALE_DEFAULT (0) is a valid scale: the call gets past every argument check
+    (here, without a GPU, to the device check) instead of being rejected."""
+    m = re.search(r"#define GQA_SCALE_DEFAULT (\S+)f", open(HEADER).read())
+    assert float(m.group(1)) == gqa.SCALE_DEFAULT == 0.0
+    expect = 5 if not os.path.exists("/dev/nvidia0") else 0
+    if expect == 5:
+        assert _decode(gqa_lib, scale=gqa.SCALE_DEFAULT) == 5
+        assert _decode(gqa_lib, scale=-0.5) == 5     # any finite value is used as given
+
+
+def test_binding_computes_no_scale():
+    """The binding only marshals: the default scale is resolved in the library."""
+    src = open(os.path.join(ROOT, "kv_cache_decode_06_b300", "gqa.py")).read()
+    assert "sqrt" not in src
 
 
 def test_decode_rejects_misaligned_pointers(gqa_lib):

@@ -108,6 +108,30 @@ def test_split_invariance(path):
     assert spread <= 1e-5
 
 
+@pytest.mark.parametrize("shape", [
+    (2, 64, 1, 64, 1030, [1030, 600]),        # 64 heads per group at d = 64: heads on M
+    (3, 32, 4, 64, 1030, [1030, 515, 77]),    # d = 64, even Lmax: paired layout
+    (4, 64, 8, 128, 2000, [2000, 1, 999, 1500]),
+    (3, 128, 2, 128, 700, [700, 129, 640]),   # 64 heads at d = 128: chunked softmax
+], ids=lambda s: "B{}H{}G{}d{}L{}".format(*s[:5]))
+def test_split_invariance_layouts(shape):
+    """Every layout (heads on M, paired d = 64, d = 128, chunked softmax), from a few CTAs
+    to one tile per CTA, gives the oracle's answer, call after call on one workspace, and
+    leaves the workspace's counters at zero."""
+    B, H, G, d, L, seq = shape
+    cfg = DecodeConfig("splitl", 59, B=B, H=H, G=G, d=d, Lmax=L)
+    inp = make_decode_inputs(cfg, seq_lens=seq)
+    ref = oracle_out(inp)
+    ws = gqa.alloc_workspace(B, H, G, d, L)
+    for ctas in (2, 5, 13, 64, 300, 1024):
+        for rep in range(2):
+            got = run(inp, path=gqa.PATH_TCGEN05, num_ctas=ctas, ws=ws)
+            check_close(got, ref, what=f"{shape} ctas={ctas} rep={rep}")
+    assert gqa.read_flags(ws) == 0
+    hdr = ws[:gqa.WORKSPACE_HEADER_BYTES].cpu()
+    assert int(hdr[4:].count_nonzero()) == 0, "counters left non-zero"
+
+
 @pytest.mark.parametrize("d", [128, 64])
 def test_dynamic_pool_with_empty_and_short_sequences(d):
     """Small grids (>= 64 tiles per CTA) put a quarter of the tiles in the claimed pool:
@@ -140,9 +164,25 @@ def test_repeated_calls_reuse_workspace():
     assert gqa.read_flags(ws) == 0
 
 
+def test_default_scale_sentinel_matches_explicit_scale():
+    """scale = GQA_SCALE_DEFAULT (0) makes the library use 1/sqrt(d): bit-identical to passing
+    the fp32 value of 1/sqrt(d) itself, for both head dims."""
+    for d in (64, 128):
+        cfg = DecodeConfig("scale", 58, B=2, H=8, G=2, d=d, Lmax=300)
+        inp = make_decode_inputs(cfg, seq_lens=[300, 77])
+        q, k, v, sl = to_device(inp)
+        a = gqa.decode(q, k, v, sl, scale=float(np.float32(1.0 / np.sqrt(d)))).clone()
+        b = gqa.decode(q, k, v, sl, scale=gqa.SCALE_DEFAULT).clone()
+        c = gqa.decode(q, k, v, sl).clone()   # the binding passes the sentinel
+        torch.cuda.synchronize()
+        assert torch.equal(a, b) and torch.equal(a, c), d
+        check_close(a.cpu().numpy(), oracle_out(inp), what=f"default scale d={d}")
+
+
 def test_back_to_back_calls_on_other_shapes_and_streams():
-    """Decode + split-combine pairs launched back to back (programmatic serialisation) never
-    read each other's partials: alternating shapes on one workspace and one stream stay exact."""
+    """Decode + split-combine pairs launched back to back (programmatic serialisation, each
+    kernel starting beside the previous one) never read each other's partials: alternating
+    shapes on one workspace and one stream stay exact."""
     cfgs = [DecodeConfig("bb1", 55, B=3, H=16, G=4, d=128, Lmax=2048),
             DecodeConfig("bb2", 56, B=5, H=8, G=2, d=128, Lmax=700)]
     inps = [make_decode_inputs(c) for c in cfgs]
@@ -299,23 +339,26 @@ def test_long_ragged_workload():
 
 
 def test_wait_timeout_sets_flag_and_context_survives():
-    """Failure detection without a fault: a K copy that is never made (test hook) leaves a barrier that
-    nothing completes; block 0's bounded wait runs out after about a second, the call sets
-    GQA_FLAG_WAIT_TIMEOUT and returns, and after the workspace header is zeroed the next call is exact."""
+    """Failure detection without a fault: a K copy that is never made (test-hooks build) leaves a
+    barrier that nothing completes; block 0's bounded wait runs out after about a second, the call
+    sets GQA_FLAG_WAIT_TIMEOUT and returns, and after the workspace is zeroed the next call is exact."""
     import time
+    from kv_cache_decode_06_b300 import build_lib
+    build_lib.build(test_hooks=True)
     cfg = CONFIGS["mistral7b"].with_(B=4)
     inp = make_decode_inputs(cfg)
     q, k, v, sl = to_device(inp)
-    ws = gqa.alloc_workspace(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax)
-    gqa.debug_withhold_copy(1)
-    t0 = time.time()
-    gqa.decode(q, k, v, sl, workspace=ws, scale=float(inp.scale), path=gqa.PATH_TCGEN05)
-    torch.cuda.synchronize()
-    elapsed = time.time() - t0
-    assert gqa.read_flags(ws) & gqa.FLAG_WAIT_TIMEOUT
-    assert 0.5 < elapsed < 30.0, elapsed
-    ws[:256].zero_()
-    got = gqa.decode(q, k, v, sl, workspace=ws, scale=float(inp.scale))
-    torch.cuda.synchronize()
-    check_close(got.cpu().numpy(), oracle_out(inp), what="after a timed-out call")
-    assert gqa.read_flags(ws) == 0
+    with gqa.using_library(gqa.load_test_hooks()):
+        ws = gqa.alloc_workspace(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax)
+        gqa.debug_withhold_copy(1)
+        t0 = time.time()
+        gqa.decode(q, k, v, sl, workspace=ws, scale=float(inp.scale), path=gqa.PATH_TCGEN05)
+        torch.cuda.synchronize()
+        elapsed = time.time() - t0
+        assert gqa.read_flags(ws) & gqa.FLAG_WAIT_TIMEOUT
+        assert 0.5 < elapsed < 30.0, elapsed
+        ws.zero_()
+        got = gqa.decode(q, k, v, sl, workspace=ws, scale=float(inp.scale))
+        torch.cuda.synchronize()
+        check_close(got.cpu().numpy(), oracle_out(inp), what="after a timed-out call")
+        assert gqa.read_flags(ws) == 0
