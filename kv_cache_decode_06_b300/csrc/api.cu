@@ -121,13 +121,16 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // Lmax read as zero.  Paired (d = 64, Lmax even): viewed as [B*G][Lmax/2][128],
 // rows of two consecutive positions, so a box of 128 rows and 64 columns holds
 // the even (column 0) or the odd (column 64) positions of 256.
-bool make_cache_map(CUtensorMap *map, const void *base, int B, int G, int d, int Lmax, bool paired) {
+// box_rows: 128 (a whole tile), or 64, 32, 16 for the tail maps (the last tile
+// of a segment, loaded only as far as its attended rows reach).
+bool make_cache_map(CUtensorMap *map, const void *base, int B, int G, int d, int Lmax, bool paired,
+                    int box_rows = gqa::kTile) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const int cols = paired ? 2 * d : d, rows = paired ? Lmax / 2 : Lmax;
     const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)B * G};
     const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)Lmax * d * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)gqa::kBoxCols, (cuuint32_t)gqa::kTile, 1};
+    const cuuint32_t box[3] = {(cuuint32_t)gqa::kBoxCols, (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -310,7 +313,14 @@ gqa_status decode_impl(const DecodeRequest &r) {
         const int rows = gqa::tc_rows_for(n);
         CUtensorMap tq;
         if (!make_q_map(&tq, r.q, B, H, d, rows)) return GQA_ERR_LAUNCH;
-        e = gqa::launch_decode_tc(tk, tv, tq, p, d, paired, (int)ctas, st);
+        gqa::TailMaps tails;
+        std::memset(&tails, 0, sizeof tails);
+        const bool plain = !r.block_table && !r.k_new && o.window == 0;   // the instances that trim last tiles
+        for (int t = 0; plain && t < 3; ++t)
+            if (!make_cache_map(&tails.k[t], r.k, B, G, d, Lmax, paired, 64 >> t) ||
+                !make_cache_map(&tails.v[t], r.v, B, G, d, Lmax, paired, 64 >> t))
+                return GQA_ERR_LAUNCH;
+        e = gqa::launch_decode_tc(tk, tv, tq, tails, p, d, paired, (int)ctas, st);
     }
     if (e == cudaErrorNotSupported) return GQA_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return GQA_ERR_LAUNCH;

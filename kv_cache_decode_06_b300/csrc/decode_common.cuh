@@ -232,8 +232,9 @@ __device__ inline void build_prefix(const DecodeParams &p, int shift, int *prefi
 // barrier): lane l takes sequences [l*per, (l+1)*per).  *last_long receives the
 // last sequence whose segments are too long for the dynamic pool (-1 if none).
 // Ends with __syncwarp().
+// tlen (nullable): receives T_b, the clamped sequence lengths.
 __device__ inline void build_prefix_warp(const DecodeParams &p, int shift, int *prefix, int *last_long,
-                                         unsigned int *flags) {
+                                         unsigned int *flags, int *tlen) {
     const int lane = threadIdx.x & 31, B = p.B;
     const int per = (B + 31) >> 5;
     const int b0 = min(B, lane * per), b1 = min(B, b0 + per);
@@ -247,6 +248,7 @@ __device__ inline void build_prefix_warp(const DecodeParams &p, int shift, int *
             T = clamp_seq(sv, p.Lmax);
         }
         const int tb = segment_tiles(p, T, shift);
+        if (tlen) tlen[b] = T;
         prefix[b] = local;   // exclusive within this lane; offset below
         local += tb;
         if (tb > kPoolSegChunks * kChunk) ll = b;
@@ -266,6 +268,12 @@ __device__ inline void build_prefix_warp(const DecodeParams &p, int shift, int *
     if (__any_sync(0xffffffffu, bad) && flags && blockIdx.x == 0 && lane == 0)
         atomicOr(flags, 0x1u /* GQA_FLAG_SEQ_LEN_CLAMPED */);
     __syncwarp();
+}
+
+// Where a CTA keeps T_b beside the tile prefix: the prefix array's unused tail,
+// when the batch leaves room for it (null otherwise).
+__device__ __forceinline__ int *seq_len_array(int *prefix, int B) {
+    return 2 * B + 1 <= kMaxBatch + 1 ? prefix + B + 1 : nullptr;
 }
 
 // Segments with no valid position get out = 0 (the empty sum).  CTA c takes

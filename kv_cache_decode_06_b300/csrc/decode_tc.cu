@@ -451,8 +451,8 @@ __device__ __noinline__ void produce_tile(const DecodeParams &p, const CUtensorM
 }
 
 // Producer, plain instances: contiguous cache, every valid position: tile j of
-// segment b*G + g is tensor-map rows j*128 .. (no sequence length needed).
-// (j0: the segment's first tile, nonzero only with a window)
+// segment b*G + g is tensor-map rows j*128 .. (j0: the segment's first tile,
+// nonzero only with a window).
 template <class C>
 __device__ __forceinline__ void produce_plain_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst,
                                                    uint64_t *bar, const Cursor &c, uint64_t pol, int j0 = 0) {
@@ -460,6 +460,40 @@ __device__ __forceinline__ void produce_plain_tile(const DecodeParams &p, const 
 #pragma unroll
     for (int cb = 0; cb < C::kColBoxes; ++cb)
         tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, (j0 + c.j) * kTile, c.b * p.G + c.g, bar, pol);
+}
+
+// The last tile of a segment, `rows` tensor-map rows of it (a multiple of 16 below
+// 128): boxes of 64, 32 and 16 rows from the tail maps, each at its place in the
+// slot (multiples of 16 rows keep the 128-byte swizzle pattern of a whole tile).
+// The slot's rows past `rows` keep older data; the softmax masks those positions
+// of K and clears those rows of V, as for any position past the sequence.
+template <class C>
+__device__ __noinline__ void produce_tail_tile(const DecodeParams &p, const CUtensorMap *tails, uint8_t *dst,
+                                               uint64_t *bar, const Cursor &c, uint64_t pol, int rows) {
+    mbar_arrive_expect_tx(bar, (uint32_t)(rows * 128 * C::kColBoxes));
+    int r0 = 0;
+#pragma unroll
+    for (int t = 0; t < 3; ++t) {
+        const int h = 64 >> t;
+        if (rows & h) {
+#pragma unroll
+            for (int cb = 0; cb < C::kColBoxes; ++cb)
+                tma_load_3d(dst + cb * kBoxBytes + r0 * 128, tails + t, cb * kBoxCols, c.j * kTile + r0,
+                            c.b * p.G + c.g, bar, pol);
+            r0 += h;
+        }
+    }
+}
+
+// Tensor-map rows of tile c.j worth loading: all 128, or for a segment's last tile
+// the rows holding attended positions, rounded up to 16 (tlen: T_b per sequence,
+// null when the batch leaves no room for it).
+template <class C>
+__device__ __forceinline__ int plain_tile_rows(const Cursor &c, const int *tlen) {
+    if (!tlen || c.j + 1 != c.tiles) return kTile;
+    const int rem = tlen[c.b] - (c.j << C::kTileShift);   // attended positions in the tile, >= 1
+    const int rows = C::kParts == 2 ? (rem + 1) >> 1 : rem;
+    return (rows + 15) & ~15;
 }
 
 // Producer, variant instances: tiles without an appended row stay on a short
@@ -532,7 +566,8 @@ __device__ __noinline__ void patch_tile(uint8_t *tile, const uint8_t *stage_row,
 template <int D, bool kPair, int N, int NH, int kVar>
 __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
     gqa_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+                         const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ TailMaps tails,
+                         const DecodeParams p) {
     using C = TcCfg<D, kPair, N, NH, kVar>;
     constexpr bool kExt = C::kExt, kPaged = C::kPaged;
     constexpr int SK = C::kSK, SV = C::kSV, QB = C::kQBuf, NP = C::kParts, PB = C::kPBuf;
@@ -610,6 +645,13 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_q);
+        if constexpr (kVar == 0) {
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+                tma_prefetch_desc(&tails.k[t]);
+                tma_prefetch_desc(&tails.v[t]);
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(s_tmem, C::kTmemCols);
@@ -628,7 +670,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
     // first copies; the other roles wait for it on an mbarrier.
     bool pre_ok = true;
     if (warp == 0) {
-        build_prefix_warp(p, C::kTileShift, prefix, scratch + 32, p.flags);
+        build_prefix_warp(p, C::kTileShift, prefix, scratch + 32, p.flags, seq_len_array(prefix, p.B));
         mbar_arrive(prebar);
     } else {
         pre_ok = mbar_wait(prebar, 0, ab);   // false only if the CTA aborts: its roles then do nothing
@@ -648,6 +690,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
         // range first, then one claimed chunk at a time, then an end marker.
         if (lane == 0) {
             GQA_TRACE_AT(kTrProdIn, clock64());
+            const int *tlen = seq_len_array(prefix, p.B);   // plain instances: the last tiles' lengths
             const uint64_t pol_kv = l2_policy_evict_first();
             const uint64_t pol_q = l2_policy_evict_last();
             RangeEntry next{0, 0, -1};
@@ -743,7 +786,11 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                             produce_variant_tile<C>(p, &tm_k, kdst, &kfull[st], kc, T, pol_kv, p.k_new,
                                                     kstage + st * C::kRowBytes, &kinfo[st], p.k_dst, ids);
                         } else {
-                            produce_plain_tile<C>(p, &tm_k, kdst, &kfull[st], kc, pol_kv);
+                            const int rows = plain_tile_rows<C>(kc, tlen);
+                            if (rows == kTile)
+                                produce_plain_tile<C>(p, &tm_k, kdst, &kfull[st], kc, pol_kv);
+                            else
+                                produce_tail_tile<C>(p, tails.k, kdst, &kfull[st], kc, pol_kv, rows);
                         }
                         if constexpr (kPaged) mbar_arrive(&idempty[i % C::kIdRing]);   // the ids are no longer read here
                         if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i + 1, clock64());
@@ -780,7 +827,11 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                             produce_variant_tile<C>(p, &tm_v, vdst, &vfull[st], vc, T, pol_kv, p.v_new,
                                                     vstage + st * C::kRowBytes, &vinfo[st], p.v_dst, ids);
                         } else {
-                            produce_plain_tile<C>(p, &tm_v, vdst, &vfull[st], vc, pol_kv);
+                            const int rows = plain_tile_rows<C>(vc, tlen);
+                            if (rows == kTile)
+                                produce_plain_tile<C>(p, &tm_v, vdst, &vfull[st], vc, pol_kv);
+                            else
+                                produce_tail_tile<C>(p, tails.v, vdst, &vfull[st], vc, pol_kv, rows);
                         }
                         if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i + 3, clock64());
                         if (i < 128) GQA_TRACE_AT(kTrVIssue + i, clock64());
@@ -1576,8 +1627,8 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
 }
 
 template <int D, bool kPair, int N, int NH, int kVar>
-cudaError_t launch_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const DecodeParams &p,
-                        int ctas, cudaStream_t stream) {
+cudaError_t launch_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const TailMaps &tails,
+                        const DecodeParams &p, int ctas, cudaStream_t stream) {
     using C = TcCfg<D, kPair, N, NH, kVar>;
     auto kern = gqa_decode_tc_kernel<D, kPair, N, NH, kVar>;
     static unsigned long long attr_set = 0;   // one bit per device; setting twice is harmless
@@ -1589,31 +1640,32 @@ cudaError_t launch_tc_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUte
         if (e != cudaSuccess) return e;
         attr_set |= bit;
     }
-    return launch_pdl(kern, ctas, C::kThreads, C::kSmemBytes, stream, tk, tv, tq, p);
+    return launch_pdl(kern, ctas, C::kThreads, C::kSmemBytes, stream, tk, tv, tq, tails, p);
 }
 
 template <int D, bool kPair, int kVar>
-cudaError_t launch_tc_d(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const DecodeParams &p,
-                        int ctas, cudaStream_t stream) {
+cudaError_t launch_tc_d(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq, const TailMaps &tails,
+                        const DecodeParams &p, int ctas, cudaStream_t stream) {
     const int n = p.n;
-    if (n <= 1) return launch_tc_t<D, kPair, 16, 1, kVar>(tk, tv, tq, p, ctas, stream);
-    if (n <= 2) return launch_tc_t<D, kPair, 16, 2, kVar>(tk, tv, tq, p, ctas, stream);
-    if (n <= 4) return launch_tc_t<D, kPair, 16, 4, kVar>(tk, tv, tq, p, ctas, stream);
-    if (n <= 8) return launch_tc_t<D, kPair, 16, 8, kVar>(tk, tv, tq, p, ctas, stream);
-    if (n <= 16) return launch_tc_t<D, kPair, 16, 16, kVar>(tk, tv, tq, p, ctas, stream);
+    if (n <= 1) return launch_tc_t<D, kPair, 16, 1, kVar>(tk, tv, tq, tails, p, ctas, stream);
+    if (n <= 2) return launch_tc_t<D, kPair, 16, 2, kVar>(tk, tv, tq, tails, p, ctas, stream);
+    if (n <= 4) return launch_tc_t<D, kPair, 16, 4, kVar>(tk, tv, tq, tails, p, ctas, stream);
+    if (n <= 8) return launch_tc_t<D, kPair, 16, 8, kVar>(tk, tv, tq, tails, p, ctas, stream);
+    if (n <= 16) return launch_tc_t<D, kPair, 16, 16, kVar>(tk, tv, tq, tails, p, ctas, stream);
     if constexpr (!kPair) {
-        if (n <= 32) return launch_tc_t<D, kPair, 32, 32, kVar>(tk, tv, tq, p, ctas, stream);
-        return launch_tc_t<D, kPair, 64, 64, kVar>(tk, tv, tq, p, ctas, stream);
+        if (n <= 32) return launch_tc_t<D, kPair, 32, 32, kVar>(tk, tv, tq, tails, p, ctas, stream);
+        return launch_tc_t<D, kPair, 64, 64, kVar>(tk, tv, tq, tails, p, ctas, stream);
     }
     return cudaErrorNotSupported;
 }
 
 template <int kVar>
 cudaError_t launch_tc_layout(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
-                             const DecodeParams &p, int D, bool paired, int ctas, cudaStream_t stream) {
-    if (D == 128) return launch_tc_d<128, false, kVar>(tk, tv, tq, p, ctas, stream);
-    if (paired) return launch_tc_d<64, true, kVar>(tk, tv, tq, p, ctas, stream);
-    return launch_tc_d<64, false, kVar>(tk, tv, tq, p, ctas, stream);
+                             const TailMaps &tails, const DecodeParams &p, int D, bool paired, int ctas,
+                             cudaStream_t stream) {
+    if (D == 128) return launch_tc_d<128, false, kVar>(tk, tv, tq, tails, p, ctas, stream);
+    if (paired) return launch_tc_d<64, true, kVar>(tk, tv, tq, tails, p, ctas, stream);
+    return launch_tc_d<64, false, kVar>(tk, tv, tq, tails, p, ctas, stream);
 }
 
 }  // namespace
@@ -1625,11 +1677,12 @@ int tc_rows_for(int n) { return n <= 16 ? 16 : (n <= 32 ? 32 : 64); }
 bool tc_paired(int D, int Lmax, int n) { return D == 64 && Lmax % 2 == 0 && n <= 16; }
 
 cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
-                             const DecodeParams &p, int D, bool paired, int ctas, cudaStream_t stream) {
+                             const TailMaps &tails, const DecodeParams &p, int D, bool paired, int ctas,
+                             cudaStream_t stream) {
     // the variants run the instances built for them
-    if (p.block_table) return launch_tc_layout<2>(tk, tv, tq, p, D, paired, ctas, stream);
-    if (p.window > 0 || p.k_new) return launch_tc_layout<1>(tk, tv, tq, p, D, paired, ctas, stream);
-    return launch_tc_layout<0>(tk, tv, tq, p, D, paired, ctas, stream);
+    if (p.block_table) return launch_tc_layout<2>(tk, tv, tq, tails, p, D, paired, ctas, stream);
+    if (p.window > 0 || p.k_new) return launch_tc_layout<1>(tk, tv, tq, tails, p, D, paired, ctas, stream);
+    return launch_tc_layout<0>(tk, tv, tq, tails, p, D, paired, ctas, stream);
 }
 
 }  // namespace gqa

@@ -34,13 +34,22 @@ int simt_max_heads();
 cudaError_t launch_decode_simt(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p, int D,
                                int ctas, cudaStream_t stream);
 
+// The contiguous cache's tensor maps again, with boxes of 64, 32 and 16 rows:
+// the last tile of a segment is loaded only as far as its attended rows reach
+// (rounded up to 16 rows).  Unused (zero) for a paged cache.
+struct TailMaps {
+    CUtensorMap k[3];
+    CUtensorMap v[3];
+};
+
 int tc_max_heads();
 int tc_rows_for(int n);   // rows of the q tensor-map box (n rounded up to 16, 32 or 64)
 // Whether the tensor-core kernel reads this shape's cache in the paired layout
 // (D = 64: rows of two positions, 256-position tiles, tile_shift 8).
 bool tc_paired(int D, int Lmax, int n);
 cudaError_t launch_decode_tc(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tq,
-                             const DecodeParams &p, int D, bool paired, int ctas, cudaStream_t stream);
+                             const TailMaps &tails, const DecodeParams &p, int D, bool paired, int ctas,
+                             cudaStream_t stream);
 
 // Leading bytes of a decode workspace that must be zero before its first call:
 // GQA_WORKSPACE_HEADER_BYTES (flag word, dynamic-pool ticket, failed-claim
