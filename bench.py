@@ -1,23 +1,33 @@
 """Benchmark of one GQA decode step (KV-cache HBM GB/s and decode steps/s).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--secondary NAME|none] [--variant ...] [--repeat-seconds S]
 
 One step = one gqa_decode call on the workload's whole batch (one layer), with
-the bf16 KV cache resident in HBM.  GB/s counts algorithmic bytes only: the
-valid K and V rows, sum_b seq_lens[b] * G * d * 2 bytes * 2.
+the bf16 KV cache resident in HBM: the decode kernel plus the split-combine
+kernel that follows it (programmatic dependent launch).  GB/s counts
+algorithmic bytes only: the attended K and V rows,
+sum_b seq_lens[b] * G * d * 2 bytes * 2.  The headline workload is the
+Llama-3-70B-shaped batch (the largest single-GPU configuration); the
+Mistral-7B-shaped step is measured in the same run and reported beside it
+("secondary").
 
 L2: inputs larger than L2.  The K/V caches are held in C copies and step i
 reads copy i % C, with C chosen so that the C - 1 steps between two reads of a
 copy stream at least three L2 capacities of other data; no step finds its
 cache in L2.  (A write-flush between steps is not used: the dirty lines it
 leaves slow the next kernel down by write-back traffic that is not its own.)
-The K steps run back to back on one stream between one pair of CUDA events;
-a step is the decode kernel plus the split-combine kernel that follows it
-(programmatic dependent launch), so total time / K is the average duration of
-one whole step.
 
-``--variant meanpool`` times the K/V mean-pool conversion instead (one call per
-step on one projection; GB/s counts its input and output bytes).
+Timing: after W warm-up steps, K steps are captured in a CUDA graph (calls
+through the public API, captured on one stream; the copy schedule continues
+across replays).  A block = one replay = K steps back to back between its own
+pair of CUDA events; R blocks run back to back (R chosen so that they take
+about --repeat-seconds, for the clock samples), and ms_per_step = the median
+block / K.  The read-bandwidth ceiling (a read-only TMA stream with the decode's
+boxes, libgqa_b300_bench.so) is measured in the same run.
+
+``--variant meanpool`` times the K/V mean-pool conversion instead; ``--variant
+readonly`` prints the read-only stream's own line.
 
 Under torchrun (N > 1) every rank runs an independent replica of the step on
 its own GPU (nothing is sharded); value = bytes of all ranks / max time.
@@ -218,7 +228,7 @@ def run_reference(args, rank: int) -> None:
     if args.variant == "meanpool":
         run_reference_meanpool(args)
         return
-    cfg = workload(args.workload or "mistral7b")
+    cfg = workload(args.workload or "llama3_70b")
     inp = make_decode_inputs(cfg, poison_tail=False)
     nrows_all = cfg.B * cfg.H
     cores = oracle.num_threads()
@@ -242,7 +252,8 @@ def run_reference(args, rank: int) -> None:
         "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": config_dict(cfg, inp, extra={"sample_rows_per_step": nrow}),
+        "config": config_dict(cfg, inp, extra={"variant": variant_note(args.variant, args)}),
+        "measurement": {"sample_rows_per_step": nrow, "timing": "host wall clock per step"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{nrow} of {nrows_all} output rows (query heads of sequences) per step, "
                                    f"seeded order, float64 oracle (OpenMP over rows)"},
@@ -303,6 +314,7 @@ def variant_note(variant, args):
 
 
 def config_dict(cfg, inp, extra=None):
+    """The workload's definition (the same keys and values in both arms' lines)."""
     d = {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "G": cfg.G, "d": cfg.d, "Lmax": cfg.Lmax,
          "seq_lens": (list(cfg.fixed_seq) if cfg.fixed_seq else f"U[{cfg.seq_lo},{cfg.seq_hi}] seeded"),
          "kv_bytes_per_step": inp.kv_bytes, "inputs": "N(0,1) -> bf16, seeded",
@@ -312,6 +324,84 @@ def config_dict(cfg, inp, extra=None):
     return d
 
 
+def time_blocks(torch, dist, run_block, stream, world, dev, repeat_seconds, local_rank):
+    """Times R back-to-back blocks (run_block(r) enqueues block r on `stream`), each between its own
+    pair of CUDA events, with nvidia-smi clock samples during them; R is chosen from a first block so
+    that they take about `repeat_seconds`.  Returns (median block ms, max over ranks), the sorted
+    block times, R and the clock summary."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run_block(0)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    est = max(float(e0.elapsed_time(e1)), 1e-3)
+    R = int(min(20000, max(3, math.ceil(repeat_seconds * 1e3 / est))))
+    if world > 1:   # every rank runs the same number of blocks
+        t = torch.tensor([R], dtype=torch.int64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        R = int(t.item())
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(R)]
+    with ClockSampler(local_rank) as clk:
+        for r, (a, b) in enumerate(evs):
+            a.record(stream)
+            run_block(r + 1)
+            b.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    blocks = sorted(float(a.elapsed_time(b)) for a, b in evs)
+    med = max_over_ranks(statistics.median(blocks), world, dev)
+    return med, blocks, R, clk.summary()
+
+
+def block_stats(blocks, R, steps):
+    return {"blocks": R, "steps_per_block": steps, "median_ms": statistics.median(blocks),
+            "p10_ms": blocks[int(0.1 * (len(blocks) - 1))], "p90_ms": blocks[int(0.9 * (len(blocks) - 1))]}
+
+
+def make_graphs(torch, step, stream, K, period):
+    """CUDA graphs of K steps (step(i) enqueues step i through the public API on the current stream),
+    one for each starting offset of the copy schedule (i mod period), so that consecutive blocks
+    continue the schedule; None if capture is not available."""
+    offsets = []
+    o = 0
+    while o not in offsets:
+        offsets.append(o)
+        o = (o + K) % period
+    graphs = {}
+    try:
+        for o in offsets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(K):
+                    step(o + i)
+            graphs[o] = g
+    except RuntimeError:
+        return None, offsets
+    return graphs, offsets
+
+
+def block_runner(torch, step, stream, K, period):
+    """run_block(r): block r of K steps, as a graph replay (or K eager calls if capture fails)."""
+    graphs, offsets = make_graphs(torch, step, stream, K, period)
+
+    def run_block(r):
+        o = offsets[r % len(offsets)]
+        if graphs is not None:
+            graphs[o].replay()
+        else:
+            for i in range(K):
+                step(o + i)
+
+    with torch.cuda.stream(stream):   # warm the graphs (and the eager path's host side)
+        for r in range(len(offsets)):
+            run_block(r)
+    torch.cuda.synchronize()
+    return run_block, graphs is not None
+
+
 def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
     """Times gqa_meanpool_kv: [H, h, d_model] fp32 -> [G, h, d_model] fp32, one call per step."""
     name, shp = meanpool_workload(args.workload or "t5xxl_sweep_G8")
@@ -319,7 +409,7 @@ def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
     w_h = make_meanpool_input(H, G, h, dm, shp["config_id"])
     in_bytes, out_bytes = w_h.nbytes, G * h * dm * 4
     alg = in_bytes + out_bytes                  # each input read once, each output written once
-    stream = torch.cuda.current_stream(dev)
+    stream = torch.cuda.Stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     copies = max(3, math.ceil(L2_COPIES_SPAN * l2 / alg) + 1)
     w = torch.from_numpy(w_h).to(dev)
@@ -328,34 +418,26 @@ def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
 
     def step(i):
         c = i % copies
-        gqa.meanpool_kv(ws[c], G, out=outs[c], stream=stream)
+        gqa.meanpool_kv(ws[c], G, out=outs[c], stream=torch.cuda.current_stream(dev))
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
-        t0.record(stream)
-        for i in range(args.steps):
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
             step(i)
-        t1.record(stream)
-        torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    total_ms = max_over_ranks(float(t0.elapsed_time(t1)), world, dev)
-    ms_per_step = total_ms / args.steps
-    value = whole_job_gbs(alg, args.steps, world, total_ms)
+    torch.cuda.synchronize()
+    run_block, graphed = block_runner(torch, step, stream, args.steps, copies)
+    with torch.cuda.stream(stream):
+        med_ms, blocks, R, clocks = time_blocks(torch, dist, run_block, stream, world, dev, args.repeat_seconds,
+                                                local_rank)
+    ms_per_step = med_ms / args.steps
+    value = whole_job_gbs(alg, args.steps, world, med_ms)
 
     hw = torch.from_numpy(w_h).pin_memory()
     hout = torch.empty((G, h, dm), dtype=torch.float32).pin_memory()
+    cur = torch.cuda.current_stream(dev)
 
     def e2e_step():
         w.copy_(hw, non_blocking=True)
-        gqa.meanpool_kv(w, G, out=outs[0], stream=stream)
+        gqa.meanpool_kv(w, G, out=outs[0], stream=cur)
         hout.copy_(outs[0], non_blocking=True)
 
     for _ in range(3):
@@ -363,10 +445,10 @@ def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(cur)
     for _ in range(args.e2e_steps):
         e2e_step()
-    e1.record(stream)
+    e1.record(cur)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
     if rank != 0:
@@ -397,7 +479,8 @@ def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU", "copies": copies,
                    "l2": f"inputs larger than L2: {copies} input/output copies, step i uses copy i % {copies}"
                          if copies * alg > l2 else "fits in L2: launch-bound, not an HBM figure",
-                   "timing": "K calls back to back between one pair of CUDA events"},
+                   "timing": ("median of R blocks of K calls, each block a CUDA-graph replay between its own "
+                              "pair of CUDA events" if graphed else "median of R blocks of K eager calls")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": profiled_traffic("meanpool_kernel", name), "kernel": "meanpool_kernel",
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
@@ -406,34 +489,264 @@ def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
         "e2e": {"value": alg / (e2e_ms / 1e3) / 1e9 * world, "unit": UNIT, "h2d_bytes_per_step": in_bytes,
                 "d2h_bytes_per_step": out_bytes, "steps": args.e2e_steps,
                 "what": "H2D of the projection from pinned host memory + the conversion + D2H of the result"},
-        "gpu_launches": args.steps,
-        "clocks": clk.summary(),
+        "timing": block_stats(blocks, R, args.steps),
+        "gpu_launches": args.steps * R,
+        "clocks": clocks,
     }
+    print(json.dumps(line), flush=True)
+
+
+READONLY_SHAPE = (1024, 8192)   # [z, rows] of 256-byte rows: 2 GiB, 17x the L2
+
+
+def measure_readonly(torch, dist, gqa, dev, world, local_rank, repeat_seconds):
+    """The read-bandwidth ceiling: GB/s of the read-only TMA stream (gqa_bench.h) over a 2 GiB buffer,
+    median of R calls, each between its own pair of CUDA events."""
+    z, rows = READONLY_SHAPE
+    buf = torch.empty((z, rows, 128), dtype=torch.bfloat16, device=dev)
+    buf.view(torch.int16).fill_(0x3F80)    # bf16 1.0: the data is never used, only read
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    nbytes = buf.numel() * 2
+
+    def run_block(r):
+        gqa.stream_read(buf, flags, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            run_block(0)
+    torch.cuda.synchronize()
+    med_ms, blocks, R, clocks = time_blocks(torch, dist, run_block, stream, world, dev, repeat_seconds, local_rank)
+    torch.cuda.synchronize()
+    if int(flags.item()) != 0:
+        raise RuntimeError(f"read-only stream reported flags 0x{int(flags.item()):x}")
+    del buf
+    return {"value": nbytes / (med_ms / 1e3) / 1e9, "best": nbytes / (blocks[0] / 1e3) / 1e9, "unit": UNIT,
+            "bytes_per_call": nbytes, "calls": R, "clocks": clocks,
+            "what": "read-only TMA stream, one CTA per SM, the decode's 64-column x 128-row boxes (two per 32 KiB "
+                    "tile), six-stage ring, 2 GiB buffer; median of R calls"}
+
+
+def decode_case(args, cfg, variant, torch, gqa, dev):
+    """Inputs, cache copies, workspace and the step function of one decode workload on the device."""
+    if variant == "cross":   # every one of the Lmax positions is valid
+        inp = make_decode_inputs(cfg, poison_tail=False, seq_lens=[cfg.Lmax] * cfg.B)
+    else:
+        inp = make_decode_inputs(cfg, poison_tail=False)
+    window = args.window if variant == "window" else 0
+    attended = np.minimum(inp.seq_lens.astype(np.int64), window) if window else inp.seq_lens.astype(np.int64)
+    kv_bytes = int(attended.sum()) * cfg.G * cfg.d * 2 * 2   # algorithmic K+V bytes of one step
+    scale = float(inp.scale)
+    path = args.path or gqa.select_path(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax)
+    if variant != "contiguous" and path != gqa.PATH_TCGEN05:
+        raise SystemExit("the decode variants run on the tensor-core path")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    def to_dev(a, dtype=torch.bfloat16):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(dtype) if dtype == torch.bfloat16 else t).to(dev)
+
+    q = to_dev(inp.q)
+    sl = to_dev(inp.seq_lens, torch.int32)
+    kn = vn = kn_h = vn_h = None
+    if variant == "paged":
+        kp, vp, table = make_paged_layout(inp, args.page_size)
+        k, v, tbl = to_dev(kp), to_dev(vp), to_dev(table, torch.int32)
+        host_kv = (kp, vp, table)
+    else:
+        k, v, tbl = to_dev(inp.k), to_dev(inp.v), None
+        host_kv = (inp.k, inp.v)
+    if variant == "append":
+        kn_h, vn_h = make_new_rows(cfg)
+        kn, vn = to_dev(kn_h), to_dev(vn_h)
+    copies = max(3, math.ceil(L2_COPIES_SPAN * l2 / kv_bytes) + 1)
+    ks = [k] + [k.clone() for _ in range(copies - 1)]
+    vs = [v] + [v.clone() for _ in range(copies - 1)]
+    out = torch.empty((cfg.B, cfg.H, cfg.d), dtype=torch.float32, device=dev)
+    ws = gqa.alloc_workspace(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax, dev)
+
+    def call(kk, vv):
+        st = torch.cuda.current_stream(dev)
+        if variant == "paged":
+            gqa.decode_paged(q, kk, vv, tbl, sl, out=out, workspace=ws, scale=scale, stream=st)
+        elif variant == "append":
+            gqa.decode_append(q, kn, vn, kk, vv, sl, out=out, workspace=ws, scale=scale, stream=st)
+        else:
+            gqa.decode(q, kk, vv, None if variant == "cross" else sl, out=out, workspace=ws, scale=scale,
+                       stream=st, path=path, window=window)
+
+    def step(i):
+        c = i % copies
+        call(ks[c], vs[c])
+
+    return dict(inp=inp, kv_bytes=kv_bytes, path=path, copies=copies, step=step, call=call, q=q, sl=sl, k=k, v=v,
+                tbl=tbl, kn=kn, vn=vn, kn_h=kn_h, vn_h=vn_h, host_kv=host_kv, out=out, ws=ws, window=window)
+
+
+def measure_decode(args, cfg, variant, world, local_rank, dev, torch, dist, gqa, e2e=True):
+    """The timed step of one decode workload (see the module docstring) and its end-to-end figure."""
+    c = decode_case(args, cfg, variant, torch, gqa, dev)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            c["step"](i)
+    torch.cuda.synchronize()
+    run_block, graphed = block_runner(torch, c["step"], stream, args.steps, c["copies"])
+    with torch.cuda.stream(stream):
+        med_ms, blocks, R, clocks = time_blocks(torch, dist, run_block, stream, world, dev, args.repeat_seconds,
+                                                local_rank)
+    flags = gqa.read_flags(c["ws"])
+    if flags:
+        raise RuntimeError(f"decode reported flags 0x{flags:x} during the benchmark")
+    res = {"cfg": cfg, "inp": c["inp"], "kv_bytes": c["kv_bytes"], "path": c["path"], "copies": c["copies"],
+           "ms_per_step": med_ms / args.steps, "value": whole_job_gbs(c["kv_bytes"], args.steps, world, med_ms),
+           "timing": block_stats(blocks, R, args.steps), "R": R, "clocks": clocks, "graphed": graphed,
+           "window": c["window"]}
+    if e2e:
+        res["e2e"] = measure_e2e(args, c, variant, world, dev, torch)
+    return res
+
+
+def measure_e2e(args, c, variant, world, dev, torch):
+    """The same metric through the public API with host buffers: every step copies all of its inputs
+    from pinned host memory (the whole caches or page pools included), decodes, and reads out back."""
+    def pinned(a, dtype=torch.bfloat16):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(dtype) if dtype == torch.bfloat16 else t).pin_memory()
+
+    inp = c["inp"]
+    host = [(c["q"], pinned(inp.q)), (c["sl"], pinned(inp.seq_lens, torch.int32)), (c["k"], pinned(c["host_kv"][0])),
+            (c["v"], pinned(c["host_kv"][1]))]
+    if c["tbl"] is not None:
+        host.append((c["tbl"], pinned(c["host_kv"][2], torch.int32)))
+    if variant == "append":
+        host += [(c["kn"], pinned(c["kn_h"])), (c["vn"], pinned(c["vn_h"]))]
+    out = c["out"]
+    hout = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for _, h in host)
+    d2h = hout.numel() * 4
+    cur = torch.cuda.current_stream(dev)
+
+    def e2e_step():
+        for dst, src in host:
+            dst.copy_(src, non_blocking=True)
+        c["call"](c["k"], c["v"])
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    return {"value": whole_job_gbs(c["kv_bytes"], 1, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "what": "H2D of every input (q, seq_lens, the whole K/V caches or page pools, the block table and "
+                    "appended rows where used) from pinned host memory + the decode call + D2H of out, per step"}
+
+
+def roofline_of(res, variant, readonly, kernel="gqa_decode_tc_kernel"):
+    peak, peak_kind = measured_peak()
+    achieved = res["kv_bytes"] / (res["ms_per_step"] / 1e3) / 1e9
+    r = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+         "traffic": profiled_traffic(kernel, res["cfg"].name) if variant == "contiguous" else None,
+         "kernel": kernel, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind}, a copy)",
+         "algorithmic_bytes_per_launch": res["kv_bytes"], "frac_of_8TBps_nominal": achieved / 8000.0,
+         "achieved_covers": "whole steps (decode kernel + split-combine kernel)"}
+    if readonly:
+        r["readonly_peak"] = readonly["value"]
+        r["frac_of_readonly"] = achieved / readonly["value"]
+        r["readonly_peak_source"] = "measured in this run: gqa_bench_stream_read (read-only TMA stream)"
+    return r
+
+
+def cpu_baseline_decode(inp, window):
+    """The float64 oracle on the host cores (all of them, then one thread), each on a bounded sample of
+    the workload's (batch, K/V head) segments."""
+    import oracle
+    cfg = inp.cfg
+    segs = all_segments(cfg)
+
+    def sample(seconds):
+        cpu_oracle_step(inp, segs[:1], window)               # warm: thread pool, page faults
+        t, _ = cpu_oracle_step(inp, segs[:1], window)
+        nseg = int(max(1, min(len(segs), seconds / max(t, 1e-4))))
+        total_t, total_b, passes = 0.0, 0, 0
+        while total_t < seconds and passes < 1000:
+            t, b = cpu_oracle_step(inp, segs[:nseg], window)
+            total_t += t
+            total_b += b
+            passes += 1
+        return total_b / total_t / 1e9, nseg, passes, total_t
+
+    cores = oracle.num_threads()
+    v, nseg, passes, tt = sample(CPU_BASELINE_SECONDS)
+    oracle.set_num_threads(1)
+    try:
+        v1, nseg1, passes1, tt1 = sample(CPU_BASELINE_SECONDS / 2)
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{passes} pass(es) over {nseg} of {len(segs)} (batch, K/V head) segments, all H/G query "
+                      f"heads each, float64 oracle, {tt:.1f} s after one warm-up pass",
+            "cores_1": {"value": v1, "unit": UNIT, "cores": 1,
+                        "sample": f"{passes1} pass(es) over {nseg1} segments, one thread, {tt1:.1f} s"}}
+
+
+def run_readonly(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
+    """--variant readonly: the read-only stream's own line."""
+    ro = measure_readonly(torch, dist, gqa, dev, world, local_rank, args.repeat_seconds)
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    line = {"metric": "read-only TMA stream GB/s (the decode's read ceiling), 1 GPU", "value": ro["value"] * world,
+            "unit": UNIT, "n_gpus": world, "steps": ro["calls"], "warmup": 3,
+            "ms_per_step": ro["bytes_per_call"] / ro["value"] / 1e6, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "readonly_stream", "bytes_per_step": ro["bytes_per_call"], "what": ro["what"]},
+            "roofline": {"bound": "hbm", "achieved": ro["value"], "peak": peak, "unit": "GB/s",
+                         "frac": ro["value"] / peak, "traffic": None, "kernel": "stream_read_kernel",
+                         "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind}, a copy)"},
+            "best": ro["best"], "gpu_launches": ro["calls"], "clocks": ro["clocks"]}
     print(json.dumps(line), flush=True)
 
 
 def main() -> None:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=None,
-                    help="mistral7b (default) | llama3_70b | long_ragged | tiny | t5xxl_sweep_G<1..64>; "
+                    help="llama3_70b (default) | mistral7b | long_ragged | tiny | t5xxl_sweep_G<1..64>; "
                          "--variant meanpool: tiny | t5xxl_sweep_G<g> (default t5xxl_sweep_G8)")
+    ap.add_argument("--secondary", default="mistral7b",
+                    help="a second workload measured in the same run and reported in the line's 'secondary' "
+                         "object (contiguous cache only; 'none' to skip)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", type=int, default=0, help="0 auto, 1 simt, 2 tcgen05")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--repeat-seconds", type=float, default=1.5,
+                    help="about how long the repeated timed blocks of a workload take (clock samples)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-readonly", action="store_true", help="skip the read-only ceiling measurement")
     ap.add_argument("--variant", default="contiguous",
-                    choices=["contiguous", "paged", "append", "cross", "window", "meanpool"],
+                    choices=["contiguous", "paged", "append", "cross", "window", "meanpool", "readonly"],
                     help="contiguous cache (default); paged cache (--page-size); fused append of the new "
                          "token's K/V rows; cross-attention (every position valid); sliding window (--window); "
-                         "meanpool: the K/V mean-pool conversion instead of the decode")
+                         "meanpool: the K/V mean-pool conversion instead of the decode; readonly: the read-only "
+                         "stream that bounds the decode")
     ap.add_argument("--page-size", type=int, default=64)
     ap.add_argument("--window", type=int, default=1024)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -452,197 +765,70 @@ def main() -> None:
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     build_lib.build()
+    build_lib.build(bench=True)
     gqa.load()
-    if args.variant == "meanpool":
-        run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa)
-        if world > 1:
-            dist.destroy_process_group()
-        return
-
-    cfg = workload(args.workload or "mistral7b")
-    variant = args.variant
-    if variant == "cross":   # every one of the Lmax positions is valid
-        inp = make_decode_inputs(cfg, poison_tail=False, seq_lens=[cfg.Lmax] * cfg.B)
-    else:
-        inp = make_decode_inputs(cfg, poison_tail=False)
-    window = args.window if variant == "window" else 0
-    attended = np.minimum(inp.seq_lens.astype(np.int64), window) if window else inp.seq_lens.astype(np.int64)
-    kv_bytes = int(attended.sum()) * cfg.G * cfg.d * 2 * 2   # algorithmic K+V bytes of one step
-    stream = torch.cuda.current_stream(dev)
-    scale = float(inp.scale)
-    path = args.path or gqa.select_path(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax)
-    if variant != "contiguous" and path != gqa.PATH_TCGEN05:
-        ap.error("the decode variants run on the tensor-core path")
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-
-    def to_dev(a, dtype=torch.bfloat16):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return (t.view(dtype) if dtype == torch.bfloat16 else t).to(dev)
-
-    q = to_dev(inp.q)
-    sl = to_dev(inp.seq_lens, torch.int32)
-    if variant == "paged":
-        kp, vp, table = make_paged_layout(inp, args.page_size)
-        k, v, tbl = to_dev(kp), to_dev(vp), to_dev(table, torch.int32)
-        host_kv = (kp, vp, table)
-    else:
-        k, v, tbl = to_dev(inp.k), to_dev(inp.v), None
-        host_kv = (inp.k, inp.v)
-    if variant == "append":
-        kn_h, vn_h = make_new_rows(cfg)
-        kn, vn = to_dev(kn_h), to_dev(vn_h)
-    copies = max(3, math.ceil(L2_COPIES_SPAN * l2 / kv_bytes) + 1)
-    ks = [k] + [k.clone() for _ in range(copies - 1)]
-    vs = [v] + [v.clone() for _ in range(copies - 1)]
-    out = torch.empty((cfg.B, cfg.H, cfg.d), dtype=torch.float32, device=dev)
-    ws = gqa.alloc_workspace(cfg.B, cfg.H, cfg.G, cfg.d, cfg.Lmax, dev)
-
-    def call(kk, vv):
-        if variant == "paged":
-            gqa.decode_paged(q, kk, vv, tbl, sl, out=out, workspace=ws, scale=scale, stream=stream)
-        elif variant == "append":
-            gqa.decode_append(q, kn, vn, kk, vv, sl, out=out, workspace=ws, scale=scale, stream=stream)
+    try:
+        if args.variant == "meanpool":
+            run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa)
+        elif args.variant == "readonly":
+            run_readonly(args, world, rank, local_rank, dev, torch, dist, gqa)
         else:
-            gqa.decode(q, kk, vv, None if variant == "cross" else sl, out=out, workspace=ws, scale=scale,
-                       stream=stream, path=path, window=window)
-
-    def step(i):
-        c = i % copies
-        call(ks[c], vs[c])
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
-        t0.record(stream)
-        for i in range(args.steps):
-            step(i)
-        t1.record(stream)
-        torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    total_ms = max_over_ranks(float(t0.elapsed_time(t1)), world, dev)
-    ms_per_step = total_ms / args.steps
-    value = whole_job_gbs(kv_bytes, args.steps, world, total_ms)
-    flags = gqa.read_flags(ws)
-    if flags:
-        raise RuntimeError(f"decode reported flags 0x{flags:x} during the benchmark")
-
-    # ---- per-step distribution (extra information): each of a few hundred steps between its own
-    # pair of events; the events themselves serialise the steps, so this is not the headline number
-    nper = min(200, args.steps)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nper)]
-    for i, (ea, eb) in enumerate(evs):
-        ea.record(stream)
-        step(i)
-        eb.record(stream)
-    torch.cuda.synchronize()
-    per_us = sorted(1e3 * ea.elapsed_time(eb) for ea, eb in evs)
-    per_step = {"samples": nper, "median_us": statistics.median(per_us),
-                "p10_us": per_us[int(0.1 * (nper - 1))], "p90_us": per_us[int(0.9 * (nper - 1))],
-                "what": "each step alone between its own event pair: launch gaps included and no overlap "
-                        "with the neighbouring steps (the headline times K steps back to back)"}
-
-    # ---- end to end through the public API with host buffers (pinned)
-    def pinned(a, dtype=torch.bfloat16):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return (t.view(dtype) if dtype == torch.bfloat16 else t).pin_memory()
-
-    host = [(q, pinned(inp.q)), (sl, pinned(inp.seq_lens, torch.int32)), (k, pinned(host_kv[0])),
-            (v, pinned(host_kv[1]))]
-    if tbl is not None:
-        host.append((tbl, pinned(host_kv[2], torch.int32)))
-    if variant == "append":
-        host += [(kn, pinned(kn_h)), (vn, pinned(vn_h))]
-    hout = torch.empty((cfg.B, cfg.H, cfg.d), dtype=torch.float32).pin_memory()
-    h2d = sum(h.numel() * h.element_size() for _, h in host)
-    d2h = hout.numel() * 4
-
-    def e2e_step():
-        for dst, src in host:
-            dst.copy_(src, non_blocking=True)
-        call(k, v)
-        hout.copy_(out, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
-    e2e_value = whole_job_gbs(kv_bytes, 1, world, e2e_ms)
-
-    if rank != 0:
+            run_decode(args, world, rank, local_rank, dev, torch, dist, gqa)
+    finally:
         if world > 1:
             dist.destroy_process_group()
+
+
+def run_decode(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
+    variant = args.variant
+    cfg = workload(args.workload or "llama3_70b")
+    prim = measure_decode(args, cfg, variant, world, local_rank, dev, torch, dist, gqa)
+    torch.cuda.empty_cache()
+    sec = None
+    if args.secondary != "none" and variant == "contiguous" and args.secondary != cfg.name:
+        sec = measure_decode(args, workload(args.secondary), "contiguous", world, local_rank, dev, torch, dist, gqa,
+                             e2e=False)
+        torch.cuda.empty_cache()
+    readonly = None if args.no_readonly else measure_readonly(torch, dist, gqa, dev, world, local_rank,
+                                                             min(args.repeat_seconds, 0.5))
+    if rank != 0:
         return
-
-    peak, peak_kind = measured_peak()
-    kernel = "gqa_decode_tc_kernel" if path == gqa.PATH_TCGEN05 else "gqa_decode_simt_kernel"
-    achieved = kv_bytes / (ms_per_step / 1e3) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(kernel, cfg.name) if variant == "contiguous" else None,
-                "kernel": kernel,
-                "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
-                "algorithmic_bytes_per_launch": kv_bytes,
-                "frac_of_8TBps_nominal": achieved / 8000.0}
-
-    cpu = None
-    if not args.no_cpu_baseline:
-        import oracle
-        segs = all_segments(cfg)
-        cpu_oracle_step(inp, segs[:1], window)               # warm: thread pool, page faults
-        t, _ = cpu_oracle_step(inp, segs[:1], window)
-        nseg = int(max(1, min(len(segs), CPU_BASELINE_SECONDS / max(t, 1e-4))))
-        total_t, total_b, passes = 0.0, 0, 0
-        while total_t < CPU_BASELINE_SECONDS and passes < 1000:
-            t, b = cpu_oracle_step(inp, segs[:nseg], window)
-            total_t += t
-            total_b += b
-            passes += 1
-        cpu = {"value": total_b / total_t / 1e9, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-               "sample": f"{passes} pass(es) over {nseg} of {len(segs)} (batch, K/V head) segments, all H/G "
-                         f"query heads each, float64 oracle, {total_t:.1f} s after one warm-up pass"}
-
+    kernel = "gqa_decode_tc_kernel" if prim["path"] == gqa.PATH_TCGEN05 else "gqa_decode_simt_kernel"
+    cpu = None if args.no_cpu_baseline else cpu_baseline_decode(prim["inp"], prim["window"])
+    timing = ("K steps captured in CUDA graphs (public API calls); the median of R blocks, each one graph "
+              "replay between its own pair of CUDA events" if prim["graphed"] else
+              "the median of R blocks of K eager steps, each between its own pair of CUDA events")
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if path == gqa.PATH_TCGEN05 else "f32", "data": "synthetic",
-        "steps_per_s": world * 1e3 / ms_per_step,
-        "config": config_dict(cfg, inp, extra={"path": "tcgen05" if path == gqa.PATH_TCGEN05 else "simt",
-                                               "variant": variant_note(variant, args),
-                                               "kv_bytes_per_step": kv_bytes,
-                                               "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                                               "cache_copies": copies,
-                                               "l2": f"inputs larger than L2: K/V caches held in {copies} copies, "
-                                                     f"step i reads copy i % {copies}, so >= {L2_COPIES_SPAN} L2 "
-                                                     "capacities of other KV data stream between two reads of a copy",
-                                               "timing": "K steps back to back between one pair of CUDA events"}),
-        "roofline": roofline,
+        "metric": METRIC, "value": prim["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": prim["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if prim["path"] == gqa.PATH_TCGEN05 else "f32", "data": "synthetic",
+        "steps_per_s": world * 1e3 / prim["ms_per_step"],
+        "config": config_dict(cfg, prim["inp"], extra={"variant": variant_note(variant, args)}),
+        "measurement": {
+            "path": "tcgen05" if prim["path"] == gqa.PATH_TCGEN05 else "simt",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU", "cache_copies": prim["copies"],
+            "l2": f"K/V caches held in {prim['copies']} copies, step i reads copy i % {prim['copies']}, so >= "
+                  f"{L2_COPIES_SPAN} L2 capacities of other KV data stream between two reads of a copy",
+            "timing": timing},
+        "roofline": roofline_of(prim, variant, readonly, kernel),
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": args.e2e_steps,
-                "what": "H2D of every input (q, seq_lens, the whole K/V caches or page pools, the block table "
-                        "and appended rows where used) from pinned host memory + the decode call + D2H of "
-                        "out, per step"},
-        "per_step_events": per_step,
-        "gpu_launches": 2 * args.steps,   # decode kernel + split-combine kernel per step
-        "clocks": clk.summary(),
+        "e2e": prim["e2e"],
+        "timing": prim["timing"],
+        "gpu_launches": 2 * args.steps * prim["R"],   # decode + split-combine per step, every timed block
+        "clocks": prim["clocks"],
     }
+    if sec is not None:
+        line["secondary"] = {
+            "workload": sec["cfg"].name, "value": sec["value"], "unit": UNIT, "ms_per_step": sec["ms_per_step"],
+            "steps_per_s": world * 1e3 / sec["ms_per_step"],
+            "config": config_dict(sec["cfg"], sec["inp"], extra={"variant": variant_note("contiguous", args)}),
+            "cache_copies": sec["copies"],
+            "roofline": roofline_of(sec, "contiguous", readonly, kernel), "timing": sec["timing"],
+            "gpu_launches": 2 * args.steps * sec["R"], "clocks": sec["clocks"]}
+    if readonly is not None:
+        line["readonly_stream"] = {k: readonly[k] for k in ("value", "best", "unit", "bytes_per_call", "calls",
+                                                             "what")}
     print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
 
 
 if __name__ == "__main__":

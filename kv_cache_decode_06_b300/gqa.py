@@ -36,6 +36,9 @@ EXPORTS = ("gqa_status_string", "gqa_abi_version", "gqa_decode_workspace_size", 
            "gqa_decode_noalloc", "gqa_decode_append", "gqa_decode_paged")
 # Declared in include/gqa.h under GQA_TEST_HOOKS: exported by the test-hooks build only.
 TEST_HOOK_EXPORTS = ("gqa_debug_withhold_copy",)
+# Declared in include/gqa_bench.h: the measurement helper library (libgqa_b300_bench.so).
+BENCH_EXPORTS = ("gqa_bench_stream_read",)
+BENCH_LIB_PATH = os.path.join(_HERE, "libgqa_b300_bench.so")
 NOALLOC_WORKSPACE_BYTES = 8 << 20
 
 _lock = threading.Lock()
@@ -107,6 +110,40 @@ def load_test_hooks():
         raise RuntimeError(f"{TEST_HOOKS_LIB_PATH} is missing: build it with "
                            "`python -m kv_cache_decode_06_b300.build_lib --test-hooks`")
     return load(TEST_HOOKS_LIB_PATH)
+
+
+_bench_lib = None
+
+
+def load_bench():
+    """Load libgqa_b300_bench.so (``build_lib --bench``): the read-only stream of gqa_bench.h."""
+    global _bench_lib
+    if _bench_lib is not None:
+        return _bench_lib
+    if not os.path.exists(BENCH_LIB_PATH):
+        raise RuntimeError(f"{BENCH_LIB_PATH} is missing: build it with "
+                           "`python -m kv_cache_decode_06_b300.build_lib --bench`")
+    with _lock:
+        lib = ctypes.CDLL(BENCH_LIB_PATH)
+        lib.gqa_bench_stream_read.restype = ctypes.c_int
+        lib.gqa_bench_stream_read.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_int,
+                                              ctypes.c_void_p, ctypes.c_void_p]
+        _bench_lib = lib
+    return lib
+
+
+def stream_read(buf: torch.Tensor, flags: torch.Tensor, ctas: int = 0,
+                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Read ``buf`` (bf16 [z, rows, 128], rows a multiple of 128) once with the decode's
+    TMA access pattern (gqa_bench.h); ``flags`` is a zeroed int32 [1] device tensor."""
+    dev = buf.device
+    _require(buf, "buf", torch.bfloat16, dev)
+    if buf.dim() != 3 or buf.shape[2] != 128:
+        raise ValueError("buf must be [z, rows, 128]")
+    _require(flags, "flags", torch.int32, dev)
+    _check(load_bench().gqa_bench_stream_read(buf.data_ptr(), buf.shape[0], buf.shape[1], int(ctas),
+                                               flags.data_ptr(), _stream_handle(stream, dev)),
+           "gqa_bench_stream_read")
 
 
 @contextlib.contextmanager

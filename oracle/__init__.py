@@ -185,3 +185,8 @@ def group_of(i: int, H: int, G: int, lib=None) -> int:
 
 def num_threads(lib=None) -> int:
     return (lib or load()).oracle_num_threads()
+
+
+def set_num_threads(n: int, lib=None) -> None:
+    """OpenMP threads of later oracle calls (the CPU baseline times one thread and all cores)."""
+    (lib or load()).oracle_set_num_threads(int(n))

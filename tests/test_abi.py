@@ -44,6 +44,22 @@ def test_product_library_has_no_test_hook(gqa_lib):
         assert not hasattr(gqa_lib, name), name
 
 
+def test_bench_library_exports_its_header():
+    """include/gqa_bench.h is the measurement helper's header (libgqa_b300_bench.so)."""
+    from kv_cache_decode_06_b300 import build_lib
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "gqa_bench.h")).read(), flags=re.S)
+    declared = sorted(set(re.findall(r"\b(gqa_[a-z_0-9]+)\s*\(", src)))
+    assert declared == sorted(gqa.BENCH_EXPORTS)
+    build_lib.build(bench=True)
+    lib = gqa.load_bench()
+    for name in declared:
+        assert hasattr(lib, name), name
+    f = ctypes.c_uint32(0)
+    assert lib.gqa_bench_stream_read(None, 1, 128, 0, ctypes.byref(f), None) == 1   # null buffer
+    assert lib.gqa_bench_stream_read(FAKE, 1, 100, 0, ctypes.byref(f), None) == 1   # rows not a multiple of 128
+    assert lib.gqa_bench_stream_read(FAKE + 8, 1, 128, 0, ctypes.byref(f), None) == 1   # misaligned
+
+
 def test_test_hooks_library_exports_the_hook():
     from kv_cache_decode_06_b300 import build_lib
     build_lib.build(test_hooks=True)
