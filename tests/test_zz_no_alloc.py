@@ -4,18 +4,23 @@ Some callers cannot hand the library a workspace (a plugin that only gets its
 tensors from a host framework owning all device memory, a runtime that may not
 allocate after start-up, a loop that cannot pay for cudaMalloc's device
 synchronisation).  For them the library carries its own scratch array.  These
-tests call that entry point through the C ABI and check it against gqa_decode
-with a caller workspace, twice in a row, within the decode tolerance.
+tests call that entry point through the C ABI and check it against the float64
+oracle and against gqa_decode with a caller workspace, twice in a row, within
+the decode tolerance, and check that a call after one whose pipeline wait ran
+out (the test-hooks build withholds a copy) is exact without any reset by the
+caller.
 
 This file is collected last on purpose: a run that stops at the first failure
 has then already run every other test.
 """
 import ctypes
+import time
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from gpu_helpers import check_close, to_device
 from kv_cache_decode_06_b300 import gqa
 from kv_cache_decode_06_b300.inputs import CONFIGS, DecodeConfig, make_decode_inputs
@@ -49,8 +54,37 @@ def test_noalloc_matches_workspace_entry_point(cfg, gqa_lib):
     q, k, v, sl = to_device(inp)
     ref = gqa.decode(q, k, v, sl, scale=float(inp.scale)).clone()
     torch.cuda.synchronize()
+    exact = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale)
     for call in range(2):   # two calls in a row share (and must reset) the scratch
         out = torch.full((cfg.B, cfg.H, cfg.d), float("nan"), dtype=torch.float32, device="cuda")
         assert _call_noalloc(gqa_lib, q, k, v, sl, out, cfg, inp.scale) == 0
         torch.cuda.synchronize()
-        check_close(out.cpu().numpy(), ref.cpu().numpy(), what=f"noalloc call {call}")
+        got = out.cpu().numpy()
+        check_close(got, ref.cpu().numpy(), what=f"noalloc call {call} vs gqa_decode")
+        check_close(got, exact, what=f"noalloc call {call} vs the oracle")
+
+
+@pytest.mark.gpu
+def test_noalloc_recovers_after_a_timed_out_call():
+    """A call whose pipeline wait runs out (the test-hooks build withholds one K copy, so a
+    bounded wait gives up after about a second) leaves the scratch's counters where its
+    blocks stopped; the next call clears them itself and is exact, with no reset by the
+    caller (who cannot reach the scratch)."""
+    from kv_cache_decode_06_b300 import build_lib
+    build_lib.build(test_hooks=True)
+    lib = gqa.load_test_hooks()
+    cfg = CONFIGS["mistral7b"].with_(B=4)
+    inp = make_decode_inputs(cfg)
+    q, k, v, sl = to_device(inp)
+    out = torch.zeros((cfg.B, cfg.H, cfg.d), dtype=torch.float32, device="cuda")
+    with gqa.using_library(lib):
+        gqa.debug_withhold_copy(1)
+        t0 = time.time()
+        assert _call_noalloc(lib, q, k, v, sl, out, cfg, inp.scale) == 0
+        torch.cuda.synchronize()
+        assert 0.5 < time.time() - t0 < 30.0
+        out.fill_(float("nan"))
+        assert _call_noalloc(lib, q, k, v, sl, out, cfg, inp.scale) == 0
+        torch.cuda.synchronize()
+    exact = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale)
+    check_close(out.cpu().numpy(), exact, what="noalloc after a timed-out call")
