@@ -38,6 +38,7 @@ a bounded sample of the same workload per step.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import math
@@ -324,7 +325,7 @@ def config_dict(cfg, inp, extra=None):
     return d
 
 
-def time_blocks(torch, dist, run_block, stream, world, dev, repeat_seconds, local_rank):
+def time_blocks(torch, dist, run_block, stream, world, dev, repeat_seconds, local_rank, clocks=True):
     """Times R back-to-back blocks (run_block(r) enqueues block r on `stream`), each between its own
     pair of CUDA events, with nvidia-smi clock samples during them; R is chosen from a first block so
     that they take about `repeat_seconds`.  Returns (median block ms, max over ranks), the sorted
@@ -343,7 +344,7 @@ def time_blocks(torch, dist, run_block, stream, world, dev, repeat_seconds, loca
         dist.barrier()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(R)]
-    with ClockSampler(local_rank) as clk:
+    with (ClockSampler(local_rank) if clocks else contextlib.nullcontext()) as clk:
         for r, (a, b) in enumerate(evs):
             a.record(stream)
             run_block(r + 1)
@@ -353,7 +354,7 @@ def time_blocks(torch, dist, run_block, stream, world, dev, repeat_seconds, loca
         dist.barrier()
     blocks = sorted(float(a.elapsed_time(b)) for a, b in evs)
     med = max_over_ranks(statistics.median(blocks), world, dev)
-    return med, blocks, R, clk.summary()
+    return med, blocks, R, (clk.summary() if clocks else None)
 
 
 def block_stats(blocks, R, steps):
@@ -525,6 +526,55 @@ def measure_readonly(torch, dist, gqa, dev, world, local_rank, repeat_seconds):
             "bytes_per_call": nbytes, "calls": R, "clocks": clocks,
             "what": "read-only TMA stream, one CTA per SM, the decode's 64-column x 128-row boxes (two per 32 KiB "
                     "tile), six-stage ring, 2 GiB buffer; median of R calls"}
+
+
+PAGE_SWEEP = (   # (page rows, boxes per page, issuing warps, lanes per warp)
+    [(r, 2, 1, l) for r in (16, 32, 64, 128) for l in (1, 2, 4, 8, 16) if l <= 256 // r] +
+    [(r, 1, 1, l) for r in (16, 32, 64) for l in (1, 2, 4, 8) if l <= 128 // r] +
+    [(16, 2, 2, 16), (16, 1, 2, 1), (16, 1, 2, 8)])
+
+
+def measure_page_boxes(torch, dist, gqa, dev, world, local_rank, repeat_seconds):
+    """The per-box cost of small pages: GB/s of the read-only stream when every 32 KiB tile is
+    fetched as pages of 16..128 rows at scattered places of a 2 GiB pool, two boxes per page (the
+    whole-tile layout) or one (a five-dimensional tensor map), issued by L lanes of one or two warps
+    per SM (gqa_bench_stream_read_pages); median of R calls each."""
+    z, rows = READONLY_SHAPE
+    buf = torch.empty((z, rows, 128), dtype=torch.bfloat16, device=dev)
+    buf.view(torch.int16).fill_(0x3F80)
+    flags = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    nbytes = buf.numel() * 2
+    table = []
+    for pr, per_page, warps, lanes in PAGE_SWEEP:
+        def run_block(r, pr=pr, lanes=lanes, one=per_page == 1, warps=warps):
+            gqa.stream_read_pages(buf, flags, pr, lanes, scatter=True, one_box=one, warps=warps, stream=stream)
+
+        try:
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    run_block(0)
+        except gqa.GQAError as e:   # the driver may refuse a map: report it, run the rest
+            table.append({"page_rows": pr, "boxes_per_page": per_page, "warps": warps, "lanes": lanes,
+                          "error": str(e)})
+            continue
+        torch.cuda.synchronize()
+        med_ms, blocks, R, _ = time_blocks(torch, dist, run_block, stream, world, dev, repeat_seconds,
+                                           local_rank, clocks=False)
+        gbs = nbytes / (med_ms / 1e3) / 1e9
+        boxes = (128 // pr) * per_page
+        table.append({"page_rows": pr, "boxes_per_page": per_page, "warps": warps, "lanes": lanes,
+                      "gbs": round(gbs, 1), "ns_per_box_per_sm": round(32768 / boxes / (gbs / 148), 2)})
+    torch.cuda.synchronize()
+    if int(flags.item()) != 0:
+        raise RuntimeError(f"paged read-only stream reported flags 0x{int(flags.item()):x}")
+    del buf
+    return {"unit": UNIT, "bytes_per_call": nbytes,
+            "what": "read-only TMA stream over a 2 GiB pool read as pages of R rows (R x 256 bytes) at scattered "
+                    "places, a 32 KiB tile = 128/R pages, two 64-column boxes per page or one five-dimensional box, "
+                    "issued by L lanes of W warps per SM (W warps take alternate tiles); GB/s and the time per box "
+                    "per SM it implies (median of R calls)",
+            "sweep": table}
 
 
 def decode_case(args, cfg, variant, torch, gqa, dev):
@@ -701,6 +751,7 @@ def cpu_baseline_decode(inp, window):
 def run_readonly(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
     """--variant readonly: the read-only stream's own line."""
     ro = measure_readonly(torch, dist, gqa, dev, world, local_rank, args.repeat_seconds)
+    pages = measure_page_boxes(torch, dist, gqa, dev, world, local_rank, min(args.repeat_seconds, 0.15))
     if rank != 0:
         return
     peak, peak_kind = measured_peak()
@@ -712,7 +763,7 @@ def run_readonly(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
             "roofline": {"bound": "hbm", "achieved": ro["value"], "peak": peak, "unit": "GB/s",
                          "frac": ro["value"] / peak, "traffic": None, "kernel": "stream_read_kernel",
                          "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind}, a copy)"},
-            "best": ro["best"], "gpu_launches": ro["calls"], "clocks": ro["clocks"]}
+            "best": ro["best"], "gpu_launches": ro["calls"], "clocks": ro["clocks"], "page_boxes": pages}
     print(json.dumps(line), flush=True)
 
 

@@ -32,6 +32,30 @@ extern "C" {
 int gqa_bench_stream_read(const void *buf, long long z, long long rows, int ctas, unsigned int *flags,
                           void *stream);
 
+/*
+ * The same read with every 32 KiB tile fetched as pages, as the decode kernel
+ * fetches a paged cache whose pages are smaller than its 128-position tile: the
+ * per-box cost of small pages.
+ *   page_rows  16, 32, 64 or 128: each tile is 128/page_rows pages, two boxes of
+ *              64 columns x page_rows rows each
+ *   lanes      1..32: lanes of the issuing warp that issue a tile's boxes (lane l
+ *              issues boxes l, l + lanes, ...)
+ *   scatter    nonzero: page q of the stream is read from page slot q * A mod
+ *              npages (A odd, npages = z * rows / page_rows, which must then be a
+ *              power of two), so consecutive pages sit far apart as in a pool;
+ *              zero: in order
+ *   one_box    zero: two boxes per page (64 columns x page_rows rows each);
+ *              nonzero: one box per page, through a five-dimensional tensor map
+ *              (64 columns, 8 rows, 2 column halves, page_rows / 8 row groups,
+ *              pages) that lands the page as [row group][half][8 rows][128 bytes]
+ *   warps      1 or 2: issuing warps, taking alternate tiles
+ * Other arguments as for gqa_bench_stream_read; returns 0, 1 (invalid argument),
+ * 4 (launch failed or the three-dimensional map refused), 5 (no usable device) or
+ * 6 (the driver refused the five-dimensional map).
+ */
+int gqa_bench_stream_read_pages(const void *buf, long long z, long long rows, int page_rows, int lanes, int scatter,
+                                int one_box, int warps, int ctas, unsigned int *flags, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -166,16 +166,33 @@ constexpr int kMinPage = 16;
 constexpr int kMaxPage = 1 << 20;
 constexpr long long kMaxPoolRows = 1ll << 31;
 
-// Page pool viewed as a 3-D tensor [num_pages*G][page_size][d] (paired:
-// [num_pages*G][page_size/2][2d]), boxes of 64 columns x min(rows per page,
-// 128) rows x 1, 128-byte swizzle.  A page smaller than a tile is one box.
+// Page pool viewed as [num_pages*G][rows][cols] with rows = page_size, cols = d
+// (paired: rows = page_size/2, cols = 2d), 128-byte swizzle, one box = one page
+// (or the 128 rows of a tile, for pages longer than a tile).
+// cols = 128 (d = 128, or the paired layout): a five-dimensional view (64
+// columns, 8 rows, 2 column halves, rows/8 row groups, pages) whose box lands
+// the page in shared memory as [row group][half][8 rows][128 B], the layout the
+// paged kernel instances read.  Its strides are not increasing (the halves are
+// 128 bytes apart, the rows 256): the view only reorders the page's bytes.
+// cols = 64: [pages][rows][64] with boxes of 64 columns x min(rows, 128) rows.
 bool make_page_map(CUtensorMap *map, const void *base, int num_pages, int G, int d, int page_size, bool paired) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const int cols = paired ? 2 * d : d, rows = paired ? page_size / 2 : page_size;
+    const int box_rows = rows < gqa::kTile ? rows : gqa::kTile;
+    if (cols == 2 * gqa::kBoxCols) {
+        const cuuint64_t dims[5] = {(cuuint64_t)gqa::kBoxCols, 8, 2, (cuuint64_t)rows / 8, (cuuint64_t)num_pages * G};
+        const cuuint64_t strides[4] = {(cuuint64_t)cols * 2, (cuuint64_t)gqa::kBoxCols * 2, (cuuint64_t)cols * 2 * 8,
+                                       (cuuint64_t)page_size * d * 2};
+        const cuuint32_t box[5] = {(cuuint32_t)gqa::kBoxCols, 8, 2, (cuuint32_t)box_rows / 8, 1};
+        const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+        return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
     const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)num_pages * G};
     const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)page_size * d * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)gqa::kBoxCols, (cuuint32_t)(rows < gqa::kTile ? rows : gqa::kTile), 1};
+    const cuuint32_t box[3] = {(cuuint32_t)gqa::kBoxCols, (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -18,7 +18,9 @@
 // Warp roles (224 threads): warp 0 = TMA producer (Q, K, V; hands the work
 // ranges to the others), warp 1 = score-GEMM issuer and TMEM owner, warp 6 =
 // value-GEMM issuer, warps 2-5 = softmax + epilogue (thread <-> TMEM lane).
-// Paged-cache instances add warp 7 (256 threads): block-table ids and the V copies.
+// Paged-cache instances (256 threads) add warp 7, which loads the block-table
+// entries and copies K and V; the producer thread then issues only Q and hands
+// out the work ranges.
 //
 // Producer and MMA issuers are event loops: each issues the next operation
 // whose inputs are ready.  K slot s is handed back as soon as the score GEMM of
@@ -153,6 +155,18 @@ struct TcCfg {
     static constexpr int kTileShift = kPair ? 8 : 7;                 // log2(positions per tile)
     static constexpr int kTilePos = 1 << kTileShift;
     static constexpr int kTileBytes = kColBoxes * kBoxBytes;         // one K or V tile
+    // K/V tile layout in shared memory: tensor-map row r, column box c at
+    // c * kHalfStride + (r / 8) * kGroupStride + (r % 8) * 128, 128-byte swizzled
+    // within each 8-row group.  Whole-tile layout: the column boxes one after the
+    // other (16 KB apart), the 8-row groups dense.  Paged instances with two
+    // column boxes interleave them per 8-row group ([group][box][8 rows][128 B]):
+    // a page of the pool is then one TMA box (a five-dimensional tensor map) that
+    // lands as whole groups, whatever the page size, and the tensor cores read the
+    // same tile through descriptors with these strides.
+    static constexpr bool kInter = kPaged && kColBoxes == 2;
+    static constexpr int kHalfStride = kInter ? 1024 : kBoxBytes;
+    static constexpr int kGroupStride = kInter ? 2048 : 1024;
+    static __device__ __forceinline__ int row_off(int r) { return (r >> 3) * kGroupStride + (r & 7) * 128; }
     // heads on M (64 query heads per group at d = 64), see below: Q is stored twice, as
     // the 128 rows of the score GEMM's A operand
     static constexpr bool kHM = (D == 64 && NH == 64 && !kPair);
@@ -179,11 +193,12 @@ struct TcCfg {
     static constexpr int kStageRow = kExt ? kRowBytes : 0;
     static constexpr int kStageInfo = kExt ? (int)sizeof(PatchInfo) : 0;
     static constexpr int kSlotCost = kTileBytes + kStageRow + kStageInfo;
-    // page-id ring (variant instances, paged cache): kIdRing entries of kIdStride
-    // ints, the page ids of one tile's boxes followed by the sequence length T_b,
-    // written by the page-id warp ahead of the producer
+    // page-id ring (paged cache): kIdRing entries of kIdStride ints, the page ids of
+    // one tile's pages followed by T_b, written by the page-id warp; an entry
+    // completes once the warp has issued the tile's K copy, and is free again once
+    // the producer thread has taken it
     static constexpr int kIdRing = 8;
-    static constexpr int kIdMax = kTilePos / 16;        // boxes per tile at the smallest page (16 positions)
+    static constexpr int kIdMax = kTilePos / 16;        // pages per tile at the smallest page (16 positions)
     static constexpr int kIdStride = kIdMax + 4;        // ids, T_b, padding to 16 bytes
     static constexpr int kIdBytes = kPaged ? kIdRing * kIdStride * 4 : 0;
     static constexpr int kIdBars = kPaged ? 2 * kIdRing : 0;
@@ -227,7 +242,8 @@ struct TcCfg {
     static_assert(kSmemBytes <= kSmemLimit, "shared memory layout too large");
     static_assert(NH < 4 || (kOffRed % 16 == 0 && kOffLred % 16 == 0 && kOffM % 16 == 0 && kOffA % 16 == 0),
                   "float4 alignment");
-    // warps: producer, score MMA, 4 softmax, value MMA, and (variant instances) the page-id warp
+    // warps: producer, score MMA, 4 softmax, value MMA, and (paged instances) the
+    // page-id warp, which copies K and V
     static constexpr int kThreads = kPaged ? 256 : 224;
     // TMEM: S accumulators [2][part][N] then O accumulators [3][kOW] (O is folded two tiles behind)
     // Heads on M (64 query heads per group at d = 64): the score GEMM is S = [Q; Q]·K^T
@@ -422,10 +438,14 @@ __device__ __noinline__ void produce_tile(const DecodeParams &p, const CUtensorM
             tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, pos0 >> kPairShift, seg, bar, pol);
     } else if (ps >= C::kTilePos) {
         const int z = checked_page(p, ids[0]) * p.G + c.g;
+        const int y = (pos0 & (ps - 1)) >> kPairShift;
         mbar_arrive_expect_tx(bar, bytes + C::kTileBytes);
+        if constexpr (C::kInter) {
+            tma_load_5d(dst, tm, 0, 0, 0, y >> 3, z, bar, pol);
+        } else {
 #pragma unroll
-        for (int cb = 0; cb < C::kColBoxes; ++cb)
-            tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, (pos0 & (ps - 1)) >> kPairShift, z, bar, pol);
+            for (int cb = 0; cb < C::kColBoxes; ++cb) tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, y, z, bar, pol);
+        }
     } else {
         const int prow = ps >> kPairShift;   // tensor-map rows per page
         // compact loops: this code runs from the instruction cache beside the
@@ -441,9 +461,13 @@ __device__ __noinline__ void produce_tile(const DecodeParams &p, const CUtensorM
             const int id = ids[k];
             if (id != -1) {
                 const int z = checked_page(p, id) * p.G + c.g;
+                if constexpr (C::kInter) {
+                    tma_load_5d(dst + C::row_off(k * prow), tm, 0, 0, 0, 0, z, bar, pol);
+                } else {
 #pragma unroll
-                for (int cb = 0; cb < C::kColBoxes; ++cb)
-                    tma_load_3d(dst + cb * kBoxBytes + k * prow * 128, tm, cb * kBoxCols, 0, z, bar, pol);
+                    for (int cb = 0; cb < C::kColBoxes; ++cb)
+                        tma_load_3d(dst + cb * kBoxBytes + k * prow * 128, tm, cb * kBoxCols, 0, z, bar, pol);
+                }
             }
         }
     }
@@ -496,52 +520,68 @@ __device__ __forceinline__ int plain_tile_rows(const Cursor &c, const int *tlen)
     return (rows + 15) & ~15;
 }
 
-// Producer, variant instances: tiles without an appended row stay on a short
-// inline path (contiguous: the plain copy at the window's offset; paged: one box
-// per column box from the page holding the tile, or one per page of the tile);
-// the tile holding an appended row goes to produce_tile, out of line.  Short hot code matters here: the long general
-// path costs several hundred nanoseconds per call in instruction fetches.
+// Producer, contiguous-cache variant instances: tiles without an appended row stay
+// on a short inline path (the plain copy at the window's offset); the tile holding
+// an appended row goes to produce_tile, out of line.  Short hot code matters here:
+// the long general path costs several hundred nanoseconds per call in instruction
+// fetches.
 template <class C>
 __device__ __forceinline__ void produce_variant_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst,
                                                      uint64_t *bar, const Cursor &c, int T, uint64_t pol,
                                                      const __nv_bfloat16 *row_new, uint8_t *stage_row,
-                                                     PatchInfo *info, __nv_bfloat16 *row_dst, const int *ids) {
-    const bool app = row_new != nullptr && c.j + 1 == c.tiles;
-    if (!app) {
+                                                     PatchInfo *info, __nv_bfloat16 *row_dst) {
+    static_assert(!C::kPaged, "the page-id warp copies the tiles of a paged cache");
+    if (row_new == nullptr || c.j + 1 != c.tiles) {
         if (row_new) info->on = 0;
-        if constexpr (!C::kPaged) {
-            produce_plain_tile<C>(p, tm, dst, bar, c, pol, window_start(p, T) >> C::kTileShift);
-            return;
-        }
-        constexpr int kPairShift = C::kParts - 1;
-        const int ps = 1 << p.page_shift;
-        if (C::kTilePos <= ps) {
-            const int pos0 = tile_first_pos<C>(p, T, c.j);
-            const int z = checked_page(p, ids[0]) * p.G + c.g;
-            mbar_arrive_expect_tx(bar, C::kTileBytes);
-#pragma unroll
-            for (int cb = 0; cb < C::kColBoxes; ++cb)
-                tma_load_3d(dst + cb * kBoxBytes, tm, cb * kBoxCols, (pos0 & (ps - 1)) >> kPairShift, z, bar, pol);
-        } else {
-            const int prow = ps >> kPairShift, nb = C::kTilePos / ps;
-            int loads = 0;
-#pragma unroll 1
-            for (int k = 0; k < nb; ++k) loads += ids[k] != -1;
-            mbar_arrive_expect_tx(bar, (uint32_t)(loads * prow * 128 * C::kColBoxes));
-#pragma unroll 1
-            for (int k = 0; k < nb; ++k) {
-                const int id = ids[k];
-                if (id != -1) {
-                    const int z = checked_page(p, id) * p.G + c.g;
-#pragma unroll
-                    for (int cb = 0; cb < C::kColBoxes; ++cb)
-                        tma_load_3d(dst + cb * kBoxBytes + k * prow * 128, tm, cb * kBoxCols, 0, z, bar, pol);
-                }
-            }
-        }
+        produce_plain_tile<C>(p, tm, dst, bar, c, pol, window_start(p, T) >> C::kTileShift);
         return;
     }
-    produce_tile<C>(p, tm, dst, bar, c, T, pol, row_new, stage_row, info, row_dst, ids);
+    produce_tile<C>(p, tm, dst, bar, c, T, pol, row_new, stage_row, info, row_dst, nullptr);
+}
+
+// Page-id warp, paged cache: copies the K or V tile at cursor c with the whole warp.
+// Lane k holds the page id of the tile's page k (`id`; -1 for a page without an
+// attended position, whose rows are masked) and `ids` the same ids in shared
+// memory.  Each lane issues one box: page lane / kColBoxes, column box lane %
+// kColBoxes (at most 16 pages of 16 positions x 2 column boxes per tile), so the
+// copy of a tile of small pages costs one issue slot instead of one per box; a
+// box's issue cost in a single thread, not the copy engine, bounds small pages.
+// Lane 0 sets the byte count before any lane issues.  The tile holding an
+// appended row goes to produce_tile on lane 0.
+template <class C>
+__device__ __forceinline__ void produce_paged_tile(const DecodeParams &p, const CUtensorMap *tm, uint8_t *dst,
+                                                   uint64_t *bar, const Cursor &c, int T, uint64_t pol, int id,
+                                                   int lane, const __nv_bfloat16 *row_new, uint8_t *stage_row,
+                                                   PatchInfo *info, __nv_bfloat16 *row_dst, const int *ids) {
+    static_assert(C::kIdMax * C::kColBoxes <= 32, "one box per lane");
+    constexpr int kPairShift = C::kParts - 1;
+    if (row_new != nullptr && c.j + 1 == c.tiles) {
+        if (lane == 0) produce_tile<C>(p, tm, dst, bar, c, T, pol, row_new, stage_row, info, row_dst, ids);
+        __syncwarp();
+        return;
+    }
+    const int ps = 1 << p.page_shift;
+    const bool whole = ps >= C::kTilePos;                   // one page holds the tile
+    const int nb = whole ? 1 : C::kTilePos / ps;            // pages of the tile
+    const int rows = whole ? kTile : ps >> kPairShift;      // tensor-map rows per box
+    const unsigned loads = __ballot_sync(0xffffffffu, lane < nb && id != -1);
+    if (lane == 0) {
+        if (row_new) info->on = 0;   // before the arrival that publishes it
+        mbar_arrive_expect_tx(bar, (uint32_t)(__popc(loads) * rows * 128 * C::kColBoxes));
+    }
+    __syncwarp();
+    const int y = whole ? (tile_first_pos<C>(p, T, c.j) & (ps - 1)) >> kPairShift : 0;
+    if constexpr (C::kInter) {
+        // one box per page: lane k copies page k, both column boxes, as whole 8-row groups
+        if ((loads >> lane) & 1u)
+            tma_load_5d(dst + C::row_off(lane * rows), tm, 0, 0, 0, y >> 3, checked_page(p, id) * p.G + c.g, bar, pol);
+    } else {
+        const int k = lane / C::kColBoxes, cb = lane % C::kColBoxes;
+        const int my_id = __shfl_sync(0xffffffffu, id, k < C::kIdMax ? k : 0);
+        if (k < nb && ((loads >> k) & 1u))
+            tma_load_3d(dst + cb * kBoxBytes + k * rows * 128, tm, cb * kBoxCols, y,
+                        checked_page(p, my_id) * p.G + c.g, bar, pol);
+    }
 }
 
 // MMA issuer: writes a slot's staged row (the appended token) into its tile,
@@ -557,7 +597,7 @@ __device__ __noinline__ void patch_tile(uint8_t *tile, const uint8_t *stage_row,
         const uint4 v = *reinterpret_cast<const uint4 *>(stage_row + q * 16);
         const int cb = kPairL ? (rel & 1) : (q >> 3);   // column box: the position's half, or dims 64q'..
         const int qq = q & 7;                           // 16-byte chunk inside the 128-byte row
-        *reinterpret_cast<uint4 *>(tile + cb * kBoxBytes + r * 128 + ((qq ^ (r & 7)) << 4)) = v;
+        *reinterpret_cast<uint4 *>(tile + cb * C::kHalfStride + C::row_off(r) + ((qq ^ (r & 7)) << 4)) = v;
         if (info.dst) reinterpret_cast<uint4 *>(info.dst)[q] = v;
     }
     fence_proxy_async_smem();
@@ -634,8 +674,8 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
         mbar_init(prebar, 32);   // the producer warp, once the tile prefix is in shared memory
         if constexpr (kPaged) {
             for (int s = 0; s < C::kIdRing; ++s) {
-                mbar_init(&idfull[s], 32);    // every lane of the page-id warp
-                mbar_init(&idempty[s], 1);    // the producer, once V of the tile is issued
+                mbar_init(&idfull[s], 1);     // the page-id warp, once K of the tile is issued
+                mbar_init(&idempty[s], 1);    // the producer thread, once it has taken the tile
             }
         }
         *s_abort = 0;
@@ -755,9 +795,11 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                     const int st = i % SK, qb = piece % QB;
                     // K runs at most one tile ahead of V: a tile's V then lands about when its
                     // probabilities are ready, and a piece's last value GEMM does not wait long
+                    // (paged instances: the page-id warp has copied K of the tile once idfull
+                    // completes; this thread then only issues Q and paces the range claims)
                     if ((kPaged || vissued >= i) &&
                         (!first || piece < QB || mbar_test_wait(&qempty[qb], ((piece / QB) - 1) & 1)) &&
-                        (i < SK || mbar_test_wait(&kempty[st], ((i / SK) - 1) & 1)) &&
+                        (kPaged || i < SK || mbar_test_wait(&kempty[st], ((i / SK) - 1) & 1)) &&
                         (!kPaged || mbar_test_wait(&idfull[i % C::kIdRing], (i / C::kIdRing) & 1))) {
                         if (first) {
                             if (i == 0) GQA_TRACE_AT(kTrPreQ, clock64());
@@ -773,7 +815,10 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                             if (i == 0) GQA_TRACE_AT(kTrFirstQ, clock64());
                         }
                         uint8_t *kdst = smem + C::kOffK + st * C::kTileBytes;
-                        if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i, clock64());
+                        if (!kPaged && i < 20) GQA_TRACE_AT(kTrProbe + 4 * i, clock64());
+                        if constexpr (kPaged) {
+                            mbar_arrive(&idempty[i % C::kIdRing]);   // the ring entry may be reused
+                        } else
 #ifdef GQA_TEST_HOOKS
                         if (i == p.withhold_k && blockIdx.x == 0) {
                             // test hook: this copy is never made, so the score GEMM's bounded
@@ -781,10 +826,8 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         } else
 #endif
                         if constexpr (kExt) {
-                            const int *ids = kPaged ? ids_ring + (i % C::kIdRing) * C::kIdStride : nullptr;
-                            const int T = kPaged ? ids[C::kIdMax] : k_lens.get(p, kc.b);
-                            produce_variant_tile<C>(p, &tm_k, kdst, &kfull[st], kc, T, pol_kv, p.k_new,
-                                                    kstage + st * C::kRowBytes, &kinfo[st], p.k_dst, ids);
+                            produce_variant_tile<C>(p, &tm_k, kdst, &kfull[st], kc, k_lens.get(p, kc.b), pol_kv,
+                                                    p.k_new, kstage + st * C::kRowBytes, &kinfo[st], p.k_dst);
                         } else {
                             const int rows = plain_tile_rows<C>(kc, tlen);
                             if (rows == kTile)
@@ -792,10 +835,9 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                             else
                                 produce_tail_tile<C>(p, tails.k, kdst, &kfull[st], kc, pol_kv, rows);
                         }
-                        if constexpr (kPaged) mbar_arrive(&idempty[i % C::kIdRing]);   // the ids are no longer read here
-                        if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i + 1, clock64());
+                        if (!kPaged && i < 20) GQA_TRACE_AT(kTrProbe + 4 * i + 1, clock64());
                         if (i == 0) GQA_TRACE_AT(kTrFirstK, clock64());
-                        if (i < 128) GQA_TRACE_AT(kTrKIssue + i, clock64());
+                        if (!kPaged && i < 128) GQA_TRACE_AT(kTrKIssue + i, clock64());
                         ++kissued;
                         ++k_u;
                         if (last) ++piece;
@@ -821,11 +863,11 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                     if (i < SV || mbar_test_wait(&vempty[st], ((i / SV) - 1) & 1)) {
                         uint8_t *vdst = smem + C::kOffV + st * C::kTileBytes;
                         if (i < 20) GQA_TRACE_AT(kTrProbe + 4 * i + 2, clock64());
-                        if constexpr (kExt) {
-                            const int *ids = kPaged ? ids_ring + (i % C::kIdRing) * C::kIdStride : nullptr;
-                            const int T = kPaged ? ids[C::kIdMax] : v_lens.get(p, vc.b);
-                            produce_variant_tile<C>(p, &tm_v, vdst, &vfull[st], vc, T, pol_kv, p.v_new,
-                                                    vstage + st * C::kRowBytes, &vinfo[st], p.v_dst, ids);
+                        if constexpr (kPaged) {
+                            // never reached: the page-id warp copies V
+                        } else if constexpr (kExt) {
+                            produce_variant_tile<C>(p, &tm_v, vdst, &vfull[st], vc, v_lens.get(p, vc.b), pol_kv,
+                                                    p.v_new, vstage + st * C::kRowBytes, &vinfo[st], p.v_dst);
                         } else {
                             const int rows = plain_tile_rows<C>(vc, tlen);
                             if (rows == kTile)
@@ -908,7 +950,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         const uint32_t qbase = sbase + C::kOffQ + qb * C::kQBytes;
                         // part c (paired layout: the box of even / odd positions) -> S columns [bi][c];
                         // base descriptors once, then constant offsets (K step = 32 bytes in a box)
-                        const uint64_t kd0 = sdesc_sw128(kb, 16, 1024), qd0 = sdesc_sw128(qbase, 16, 1024);
+                        const uint64_t kd0 = sdesc_sw128(kb, 16, C::kGroupStride), qd0 = sdesc_sw128(qbase, 16, 1024);
                         if constexpr (C::kHM) {
                             // S [2 x 64 heads x 128 positions] = [Q; Q]·K^T: Q is the A operand (d = 64: one K atom)
                             constexpr uint32_t idS_hm = idesc_bf16_f32(128, kTile, false, false);
@@ -922,7 +964,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
 #pragma unroll
                                 for (int kk = 0; kk < D / 16; ++kk)
                                     umma_bf16(tmem + (bi * NP + c) * N,
-                                              sdesc_add(kd0, (kPair ? c : (kk >> 2)) * kBoxBytes + (kk & 3) * 32),
+                                              sdesc_add(kd0, (kPair ? c : (kk >> 2)) * C::kHalfStride + (kk & 3) * 32),
                                               sdesc_add(qd0, (kk >> 2) * (N * 128) + (kk & 3) * 32), idS, kk != 0);
                         }
                         umma_commit(&sfull[bi]);
@@ -955,8 +997,9 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                             patch_tile<C>(smem + C::kOffV + st * C::kTileBytes, vstage + st * C::kRowBytes, vinfo[st]);
                         const uint32_t vb = sbase + C::kOffV + st * C::kTileBytes;
                         const uint32_t d_o = tmem + C::kOCol + ob * C::kOBuf;
-                        // A = V^T, MN-major: the column boxes are the M atoms (LBO), 16 positions = 2 KB
-                        const uint64_t vd0 = sdesc_sw128(vb, kBoxBytes, 1024);
+                        // A = V^T, MN-major: the column boxes are the M atoms (LBO), the 8-row groups
+                        // the K steps (SBO); 16 positions = two groups
+                        const uint64_t vd0 = sdesc_sw128(vb, C::kHalfStride, C::kGroupStride);
                         const uint64_t pd0 = sdesc_sw128(sbase + C::kOffP + pbi * C::kPBufBytes, 16, 1024);
                         if constexpr (C::kHM) {
                             // O [64 heads x d] = P_hi·V + P_lo·V: P is the A operand (K-major, two
@@ -971,7 +1014,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                         } else {
 #pragma unroll
                             for (int kk = 0; kk < kTile / 16; ++kk)
-                                umma_bf16(d_o, sdesc_add(vd0, kk * 2048),
+                                umma_bf16(d_o, sdesc_add(vd0, kk * 2 * C::kGroupStride),
                                           sdesc_add(pd0, (kk >> 2) * (C::kOW * 128) + (kk & 3) * 32), idPV, kk != 0);
                         }
                         umma_commit(&ofull[ob]);
@@ -1136,7 +1179,7 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
                 const int sv = i % SV;
                 if (!mbar_wait(&vfull[sv], (i / SV) & 1, ab)) { ok = false; break; }
                 if (!(tg < hi_pos && tg >= lo_pos)) {
-                    uint4 *w = reinterpret_cast<uint4 *>(smem + C::kOffV + sv * C::kTileBytes + tg * 128);
+                    uint4 *w = reinterpret_cast<uint4 *>(smem + C::kOffV + sv * C::kTileBytes + C::row_off(tg));
 #pragma unroll
                     for (int q = 0; q < 8; ++q) w[q] = make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -1328,13 +1371,13 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
             if (valid_cnt < C::kTilePos || lo > 0) {
                 const int sv = i % SV;
                 if (!mbar_wait(&vfull[sv], (i / SV) & 1, ab)) { ok = false; break; }
-                uint8_t *vrow = smem + C::kOffV + sv * C::kTileBytes + r * 128;
+                uint8_t *vrow = smem + C::kOffV + sv * C::kTileBytes + C::row_off(r);
 #pragma unroll
                 for (int c = 0; c < C::kColBoxes; ++c) {
                     // paired layout: box c holds the positions of part c; otherwise a row's
                     // boxes hold the dims of one position (part 0)
                     if (!valid[kPair ? c : 0]) {
-                        uint4 *w = reinterpret_cast<uint4 *>(vrow + c * kBoxBytes);
+                        uint4 *w = reinterpret_cast<uint4 *>(vrow + c * C::kHalfStride);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) w[k] = make_uint4(0u, 0u, 0u, 0u);
                     }
@@ -1450,13 +1493,13 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
             if (valid_cnt < C::kTilePos || lo > 0) {
                 const int sv = i % SV;
                 if (!mbar_wait(&vfull[sv], (i / SV) & 1, ab)) { ok = false; break; }
-                uint8_t *vrow = smem + C::kOffV + sv * C::kTileBytes + r * 128;
+                uint8_t *vrow = smem + C::kOffV + sv * C::kTileBytes + C::row_off(r);
 #pragma unroll
                 for (int c = 0; c < C::kColBoxes; ++c) {
                     // paired layout: box c holds the positions of part c; otherwise a row's
                     // boxes hold the dims of one position (part 0)
                     if (!valid[kPair ? c : 0]) {
-                        uint4 *w = reinterpret_cast<uint4 *>(vrow + c * kBoxBytes);
+                        uint4 *w = reinterpret_cast<uint4 *>(vrow + c * C::kHalfStride);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) w[k] = make_uint4(0u, 0u, 0u, 0u);
                     }
@@ -1537,13 +1580,19 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
         }
     } else if (kPaged) {
         // ================================================================ page-id warp (paged cache)
-        // Walks the same tiles as the producer, up to kIdRing tiles ahead, and puts
-        // each tile's page ids (lane k: box k) and T_b into the ring.  The block-table
-        // loads thus never sit in the producer's thread, whose barrier arrivals
-        // would otherwise wait for them.
-        int rr = 0, ti = 0, cached_b = -1, T = 0, v_copies = 0;
+        // Walks the same tiles as the producer: lane k loads the block-table entry of
+        // the tile's page k, then the warp copies the tile's K and then its V
+        // (produce_paged_tile: one box per page, one page per lane).  Its id-ring
+        // entry completes once K is issued; the producer thread paces its range
+        // claims and Q copies on it and frees it (the ids and T_b are written into
+        // it only for the appended-row path, which reads them).  One warp issues
+        // both copies in order, K(i) V(i) K(i+1): K never runs ahead of V, which
+        // measured faster than a second warp copying V beside this one.
+        int rr = 0, ti = 0, k_copies = 0, v_copies = 0;
         bool ok = true;
-        const uint64_t pol_v = l2_policy_evict_first();
+        const uint64_t pol_kv = l2_policy_evict_first();
+        const int *tlen = seq_len_array(prefix, p.B);   // T_b per sequence, when the batch leaves room
+        const int ps = 1 << p.page_shift;
         while (ok) {
             const int rslot = rr % kRing;
             if (!mbar_wait(&rfull[rslot], (rr / kRing) & 1, ab)) break;
@@ -1553,52 +1602,64 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
             ++rr;
             if (range.chunk == -2) break;
             Cursor cur = cursor_at(range.ub, prefix, p.B, G);
-            const int ps = 1 << p.page_shift;
+            int cached_b = -1, T = 0;
             for (int k = 0; k < range.len; ++k, ++ti) {
-                const int slot = ti % C::kIdRing;
-                if (ti >= C::kIdRing && !mbar_wait(&idempty[slot], ((ti / C::kIdRing) - 1) & 1, ab)) {
-                    ok = false;
-                    break;
-                }
+                const int slot = ti % C::kIdRing, sk = ti % SK, sv = ti % SV;
                 if (cur.b != cached_b) {
                     cached_b = cur.b;
-                    T = seq_len_of(p, cur.b);
+                    T = tlen ? tlen[cur.b] : seq_len_of(p, cur.b);
                 }
+                // the block-table entries first: their latency overlaps the waits below
                 const int t0 = window_start(p, T), pos0 = tile_first_pos<C>(p, T, cur.j);
                 const int32_t *trow = p.block_table + (size_t)cur.b * p.max_pages;
-                int *e = ids_ring + slot * C::kIdStride;
+                int id = -1;
                 if (lane < C::kIdMax) {
-                    int id = -1;
                     if (ps >= C::kTilePos) {
                         if (lane == 0) id = __ldg(trow + (pos0 >> p.page_shift));
                     } else {
                         const int pos = pos0 + lane * ps;
                         if (pos < pos0 + C::kTilePos && pos < T && pos + ps > t0) id = __ldg(trow + (pos >> p.page_shift));
                     }
-                    e[lane] = id;
                 }
-                if (lane == 0) e[C::kIdMax] = T;
-                mbar_arrive(&idfull[slot]);   // every lane: its own writes are released
-                __syncwarp();
-                // ---- the V copy of this tile (the producer thread copies K): a second
-                // issuing thread halves the serial copy time when pages are small
-                if (lane == 0) {
-                    const int sv = ti % SV;
-                    if (ti >= SV && !mbar_wait(&vempty[sv], ((ti / SV) - 1) & 1, ab)) {
-                        ok = false;
-                    } else {
-                        produce_variant_tile<C>(p, &tm_v, smem + C::kOffV + sv * C::kTileBytes, &vfull[sv], cur, T,
-                                                pol_v, p.v_new, vstage + sv * C::kRowBytes, &vinfo[sv], p.v_dst, e);
-                        ++v_copies;
-                    }
+                bool go = true;
+                if (lane == 0 && ti < 20) GQA_TRACE_AT(kTrProbe + 4 * ti, clock64());
+                if (lane == 0)
+                    go = (ti < C::kIdRing || mbar_wait(&idempty[slot], ((ti / C::kIdRing) - 1) & 1, ab)) &&
+                         (ti < SK || mbar_wait(&kempty[sk], ((ti / SK) - 1) & 1, ab));
+                if (lane == 0 && ti < 20) GQA_TRACE_AT(kTrProbe + 4 * ti + 1, clock64());
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
+                int *e = ids_ring + slot * C::kIdStride;
+                if (p.k_new) {   // the ids in shared memory, for the appended-row path
+                    if (lane < C::kIdMax) e[lane] = id;
+                    if (lane == 0) e[C::kIdMax] = T;
+                    __syncwarp();
+                }
+                produce_paged_tile<C>(p, &tm_k, smem + C::kOffK + sk * C::kTileBytes, &kfull[sk], cur, T, pol_kv, id,
+                                      lane, p.k_new, kstage + sk * C::kRowBytes, &kinfo[sk], p.k_dst, e);
+                ++k_copies;
+                if (lane == 0 && ti < 128) GQA_TRACE_AT(kTrKIssue + ti, clock64());
+                if (lane == 0) mbar_arrive(&idfull[slot]);   // K of the tile is issued
+                // ---- V of the tile
+                if (lane == 0) go = ti < SV || mbar_wait(&vempty[sv], ((ti / SV) - 1) & 1, ab);
+                if (lane == 0 && ti < 20) GQA_TRACE_AT(kTrProbe + 4 * ti + 2, clock64());
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
+                }
+                produce_paged_tile<C>(p, &tm_v, smem + C::kOffV + sv * C::kTileBytes, &vfull[sv], cur, T, pol_kv, id,
+                                      lane, p.v_new, vstage + sv * C::kRowBytes, &vinfo[sv], p.v_dst, e);
+                ++v_copies;
+                if (lane == 0 && ti < 128) GQA_TRACE_AT(kTrVIssue + ti, clock64());
                 cursor_next(cur, prefix, p.B, G);
             }
         }
         if (lane == 0 && *s_abort) {
-            // let this warp's V copies in flight land before the CTA's shared memory is released
+            // let this warp's copies in flight land before the CTA's shared memory is released
+            for (int k = k_copies > SK ? k_copies - SK : 0; k < k_copies; ++k)
+                mbar_wait_teardown(&kfull[k % SK], (k / SK) & 1);
             for (int k = v_copies > SV ? v_copies - SV : 0; k < v_copies; ++k)
                 mbar_wait_teardown(&vfull[k % SV], (k / SV) & 1);
         }
@@ -1612,7 +1673,8 @@ __global__ void __launch_bounds__(kVar == 2 ? 256 : 224, 1)
     }
     if (warp == 0 && lane == 0 && *s_abort) {
         // let copies in flight land before the CTA's shared memory is released
-        for (int k = kissued > SK ? kissued - SK : 0; k < kissued; ++k)
+        const int kown = kPaged ? 0 : kissued;   // paged: the page-id warp copies K and V
+        for (int k = kown > SK ? kown - SK : 0; k < kown; ++k)
             mbar_wait_teardown(&kfull[k % SK], (k / SK) & 1);
         for (int k = vissued > SV ? vissued - SV : 0; k < vissued; ++k)
             mbar_wait_teardown(&vfull[k % SV], (k / SV) & 1);

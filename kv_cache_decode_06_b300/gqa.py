@@ -37,7 +37,7 @@ EXPORTS = ("gqa_status_string", "gqa_abi_version", "gqa_decode_workspace_size", 
 # Declared in include/gqa.h under GQA_TEST_HOOKS: exported by the test-hooks build only.
 TEST_HOOK_EXPORTS = ("gqa_debug_withhold_copy",)
 # Declared in include/gqa_bench.h: the measurement helper library (libgqa_b300_bench.so).
-BENCH_EXPORTS = ("gqa_bench_stream_read",)
+BENCH_EXPORTS = ("gqa_bench_stream_read", "gqa_bench_stream_read_pages")
 BENCH_LIB_PATH = os.path.join(_HERE, "libgqa_b300_bench.so")
 NOALLOC_WORKSPACE_BYTES = 8 << 20
 
@@ -128,6 +128,10 @@ def load_bench():
         lib.gqa_bench_stream_read.restype = ctypes.c_int
         lib.gqa_bench_stream_read.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_int,
                                               ctypes.c_void_p, ctypes.c_void_p]
+        lib.gqa_bench_stream_read_pages.restype = ctypes.c_int
+        lib.gqa_bench_stream_read_pages.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_longlong,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         _bench_lib = lib
     return lib
 
@@ -144,6 +148,23 @@ def stream_read(buf: torch.Tensor, flags: torch.Tensor, ctas: int = 0,
     _check(load_bench().gqa_bench_stream_read(buf.data_ptr(), buf.shape[0], buf.shape[1], int(ctas),
                                                flags.data_ptr(), _stream_handle(stream, dev)),
            "gqa_bench_stream_read")
+
+
+def stream_read_pages(buf: torch.Tensor, flags: torch.Tensor, page_rows: int, lanes: int = 1, scatter: bool = True,
+                      one_box: bool = False, warps: int = 1, ctas: int = 0,
+                      stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Read ``buf`` once as pages of ``page_rows`` rows: ``lanes`` issuing lanes in each of
+    ``warps`` warps per block, one or two boxes per page (gqa_bench.h, gqa_bench_stream_read_pages)."""
+    dev = buf.device
+    _require(buf, "buf", torch.bfloat16, dev)
+    if buf.dim() != 3 or buf.shape[2] != 128:
+        raise ValueError("buf must be [z, rows, 128]")
+    _require(flags, "flags", torch.int32, dev)
+    _check(load_bench().gqa_bench_stream_read_pages(buf.data_ptr(), buf.shape[0], buf.shape[1], int(page_rows),
+                                                     int(lanes), 1 if scatter else 0, 1 if one_box else 0,
+                                                     int(warps), int(ctas), flags.data_ptr(),
+                                                     _stream_handle(stream, dev)),
+           "gqa_bench_stream_read_pages")
 
 
 @contextlib.contextmanager
