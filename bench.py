@@ -56,7 +56,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from kv_cache_decode_06_b300.inputs import (  # noqa: E402
-    CONFIGS, MEANPOOL_T5XXL, MEANPOOL_TINY, T5XXL_SWEEP_GS, make_decode_inputs, make_meanpool_input,
+    CONFIGS, MEANPOOL_T5XXL, MEANPOOL_T5XXL_CHECKPOINT, MEANPOOL_TINY, T5XXL_SWEEP_GS, make_decode_inputs, make_meanpool_input,
     make_new_rows, make_paged_layout,
 )
 
@@ -68,15 +68,21 @@ CPU_BASELINE_SECONDS = 10.0   # host time spent on the float64 oracle for the cp
 FALLBACK_HBM_GBS = 6400.0
 
 
+MEANPOOL_DEFAULT = "t5xxl_checkpoint"
+
+
 def meanpool_workload(name: str):
-    """Shape of one mean-pool conversion (one projection of one layer)."""
+    """Shape of one mean-pool conversion call: one projection of one layer ([H, h, d_model]),
+    or a whole checkpoint's K and V projections in one strided call ([outer, H, h * d_model])."""
     if name == "tiny":
         return "meanpool_tiny", dict(MEANPOOL_TINY)
+    if name == "t5xxl_checkpoint":
+        return "meanpool_t5xxl_checkpoint", dict(MEANPOOL_T5XXL_CHECKPOINT)
     if name.startswith("t5xxl_sweep_G"):
         d = dict(MEANPOOL_T5XXL)
         d["G"] = int(name.split("_G")[1])
         return f"meanpool_t5xxl_G{d['G']}", d
-    raise SystemExit(f"--variant meanpool takes --workload tiny or t5xxl_sweep_G<g>, not {name}")
+    raise SystemExit(f"--variant meanpool takes --workload tiny, t5xxl_checkpoint or t5xxl_sweep_G<g>, not {name}")
 
 
 def workload(name: str):
@@ -266,8 +272,9 @@ def run_reference(args, rank: int) -> None:
 def run_reference_meanpool(args) -> None:
     """The fp32 mean-pool oracle as the reference arm: one whole conversion per step."""
     import oracle
-    name, shp = meanpool_workload(args.workload or "t5xxl_sweep_G8")
-    H, G, h, dm = shp["H"], shp["G"], shp["h"], shp["d_model"]
+    name, shp = meanpool_workload(args.workload or MEANPOOL_DEFAULT)
+    H, G, h, dm, outer = shp["H"], shp["G"], shp["h"], shp["d_model"], shp.get("outer", 1)
+    # one projection per step (the checkpoint's projections are independent conversions)
     w_h = make_meanpool_input(H, G, h, dm, shp["config_id"])
     alg = w_h.nbytes + G * h * dm * 4
     for _ in range(args.warmup):
@@ -278,13 +285,15 @@ def run_reference_meanpool(args) -> None:
         oracle.meanpool_f32(w_h, H, G)
         total_t += time.perf_counter() - t
     value = args.steps * alg / total_t / 1e9
+    sample = ("one whole conversion per step, fp32 oracle (one thread)" if outer == 1 else
+              f"one [{H}, {h}, {dm}] projection of the {outer} per step, fp32 oracle (one thread)")
     line = {
         "metric": MEANPOOL_METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
-        "config": {"workload": name, "H": H, "G": G, "h": h, "d_model": dm, "bytes_per_step": alg},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "one whole conversion per step, fp32 oracle (one thread)"},
+        "config": {"workload": name, "H": H, "G": G, "h": h, "d_model": dm, "outer": outer,
+                   "bytes_per_step": alg * outer},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -404,22 +413,26 @@ def block_runner(torch, step, stream, K, period):
 
 
 def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
-    """Times gqa_meanpool_kv: [H, h, d_model] fp32 -> [G, h, d_model] fp32, one call per step."""
-    name, shp = meanpool_workload(args.workload or "t5xxl_sweep_G8")
-    H, G, h, dm = shp["H"], shp["G"], shp["h"], shp["d_model"]
-    w_h = make_meanpool_input(H, G, h, dm, shp["config_id"])
-    in_bytes, out_bytes = w_h.nbytes, G * h * dm * 4
+    """Times the mean-pool conversion, one call per step: one projection [H, h, d_model] fp32 ->
+    [G, h, d_model] (gqa_meanpool_kv), or a whole checkpoint [outer, H, h*d_model] ->
+    [outer, G, h*d_model] in one strided call (gqa_meanpool_kv_strided)."""
+    name, shp = meanpool_workload(args.workload or MEANPOOL_DEFAULT)
+    H, G, h, dm, outer = shp["H"], shp["G"], shp["h"], shp["d_model"], shp.get("outer", 1)
+    w_h = make_meanpool_input(H, G, h, dm, shp["config_id"], outer=outer)
+    in_bytes, out_bytes = w_h.nbytes, outer * G * h * dm * 4
     alg = in_bytes + out_bytes                  # each input read once, each output written once
+    out_shape = (G, h, dm) if outer == 1 else (outer, G, h * dm)
     stream = torch.cuda.Stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    copies = max(3, math.ceil(L2_COPIES_SPAN * l2 / alg) + 1)
+    copies = 2 if alg > 8 * l2 else max(3, math.ceil(L2_COPIES_SPAN * l2 / alg) + 1)
     w = torch.from_numpy(w_h).to(dev)
     ws = [w] + [w.clone() for _ in range(copies - 1)]
-    outs = [torch.empty((G, h, dm), dtype=torch.float32, device=dev) for _ in range(copies)]
+    outs = [torch.empty(out_shape, dtype=torch.float32, device=dev) for _ in range(copies)]
+    convert = gqa.meanpool_kv if outer == 1 else gqa.meanpool_kv_strided
 
     def step(i):
         c = i % copies
-        gqa.meanpool_kv(ws[c], G, out=outs[c], stream=torch.cuda.current_stream(dev))
+        convert(ws[c], G, out=outs[c], stream=torch.cuda.current_stream(dev))
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -431,14 +444,17 @@ def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
                                                 local_rank)
     ms_per_step = med_ms / args.steps
     value = whole_job_gbs(alg, args.steps, world, med_ms)
+    del ws[1:]
+    torch.cuda.empty_cache()
 
     hw = torch.from_numpy(w_h).pin_memory()
-    hout = torch.empty((G, h, dm), dtype=torch.float32).pin_memory()
+    hout = torch.empty(out_shape, dtype=torch.float32).pin_memory()
     cur = torch.cuda.current_stream(dev)
+    e2e_steps = args.e2e_steps if in_bytes < (1 << 30) else min(args.e2e_steps, 3)
 
     def e2e_step():
         w.copy_(hw, non_blocking=True)
-        gqa.meanpool_kv(w, G, out=outs[0], stream=cur)
+        convert(w, G, out=outs[0], stream=cur)
         hout.copy_(outs[0], non_blocking=True)
 
     for _ in range(3):
@@ -447,11 +463,11 @@ def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(cur)
-    for _ in range(args.e2e_steps):
+    for _ in range(e2e_steps):
         e2e_step()
     e1.record(cur)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     if rank != 0:
         return
 
@@ -460,23 +476,28 @@ def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
     cpu = None
     if not args.no_cpu_baseline:
         import oracle
-        oracle.meanpool_f32(w_h, H, G)               # warm: page faults
+        one = w_h if outer == 1 else w_h[0].reshape(H, h, dm)   # one projection: a bounded sample
+        one_bytes = one.nbytes + G * h * dm * 4
+        oracle.meanpool_f32(one, H, G)               # warm: page faults
         total_t, passes = 0.0, 0
         while total_t < CPU_BASELINE_SECONDS / 4 and passes < 10000:
             t = time.perf_counter()
-            oracle.meanpool_f32(w_h, H, G)
+            oracle.meanpool_f32(one, H, G)
             total_t += time.perf_counter() - t
             passes += 1
-        cpu = {"value": passes * alg / total_t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{passes} whole conversion(s) of the same projection, fp32 oracle (one thread), "
-                         f"{total_t:.1f} s after one warm-up pass"}
+        cpu = {"value": passes * one_bytes / total_t / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{passes} conversion(s) of one [{H}, {h}, {dm}] projection"
+                         + ("" if outer == 1 else f" (of the {outer})")
+                         + f", fp32 oracle (one thread), {total_t:.1f} s after one warm-up pass"}
+    layout = ("[H, h, d_model] -> [G, h, d_model] fp32, head-major" if outer == 1 else
+              f"[{outer}, H, h*d_model] -> [{outer}, G, h*d_model] fp32: every K and V projection of the "
+              f"checkpoint in one strided call")
     line = {
         "metric": MEANPOOL_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": name, "H": H, "G": G, "h": h, "d_model": dm,
-                   "layout": "[H, h, d_model] -> [G, h, d_model] fp32, head-major",
-                   "bytes_per_step": alg, "inputs": "N(0,1) float32, seeded",
+        "config": {"workload": name, "H": H, "G": G, "h": h, "d_model": dm, "outer": outer,
+                   "layout": layout, "bytes_per_step": alg, "inputs": "N(0,1) float32, seeded",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU", "copies": copies,
                    "l2": f"inputs larger than L2: {copies} input/output copies, step i uses copy i % {copies}"
                          if copies * alg > l2 else "fits in L2: launch-bound, not an HBM figure",
@@ -488,8 +509,8 @@ def run_meanpool(args, world, rank, local_rank, dev, torch, dist, gqa) -> None:
                      "algorithmic_bytes_per_launch": alg, "frac_of_8TBps_nominal": achieved / 8000.0},
         "cpu_baseline": cpu,
         "e2e": {"value": alg / (e2e_ms / 1e3) / 1e9 * world, "unit": UNIT, "h2d_bytes_per_step": in_bytes,
-                "d2h_bytes_per_step": out_bytes, "steps": args.e2e_steps,
-                "what": "H2D of the projection from pinned host memory + the conversion + D2H of the result"},
+                "d2h_bytes_per_step": out_bytes, "steps": e2e_steps,
+                "what": "H2D of the projections from pinned host memory + the conversion + D2H of the result"},
         "timing": block_stats(blocks, R, args.steps),
         "gpu_launches": args.steps * R,
         "clocks": clocks,
@@ -774,7 +795,7 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=None,
                     help="llama3_70b (default) | mistral7b | long_ragged | tiny | t5xxl_sweep_G<1..64>; "
-                         "--variant meanpool: tiny | t5xxl_sweep_G<g> (default t5xxl_sweep_G8)")
+                         "--variant meanpool: t5xxl_checkpoint (default) | tiny | t5xxl_sweep_G<g>")
     ap.add_argument("--secondary", default="mistral7b",
                     help="a second workload measured in the same run and reported in the line's 'secondary' "
                          "object (contiguous cache only; 'none' to skip)")

@@ -45,18 +45,24 @@ __device__ __forceinline__ T fold_heads(const T *__restrict__ src, long long str
     return acc;
 }
 
+// Each block converts one contiguous span of the outputs, blockDim.x at a time;
+// a thread's place (o, g, x) advances by additions only (no division in the loop).
 template <typename T>
-__global__ void __launch_bounds__(256) meanpool_kernel(const T *__restrict__ w, T *__restrict__ out,
+__global__ void __launch_bounds__(256, 4) meanpool_kernel(const T *__restrict__ w, T *__restrict__ out,
                                                        long long outer, int H, int G, long long inner) {
     const int n = H / G;
     const float fn = (float)n;
     const long long total = outer * G * inner;
-    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
-         e += (long long)gridDim.x * blockDim.x) {
-        const long long x = e % inner;
-        const long long og = e / inner;
-        const int g = (int)(og % G);
-        const long long o = og / G;
+    const long long per = (total + gridDim.x - 1) / gridDim.x;
+    const long long begin = blockIdx.x * per;
+    const long long end = begin + per < total ? begin + per : total;
+    long long e = begin + threadIdx.x;
+    if (e >= end) return;
+    long long og = e / inner, x = e - og * inner;
+    int g = (int)(og % G);
+    long long o = og / G;
+    const int step = blockDim.x;
+    for (; e < end; e += step) {
         T acc = fold_heads(w + ((o * H + (long long)g * n) * inner + x), inner, n);
         if constexpr (sizeof(T) == 16)
             acc = make_float4(__fdiv_rn(acc.x, fn), __fdiv_rn(acc.y, fn), __fdiv_rn(acc.z, fn),
@@ -64,6 +70,14 @@ __global__ void __launch_bounds__(256) meanpool_kernel(const T *__restrict__ w, 
         else
             acc = __fdiv_rn(acc, fn);
         out[e] = acc;
+        x += step;
+        while (x >= inner) {
+            x -= inner;
+            if (++g == G) {
+                g = 0;
+                ++o;
+            }
+        }
     }
 }
 

@@ -98,6 +98,11 @@ MEANPOOL_TINY = dict(H=8, G=2, h=64, d_model=512, config_id=0)
 # 64 over a 4096-wide model (64 MiB fp32), pooled to G groups (G = 8 in the
 # GQA paper's main setting).
 MEANPOOL_T5XXL = dict(H=64, G=8, h=64, d_model=4096, config_id=2)
+# A whole checkpoint in one call: every K and V projection of a T5-XXL-shaped
+# encoder-decoder (24 encoder layers with self-attention, 24 decoder layers with
+# self- and cross-attention: 72 attention blocks x {K, V} = 144 projections of
+# [64, 64, 4096]), as [outer = 144, H, h * d_model] fp32, 9.66 GB, pooled to G = 8.
+MEANPOOL_T5XXL_CHECKPOINT = dict(H=64, G=8, h=64, d_model=4096, config_id=3, outer=144)
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:

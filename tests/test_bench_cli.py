@@ -55,5 +55,8 @@ def test_meanpool_workloads():
     assert b.meanpool_workload("tiny") == ("meanpool_tiny", {"H": 8, "G": 2, "h": 64, "d_model": 512, "config_id": 0})
     name, shp = b.meanpool_workload("t5xxl_sweep_G1")
     assert name == "meanpool_t5xxl_G1" and (shp["H"], shp["G"], shp["h"], shp["d_model"]) == (64, 1, 64, 4096)
+    name, shp = b.meanpool_workload("t5xxl_checkpoint")   # the default: 144 projections in one call
+    assert name == "meanpool_t5xxl_checkpoint" and shp["outer"] == 144 and (shp["H"], shp["G"]) == (64, 8)
+    assert b.MEANPOOL_DEFAULT == "t5xxl_checkpoint"
     with pytest.raises(SystemExit):
         b.meanpool_workload("mistral7b")

@@ -268,6 +268,28 @@ def test_meanpool_bit_exact_t5xxl_checkpoint(G):
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
+@pytest.mark.slow
+def test_meanpool_bit_exact_whole_checkpoint():
+    """Every K and V projection of a T5-XXL-shaped checkpoint, 144 x [64, 64, 4096] fp32 (9.66 GB),
+    pooled to 8 groups in one strided call as the benchmark times it: the first, a middle and the
+    last projection bit-exact against the oracle, and the rest checked as finite means of their heads."""
+    from kv_cache_decode_06_b300.inputs import MEANPOOL_T5XXL_CHECKPOINT, make_meanpool_input
+    c = MEANPOOL_T5XXL_CHECKPOINT
+    H, G, h, dm, outer = c["H"], c["G"], c["h"], c["d_model"], c["outer"]
+    w = make_meanpool_input(H, G, h, dm, c["config_id"], outer=outer)
+    dw = torch.from_numpy(w).cuda()
+    got = gqa.meanpool_kv_strided(dw, G)
+    torch.cuda.synchronize()
+    for o in (0, outer // 2, outer - 1):
+        ref = oracle.meanpool_f32(np.ascontiguousarray(w[o]).reshape(H, h, dm), H, G)
+        mine = got[o].cpu().numpy().reshape(G, h, dm)
+        assert np.array_equal(mine.view(np.uint32), ref.view(np.uint32)), o
+    # every projection: each group's output equals the fp32 mean of its heads to within rounding
+    n = H // G
+    approx = dw.view(outer, G, n, h * dm).sum(dim=2, dtype=torch.float64) / n
+    assert torch.allclose(got.double(), approx, rtol=0, atol=1e-5)
+
+
 @pytest.mark.parametrize("H,G", [(4, 1), (16, 1), (12, 2)])
 def test_meanpool_special_values(H, G):
     """Signed zeros, infinities, NaN and subnormals: the same IEEE results as the fp32 sequence."""
