@@ -88,8 +88,10 @@ def _paged_inputs(shape, page_size, lens, seed, cid):
 
 
 # page sizes are powers of two, so Lmax is even: d = 64 is paired up to H/G = 16 and
-# unpaired above (the last shape, H/G = 32)
-PAGED_SHAPES = SHAPES[:3] + [(2, 64, 2, 64, 500), (2, 64, 1, 64, 500)]
+# unpaired above (H/G = 32, 64); d = 128 at H/G = 4, 16, 32 and 64 takes every softmax
+# form of the paged instances, whose tiles use the page-interleaved shared-memory layout
+PAGED_SHAPES = SHAPES[:3] + [(2, 64, 2, 64, 500), (2, 64, 1, 64, 500), (2, 64, 4, 128, 600),
+                             (2, 64, 2, 128, 500), (1, 64, 1, 128, 700)]
 
 
 @pytest.mark.parametrize("page_size", [16, 32, 64, 128, 256, 1024])
@@ -179,8 +181,8 @@ def test_fused_append(shape):
 
 
 @pytest.mark.parametrize("page_size", [16, 128, 512])
-def test_paged_fused_append(page_size):
-    shape = (3, 32, 8, 128, 1000)
+@pytest.mark.parametrize("shape", [(3, 32, 8, 128, 1000), (3, 16, 4, 64, 1000)], ids=["d128", "d64paired"])
+def test_paged_fused_append(page_size, shape):
     cfg, inp, kp, vp, table = _paged_inputs(shape, page_size, [1000, 1, 300], seed=9, cid=66)
     kn, vn = _new_rows(cfg, 4)
     k_ref = oracle.append_row(inp.k, kn, inp.seq_lens)
