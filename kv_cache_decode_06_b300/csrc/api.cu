@@ -220,6 +220,7 @@ struct DecodeRequest {
     float scale = 0.f;
     void *stream = nullptr;
     const gqa_decode_options *opts = nullptr;
+    bool own_ws = false;   // the workspace is the library's own scratch, checked by its owner
 };
 
 // The score scale a call uses: the caller's value, or 1/sqrt(d) for
@@ -246,7 +247,8 @@ gqa_status validate(const DecodeRequest &r, int *path_out, DeviceInfo *dev_out) 
         if (x != 0) return GQA_ERR_INVALID_ARG;
     if (o.num_ctas < 0 || o.num_ctas > GQA_MAX_CTAS) return GQA_ERR_INVALID_ARG;
     if (o.path < 0 || o.path > GQA_PATH_TCGEN05 || o.window < 0) return GQA_ERR_INVALID_ARG;
-    if (!r.ws || !aligned(r.ws, 256) || r.ws_bytes < workspace_bytes_for(B, H, G, d, Lmax)) return GQA_ERR_WORKSPACE;
+    if (!r.own_ws && (!r.ws || !aligned(r.ws, 256) || r.ws_bytes < workspace_bytes_for(B, H, G, d, Lmax)))
+        return GQA_ERR_WORKSPACE;
 
     const int n = H / G;
     const int path = o.path ? o.path : auto_path(H, G, d);
@@ -362,6 +364,7 @@ gqa_status decode_check(const void *q, const void *k_cache, const void *v_cache,
     r.out = out;
     r.ws = workspace;
     r.ws_bytes = workspace_bytes;
+    r.own_ws = workspace == nullptr;
     r.B = B, r.H = H, r.G = G, r.d = d, r.Lmax = Lmax;
     r.scale = scale;
     int path = 0;

@@ -58,7 +58,8 @@ size_t decode_workspace_zero_prefix(int B, int G);
 
 // Every host-side check gqa_decode makes (arguments, workspace, path, device),
 // without enqueueing anything: the status gqa_decode would return before its
-// first launch.
+// first launch.  workspace null: the checks of the workspace are skipped (a
+// scratch the library owns, whose size and alignment its owner checks).
 gqa_status decode_check(const void *q, const void *k_cache, const void *v_cache, const int32_t *seq_lens,
                         float *out, void *workspace, size_t workspace_bytes, int B, int H, int G, int d, int Lmax,
                         float scale);

@@ -66,16 +66,17 @@ extern "C" gqa_status gqa_decode_noalloc(const void *q, const void *k_cache, con
     const gqa_status s = gqa_decode_workspace_size(B, H, G, d, Lmax, &need);
     if (s != GQA_OK) return s;
     if (need > kScratchBytes) return GQA_ERR_WORKSPACE;   // this shape needs more scratch than the library holds
-    void *ws = nullptr;
-    const gqa_status a = scratch_address(&ws);
-    if (a != GQA_OK) return a;
     // Every host-side check of gqa_decode (pointer alignment, scale, path and
     // head limits, device) runs before anything is enqueued: a rejected call
     // leaves the stream, and the scratch that a call on another stream may be
-    // using, untouched.
-    const gqa_status c = gqa::decode_check(q, k_cache, v_cache, seq_lens, out, ws, kScratchBytes, B, H, G, d, Lmax,
-                                           scale);
+    // using, untouched.  The scratch itself (256-byte aligned, kScratchBytes
+    // long, checked against `need` above) is not a caller's workspace to check.
+    const gqa_status c = gqa::decode_check(q, k_cache, v_cache, seq_lens, out, nullptr, kScratchBytes, B, H, G, d,
+                                           Lmax, scale);
     if (c != GQA_OK) return c;
+    void *ws = nullptr;
+    const gqa_status a = scratch_address(&ws);
+    if (a != GQA_OK) return a;
     // Clear the scratch's whole header every time, on the caller's stream: the
     // flag word, so that a flag left by an earlier call does not stay set, and
     // the dynamic-pool ticket and failed-claim count.  A call that ran into a

@@ -278,3 +278,21 @@ def test_binding_rejects_host_tensors():
     with pytest.raises(ValueError, match="CUDA tensor"):
         gqa.decode(q, kv, kv, torch.full((1,), 128, dtype=torch.int32))
 
+
+
+def test_noalloc_rejects_bad_arguments_before_queueing(gqa_lib):
+    """gqa_decode_noalloc runs every host-side check before it clears its scratch header, so a
+    misaligned pointer or a non-finite scale returns GQA_ERR_INVALID_ARG with nothing queued."""
+    shape = (2, 8, 2, 64, 256)
+
+    def call(q=FAKE, k=FAKE, v=FAKE, sl=FAKE, out=FAKE, scale=0.125):
+        return gqa_lib.gqa_decode_noalloc(q, k, v, sl, out, *shape, scale, None)
+
+    assert call(q=FAKE + 2) == 1
+    assert call(k=FAKE + 8) == 1
+    assert call(v=FAKE + 8) == 1
+    assert call(out=FAKE + 4) == 1
+    assert call(sl=FAKE + 2) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(scale=float("inf")) == 1
+    assert call(scale=float("-inf")) == 1
