@@ -245,18 +245,30 @@ def _sample_rows(cfg, every=37):
     return np.arange(0, cfg.B * cfg.H, every, dtype=np.int64)
 
 
+_MISTRAL = {}
+
+
+def _mistral7b_and_oracle():
+    """The Mistral-7B-shaped inputs and their float64 oracle output, computed once per session."""
+    if not _MISTRAL:
+        inp = make_decode_inputs(CONFIGS["mistral7b"])
+        _MISTRAL["inp"] = inp
+        _MISTRAL["ref"] = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale)
+    return _MISTRAL["inp"], _MISTRAL["ref"]
+
+
 @pytest.mark.slow
-def test_paged_mistral7b_full():
-    """The Mistral-7B-shaped step on a paged cache of 64-position pages in random pool order, every row."""
-    cfg = CONFIGS["mistral7b"]
-    inp = make_decode_inputs(cfg)
-    kp, vp, table = make_paged_layout(inp, 64)
+@pytest.mark.parametrize("page_size", [16, 32, 64])
+def test_paged_mistral7b_full(page_size):
+    """The Mistral-7B-shaped step on a paged cache in random pool order, every row, at the page
+    sizes the benchmark measures (one box per page, the page-interleaved tile layout)."""
+    inp, ref = _mistral7b_and_oracle()
+    kp, vp, table = make_paged_layout(inp, page_size)
     q = torch.from_numpy(inp.q).view(torch.bfloat16).cuda()
     got = gqa.decode_paged(q, _dev(kp).view(torch.bfloat16), _dev(vp).view(torch.bfloat16), _dev(table),
                            _dev(inp.seq_lens), scale=float(inp.scale))
     torch.cuda.synchronize()
-    ref = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale)
-    check_close(got.cpu().numpy(), ref, what="paged mistral7b")
+    check_close(got.cpu().numpy(), ref, what=f"paged mistral7b ps={page_size}")
 
 
 @pytest.mark.slow
