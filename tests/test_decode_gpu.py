@@ -76,6 +76,10 @@ SMALL = [
     (3, 128, 2, 64, 300, [300, 1, 64]),
     (2, 40, 1, 64, 200, [200, 77]),        # 40 heads: padded to 64
     (2, 64, 1, 128, 300, [300, 129]),      # 64 heads at d = 128
+    # the largest batch (32 sequences per lane of the prefix warp), and a batch too large for
+    # T_b to sit beside the tile prefix in shared memory (B > 512)
+    (1024, 8, 2, 64, 130, [(37 * i) % 131 for i in range(1024)]),
+    (600, 16, 4, 128, 200, [(53 * i + 7) % 201 for i in range(600)]),
 ]
 
 

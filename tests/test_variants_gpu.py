@@ -122,6 +122,20 @@ def test_paged_cache(shape, page_size):
     assert gqa.read_flags(ws) == 0
 
 
+@pytest.mark.parametrize("page_size", [16, 128])
+def test_paged_large_batch(page_size):
+    """B = 600: T_b does not fit beside the tile prefix, so the page-id warp reads it from seq_lens."""
+    shape = (600, 16, 4, 128, 256)
+    lens = [(29 * i + 3) % 257 for i in range(600)]
+    cfg, inp, kp, vp, table = _paged_inputs(shape, page_size, lens, seed=page_size + 1, cid=68)
+    q = torch.from_numpy(inp.q).view(torch.bfloat16).cuda()
+    kd, vd, td = _dev(kp).view(torch.bfloat16), _dev(vp).view(torch.bfloat16), _dev(table)
+    got = gqa.decode_paged(q, kd, vd, td, _dev(inp.seq_lens), scale=float(inp.scale))
+    torch.cuda.synchronize()
+    ref = oracle.gqa_decode_f64(inp.q, inp.k, inp.v, inp.seq_lens, inp.scale)
+    check_close(got.cpu().numpy(), ref, what=f"paged B=600 ps={page_size}")
+
+
 def test_paged_cross_attention_and_bad_page_flag():
     shape = (2, 16, 4, 128, 640)
     cfg, inp, kp, vp, table = _paged_inputs(shape, 64, [640, 640], seed=5, cid=64)
